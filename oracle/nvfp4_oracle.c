@@ -1,0 +1,340 @@
+/*
+ * nvfp4_oracle.c -- plain, slow CPU oracle for the NVFP4 linear-layer path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may include, link,
+ * load or call this file: only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg use it.  It shares no code, header, table or
+ * constant with the CUDA library; every value below is derived from the
+ * format definitions written out in this file.
+ *
+ * Sources (the method is described on web pages about the SOAR 2026
+ * inference contest):
+ *   [P1] "SOAR 2026 Recap: From Compute Limits to the Open-Source Ecosystem",
+ *        section "1. Quantization and GEMM dispatch": linear weights are
+ *        stored as NVFP4 (FP4 E2M1, half a byte per element); each block
+ *        picks between scale=4 and scale=6; GEMMs run W4A16 for M <= 48 and
+ *        W4A4 (native NVFP4 MMA) above.
+ *   [P3] "SOAR Weekly Champion Notes 07 ... NVFP4 Quantization Improvements",
+ *        section "01 Background": the E2M1 value set {0, +-0.5, +-1, +-1.5,
+ *        +-2, +-3, +-4, +-6}, maximum 6, standard blocks normalised to
+ *        [-6, 6] (M=6);
+ *        section "02 FourOverSix": the M=4 scale is the M=6 scale times 1.5,
+ *        re-rounded to FP8; each block keeps the scale whose block mean
+ *        squared dequantisation error is smaller (strictly smaller for M=4);
+ *        the output stays standard NVFP4 (4-bit codes + FP8 block scale).
+ *
+ * Where the pages are silent this file takes the following readings (the
+ * CUDA path takes the same ones):
+ *   - 16-element blocks along K, E4M3 block scales, one FP32 tensor scale
+ *     ts = amax(|W|) / D with D = 6 * 448 by default; an all-zero tensor
+ *     gets ts = 1.
+ *   - Every step of the quantiser is IEEE binary32 with round-to-nearest-even
+ *     and no fused multiply-add (build with -ffp-contract=off):
+ *       r6  = (amax_block / 6) / ts,      s6 = E4M3(r6)
+ *       s4  = E4M3(value(s6) * 1.5)
+ *       eff = value(s) * ts
+ *       q_i = E2M1(x_i / eff)   (q_i = signed zero when eff == 0)
+ *       e_i = (x_i - value(q_i) * eff)^2
+ *       SSE = ((e_j + e_j+8) pairwise, then +4, +2, +1)  -- a fixed tree
+ *     and the block keeps s4 iff SSE4 < SSE6 (ties keep M=6).  Comparing
+ *     sums is the same as comparing means: division by 16 is exact.
+ *   - E4M3 and E2M1 conversions round to nearest, ties to the even code, and
+ *     saturate to the largest finite value (448 and 6).  The sign of a code
+ *     is the sign of x (so negative values that round to zero give -0).
+ *   - Code packing: element 2j in the low nibble of byte j, 2j+1 in the high.
+ *   - Activations (W4A4 path) use the standard M=6 rule only.
+ *   - GEMM reference: the plain definition, sum_k x[m,k] * w_hat[n,k] in
+ *     binary64, with w_hat = value(code) * value(scale) * ts (exact).
+ *
+ * parity pinned: see the test suite (format tables against a third-party
+ * library, worked examples computed by hand, brute-force scale search,
+ * invariants).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stddef.h>
+#include <string.h>
+
+#define OR_OK 0
+#define OR_ERR_SHAPE 2
+#define OR_ERR_NONFINITE 5
+
+/* ------------------------------------------------------------------------ */
+/* Formats                                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* bfloat16: the upper 16 bits of an IEEE binary32. */
+float oracle_bf16_value(uint16_t bits) {
+  uint32_t u = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* FP4 E2M1: 1 sign bit, 2 exponent bits (bias 1), 1 mantissa bit, no
+ * infinities or NaN.  Exponent field 0 is subnormal: 0.m * 2^0. */
+double oracle_e2m1_value(uint8_t code) {
+  int s = (code >> 3) & 1;
+  int e = (code >> 1) & 3;
+  int m = code & 1;
+  double mag = (e == 0) ? (m * 0.5) : ldexp(1.0 + 0.5 * m, e - 1);
+  return s ? -mag : mag;
+}
+
+/* FP8 E4M3 (the "fn" variant): 1 sign, 4 exponent bits (bias 7), 3 mantissa
+ * bits; exponent field 0 is subnormal (0.mmm * 2^-6); S.1111.111 is NaN and
+ * there is no infinity, so the largest finite magnitude is 1.75 * 2^8 = 448. */
+double oracle_e4m3_value(uint8_t byte) {
+  int s = (byte >> 7) & 1;
+  int e = (byte >> 3) & 15;
+  int m = byte & 7;
+  double mag;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) mag = ldexp(m / 8.0, -6);
+  else mag = ldexp(1.0 + m / 8.0, e - 7);
+  return s ? -mag : mag;
+}
+
+/* Round |v| to the nearest E2M1 magnitude (ties to the even code), saturate
+ * at 6, and attach the sign of v.  Written as a search over the 8
+ * magnitudes so that it reads as the definition of rounding to nearest. */
+uint8_t oracle_e2m1_encode(float v) {
+  uint8_t sign = signbit(v) ? 8 : 0;
+  double a = fabs((double)v);
+  if (a >= 6.0) return sign | 7; /* also catches +inf */
+  int best = 0;
+  double best_d = a;
+  for (int m = 1; m < 8; ++m) {
+    double d = fabs(a - oracle_e2m1_value((uint8_t)m));
+    if (d < best_d || (d == best_d && (m & 1) == 0)) {
+      best = m;
+      best_d = d;
+    }
+  }
+  return sign | (uint8_t)best;
+}
+
+/* Round |v| to the nearest finite E4M3 magnitude (ties to the even code),
+ * saturating at 448, sign from v.  Search over the 127 finite magnitudes. */
+uint8_t oracle_e4m3_encode(float v) {
+  uint8_t sign = signbit(v) ? 0x80 : 0;
+  double a = fabs((double)v);
+  if (a >= 448.0) return sign | 0x7E;
+  int best = 0;
+  double best_d = a;
+  for (int c = 1; c < 127; ++c) {
+    double d = fabs(a - oracle_e4m3_value((uint8_t)c));
+    if (d < best_d || (d == best_d && (c & 1) == 0)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  return sign | (uint8_t)best;
+}
+
+/* ------------------------------------------------------------------------ */
+/* One 16-element block, quantised with a given scale byte.                 */
+/* ------------------------------------------------------------------------ */
+
+/* Quantise 16 values with block scale byte s and tensor scale ts; return the
+ * block's sum of squared dequantisation errors in the fixed binary32 tree
+ * order.  q receives one code per element. */
+float oracle_block_sse(const float x[16], uint8_t s, float ts, uint8_t q[16]) {
+  float eff = (float)oracle_e4m3_value(s) * ts;
+  float e[16];
+  for (int i = 0; i < 16; ++i) {
+    float xhat;
+    if (eff == 0.0f) {
+      q[i] = signbit(x[i]) ? 8 : 0;
+      xhat = 0.0f;
+    } else {
+      float r = x[i] / eff;
+      q[i] = oracle_e2m1_encode(r);
+      xhat = (float)oracle_e2m1_value(q[i]) * eff;
+    }
+    float d = x[i] - xhat;
+    e[i] = d * d;
+  }
+  float a[8], b[4], c[2];
+  for (int j = 0; j < 8; ++j) a[j] = e[j] + e[j + 8];
+  for (int j = 0; j < 4; ++j) b[j] = a[j] + a[j + 4];
+  for (int j = 0; j < 2; ++j) c[j] = b[j] + b[j + 2];
+  return c[0] + c[1];
+}
+
+/* The standard (M=6) scale of a block: E4M3((amax_block / 6) / ts). */
+uint8_t oracle_block_scale_m6(const float x[16], float ts) {
+  float amax = 0.0f;
+  for (int i = 0; i < 16; ++i) {
+    float a = fabsf(x[i]);
+    if (a > amax) amax = a;
+  }
+  float r6 = (amax / 6.0f) / ts;
+  return oracle_e4m3_encode(r6);
+}
+
+/* FourOverSix on one block.  Outputs: q (chosen codes), the chosen scale byte,
+ * the choice (1 = M4), and both candidates' scale bytes and SSEs. */
+void oracle_fos_block(const float x[16], float ts, uint8_t q[16], uint8_t* scale,
+                      uint8_t* choice, uint8_t* s6_out, uint8_t* s4_out,
+                      float* sse6_out, float* sse4_out) {
+  uint8_t s6 = oracle_block_scale_m6(x, ts);
+  float s6v = (float)oracle_e4m3_value(s6);
+  uint8_t s4 = oracle_e4m3_encode(s6v * 1.5f);
+  uint8_t q6[16], q4[16];
+  float sse6 = oracle_block_sse(x, s6, ts, q6);
+  float sse4 = oracle_block_sse(x, s4, ts, q4);
+  int m4 = sse4 < sse6;
+  memcpy(q, m4 ? q4 : q6, 16);
+  *scale = m4 ? s4 : s6;
+  *choice = (uint8_t)m4;
+  if (s6_out) *s6_out = s6;
+  if (s4_out) *s4_out = s4;
+  if (sse6_out) *sse6_out = sse6;
+  if (sse4_out) *sse4_out = sse4;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Whole tensors                                                             */
+/* ------------------------------------------------------------------------ */
+
+/* Tensor scale: amax(|X|) / divisor, or 1 for an all-zero tensor.  Returns
+ * OR_ERR_NONFINITE if any element is Inf or NaN. */
+int oracle_tensor_scale(const uint16_t* X, int64_t count, float divisor, float* ts) {
+  float amax = 0.0f;
+  for (int64_t i = 0; i < count; ++i) {
+    float v = oracle_bf16_value(X[i]);
+    if (!isfinite(v)) return OR_ERR_NONFINITE;
+    float a = fabsf(v);
+    if (a > amax) amax = a;
+  }
+  *ts = (amax == 0.0f) ? 1.0f : amax / divisor;
+  return OR_OK;
+}
+
+static void pack_codes(const uint8_t q[16], uint8_t* out8) {
+  for (int j = 0; j < 8; ++j) out8[j] = (uint8_t)((q[2 * j] & 15) | ((q[2 * j + 1] & 15) << 4));
+}
+
+/* FourOverSix NVFP4 weight quantisation of W [N, K] (bf16 bits, row-major).
+ * codes [N, K/2], scales [N, K/16] (E4M3 bytes, row-major), choice [N, K/16]
+ * (nullable, 1 = M4), m4_count (nullable). */
+int oracle_quantize_fos(const uint16_t* W, int64_t N, int64_t K, float divisor,
+                        uint8_t* codes, uint8_t* scales, uint8_t* choice,
+                        float* ts_out, uint64_t* m4_count) {
+  if (N <= 0 || K <= 0 || K % 16 != 0) return OR_ERR_SHAPE;
+  float ts;
+  int st = oracle_tensor_scale(W, N * K, divisor, &ts);
+  if (st != OR_OK) return st;
+  *ts_out = ts;
+  uint64_t count = 0;
+  int64_t nb = K / 16;
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t b = 0; b < nb; ++b) {
+      float x[16];
+      for (int i = 0; i < 16; ++i) x[i] = oracle_bf16_value(W[n * K + b * 16 + i]);
+      uint8_t q[16], s, c;
+      oracle_fos_block(x, ts, q, &s, &c, NULL, NULL, NULL, NULL);
+      pack_codes(q, codes + n * (K / 2) + b * 8);
+      scales[n * nb + b] = s;
+      if (choice) choice[n * nb + b] = c;
+      count += c;
+    }
+  }
+  if (m4_count) *m4_count = count;
+  return OR_OK;
+}
+
+/* Standard (M=6 only) NVFP4 quantisation of activations X [M, K]. */
+int oracle_quantize_act(const uint16_t* X, int64_t M, int64_t K, float divisor,
+                        uint8_t* codes, uint8_t* scales, float* ts_out) {
+  if (M <= 0 || K <= 0 || K % 16 != 0) return OR_ERR_SHAPE;
+  float ts;
+  int st = oracle_tensor_scale(X, M * K, divisor, &ts);
+  if (st != OR_OK) return st;
+  *ts_out = ts;
+  int64_t nb = K / 16;
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t b = 0; b < nb; ++b) {
+      float x[16];
+      for (int i = 0; i < 16; ++i) x[i] = oracle_bf16_value(X[m * K + b * 16 + i]);
+      uint8_t q[16];
+      uint8_t s = oracle_block_scale_m6(x, ts);
+      (void)oracle_block_sse(x, s, ts, q);
+      pack_codes(q, codes + m * (K / 2) + b * 8);
+      scales[m * nb + b] = s;
+    }
+  }
+  return OR_OK;
+}
+
+/* Block-scaled tensor-core scale layout.  The scale matrix [R, K/16] is cut
+ * into tiles of 128 rows x 4 scale columns (zero-padded at the edges); tiles
+ * are stored row-tile-major, each as 512 bytes in which scale (r, c) of the
+ * tile sits at byte (r mod 32) * 16 + (r div 32) * 4 + c. */
+int64_t oracle_scales_mma_bytes(int64_t R, int64_t K) {
+  int64_t rt = (R + 127) / 128;
+  int64_t ct = (K / 16 + 3) / 4;
+  return rt * ct * 512;
+}
+
+void oracle_scales_to_mma(const uint8_t* scales, int64_t R, int64_t K, uint8_t* out) {
+  int64_t nb = K / 16;
+  int64_t ct = (nb + 3) / 4;
+  memset(out, 0, (size_t)oracle_scales_mma_bytes(R, K));
+  for (int64_t r = 0; r < R; ++r) {
+    for (int64_t c = 0; c < nb; ++c) {
+      int64_t tile = (r / 128) * ct + (c / 4);
+      int64_t rr = r % 128, cc = c % 4;
+      out[tile * 512 + (rr % 32) * 16 + (rr / 32) * 4 + cc] = scales[r * nb + c];
+    }
+  }
+}
+
+/* Dequantised element (n, k) of an NVFP4 matrix, exact in binary64. */
+static double dequant(const uint8_t* codes, const uint8_t* scales, float ts, int64_t K,
+                      int64_t n, int64_t k) {
+  uint8_t byte = codes[n * (K / 2) + k / 2];
+  uint8_t code = (k & 1) ? (byte >> 4) : (byte & 15);
+  return oracle_e2m1_value(code) * oracle_e4m3_value(scales[n * (K / 16) + k / 16]) * (double)ts;
+}
+
+/* W4A16: Y[m, n] = sum_k X[m, k] * w_hat[n, k] in binary64. */
+int oracle_gemm_w4a16(const uint16_t* X, int64_t M, int64_t K, const uint8_t* codes,
+                      const uint8_t* scales, float ts, int64_t N, double* Y) {
+  if (M < 0 || N <= 0 || K <= 0 || K % 16 != 0) return OR_ERR_SHAPE;
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; ++k)
+        acc += (double)oracle_bf16_value(X[m * K + k]) * dequant(codes, scales, ts, K, n, k);
+      Y[m * N + n] = acc;
+    }
+  return OR_OK;
+}
+
+/* Rows `rows[0..R)` of the W4A16 product only (for sampled checks). */
+int oracle_gemm_w4a16_rows(const uint16_t* X, const int64_t* rows, int64_t R, int64_t K,
+                           const uint8_t* codes, const uint8_t* scales, float ts, int64_t N,
+                           double* Y) {
+  for (int64_t i = 0; i < R; ++i) {
+    int st = oracle_gemm_w4a16(X + rows[i] * K, 1, K, codes, scales, ts, N, Y + i * N);
+    if (st != OR_OK) return st;
+  }
+  return OR_OK;
+}
+
+/* W4A4: Y[m, n] = sum_k x_hat[m, k] * w_hat[n, k] in binary64. */
+int oracle_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, float a_ts, int64_t M,
+                     const uint8_t* w_codes, const uint8_t* w_scales, float w_ts, int64_t N,
+                     int64_t K, double* Y) {
+  if (M < 0 || N <= 0 || K <= 0 || K % 16 != 0) return OR_ERR_SHAPE;
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; ++k)
+        acc += dequant(a_codes, a_scales, a_ts, K, m, k) * dequant(w_codes, w_scales, w_ts, K, n, k);
+      Y[m * N + n] = acc;
+    }
+  return OR_OK;
+}

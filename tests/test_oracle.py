@@ -1,0 +1,404 @@
+"""Pins for the CPU oracle (no GPU).
+
+Each test ties the oracle to something other than itself: the value set the
+pages print, hand-computed worked examples, a third-party implementation of
+the number formats (ml_dtypes), a plain library matmul, brute-force search over
+every E4M3 scale, and invariants of the FourOverSix rule.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([c.strip() for c in line.split("|")])
+    return rows
+
+
+# ------------------------------------------------------------------ formats ---
+
+def test_e2m1_value_set_matches_page():
+    with open(os.path.join(GOLDEN, "e2m1_value_set.txt")) as f:
+        printed = [float(v) for line in f if not line.startswith("#") for v in line.split()]
+    decoded = [oracle.e2m1_value(c) for c in range(16)]
+    assert sorted(set(decoded)) == sorted(set(printed))
+    assert max(abs(v) for v in decoded) == 6.0
+    # +0 and -0 are the only pair of codes with equal value
+    assert len(set(decoded)) == 15
+    assert np.signbit(oracle.e2m1_value(8)) and not np.signbit(oracle.e2m1_value(0))
+    # codes 0..7 are the positive magnitudes in increasing order, 8..15 their negatives
+    assert decoded[:8] == sorted(decoded[:8])
+    assert all(decoded[c + 8] == -decoded[c] for c in range(8))
+
+
+def test_e2m1_round_to_nearest_even_and_saturate():
+    # midpoints go to the neighbour whose code is even
+    table = {0.25: 0.0, 0.75: 1.0, 1.25: 1.0, 1.75: 2.0, 2.5: 2.0, 3.5: 4.0, 5.0: 4.0}
+    for v, want in table.items():
+        assert oracle.e2m1_value(oracle.e2m1_encode(v)) == want
+        assert oracle.e2m1_value(oracle.e2m1_encode(-v)) == -want
+    for v in (6.0, 6.5, 7.0, 100.0, 3e38, float("inf")):
+        assert oracle.e2m1_encode(v) == 7
+        assert oracle.e2m1_encode(-v) == 15
+    assert oracle.e2m1_encode(-0.1) == 8  # negative values rounding to 0 keep the sign
+    assert oracle.e2m1_encode(0.0) == 0 and oracle.e2m1_encode(-0.0) == 8
+    for c in range(16):  # every grid value round-trips
+        assert oracle.e2m1_encode(oracle.e2m1_value(c)) == c
+
+
+def test_e2m1_encode_matches_ml_dtypes():
+    ml = pytest.importorskip("ml_dtypes")
+    rng = np.random.default_rng(7)
+    vals = np.concatenate([np.arange(-8, 8, 1 / 64, dtype=np.float32),
+                           rng.standard_normal(4000).astype(np.float32) * 3,
+                           np.nextafter(np.float32([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]), 0),
+                           np.nextafter(np.float32([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]), 9)])
+    lib = vals.astype(ml.float4_e2m1fn).view(np.uint8) & 0xF
+    mine = np.array([oracle.e2m1_encode(float(v)) for v in vals], np.uint8)
+    np.testing.assert_array_equal(mine, lib)
+
+
+def test_e4m3_decode_matches_ml_dtypes():
+    ml = pytest.importorskip("ml_dtypes")
+    lib = np.arange(256, dtype=np.uint8).view(ml.float8_e4m3fn).astype(np.float64)
+    mine = np.array([oracle.e4m3_value(b) for b in range(256)])
+    np.testing.assert_array_equal(np.isnan(mine), np.isnan(lib))
+    ok = ~np.isnan(lib)
+    np.testing.assert_array_equal(mine[ok], lib[ok])
+    assert oracle.e4m3_value(0x7E) == 448.0 and oracle.e4m3_value(0x01) == 2.0 ** -9
+
+
+def test_e4m3_encode_matches_ml_dtypes_in_range():
+    ml = pytest.importorskip("ml_dtypes")
+    pos = np.arange(127, dtype=np.uint8).view(ml.float8_e4m3fn).astype(np.float64)
+    mids = (pos[:-1] + pos[1:]) / 2
+    rng = np.random.default_rng(3)
+    vals = np.concatenate([pos, mids, np.nextafter(mids, 0), np.nextafter(mids, 1e9),
+                           rng.uniform(0, 460, 20000), 2.0 ** rng.uniform(-14, 8.8, 20000)])
+    vals = vals.astype(np.float32)
+    vals = vals[vals < 464]  # beyond 464 ml_dtypes produces NaN; saturation is tested below
+    lib = vals.astype(ml.float8_e4m3fn).view(np.uint8)
+    mine = np.array([oracle.e4m3_encode(float(v)) for v in vals], np.uint8)
+    np.testing.assert_array_equal(mine, lib)
+
+
+def test_e4m3_saturates_to_448():
+    for v in (448.0, 449.0, 464.0, 480.0, 1e6, float("inf")):
+        assert oracle.e4m3_encode(v) == 0x7E
+
+
+# ------------------------------------------------------- the 1.5x relation ---
+
+def test_m4_scale_is_fp8_of_m6_times_1p5_for_every_scale():
+    ml = pytest.importorskip("ml_dtypes")
+    for s6 in range(1, 127):
+        v = np.float32(oracle.e4m3_value(s6)) * np.float32(1.5)  # exact in binary32
+        assert float(v) == oracle.e4m3_value(s6) * 1.5
+        s4 = oracle.e4m3_encode(float(v))
+        if v < 464:
+            assert s4 == int(np.float32(v).astype(ml.float8_e4m3fn).view(np.uint8))
+        else:
+            assert s4 == 0x7E
+        # "about 1.5x": for normal E4M3 values the re-rounding moves the product by
+        # at most half a mantissa step (1/16 relative) unless it saturates
+        if oracle.e4m3_value(s6) >= 2.0 ** -6 and oracle.e4m3_value(s6) * 1.5 <= 448:
+            assert abs(oracle.e4m3_value(s4) / (oracle.e4m3_value(s6) * 1.5) - 1) <= 0.0625
+
+
+# ------------------------------------------------------- worked examples ---
+
+@pytest.mark.parametrize("row", _golden_rows("fos_worked_examples.txt"), ids=lambda r: r[0])
+def test_fos_worked_example(row):
+    name, ts, vals, s6, s4, sse6, sse4, choice, scale, code_bytes = row
+    x = np.array([float(v) for v in vals.split()], np.float32)
+    r = oracle.fos_block(x, float(ts))
+    assert r["s6"] == int(s6, 16), name
+    assert r["s4"] == int(s4, 16), name
+    assert r["sse6"] == float(sse6), name
+    assert r["sse4"] == float(sse4), name
+    assert r["choice"] == int(choice), name
+    assert r["scale"] == int(scale, 16), name
+    packed = [int(r["codes"][2 * j]) | (int(r["codes"][2 * j + 1]) << 4) for j in range(8)]
+    assert packed == [int(b, 16) for b in code_bytes.split()], name
+
+
+@pytest.mark.parametrize("row", _golden_rows("sse_tree_order.txt"), ids=lambda r: r[0])
+def test_sse_tree_order(row):
+    name, sbyte, ts, vals, sse = row
+    x = np.array([float(v) for v in vals.split()], np.float32)
+    got, _ = oracle.block_sse(x, int(sbyte, 16), float(ts))
+    assert got == float(np.float32(float(sse))), name
+
+
+def test_worked_examples_through_whole_tensor_path():
+    """The m4_wins / grid_m6_exact blocks inside a tensor whose amax gives ts = 1
+    exactly (amax 2688 = 6 * 448 is a bf16 value)."""
+    rows = {r[0]: r for r in _golden_rows("fos_worked_examples.txt")}
+    blocks = []
+    for name in ("grid_m6_exact", "m4_wins", "tie_keeps_m6"):
+        blocks.append([float(v) for v in rows[name][2].split()])
+    blocks.append([2688.0] + [0.0] * 15)
+    w = synth.f32_to_bf16_bits(np.array(blocks, np.float32).reshape(1, -1))
+    q = oracle.quantize_fos(w)
+    assert q["ts"] == 1.0
+    assert list(q["choice"][0]) == [0, 1, 0, 0]
+    assert list(q["scales"][0][:3]) == [0x38, 0x3C, 0x38]
+    assert q["m4_count"] == 1
+    assert list(q["codes"][0][8:16]) == [0x56, 0x24, 0x01, 0xDE, 0xAC, 0x09, 0x56, 0x24]
+
+
+# --------------------------------------------------------------- invariants ---
+
+def _random_blocks(n, seed):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((n, 16)).astype(np.float32)
+    x *= np.exp(rng.uniform(-3, 3, (n, 1))).astype(np.float32)
+    mask = rng.random((n, 16)) < 0.05
+    x[mask] *= 8
+    return x
+
+
+def test_selection_rule_invariants():
+    x = _random_blocks(3000, 11)
+    ts = float(np.abs(x).max() / 2688.0)
+    m4 = 0
+    for blk in x:
+        r = oracle.fos_block(blk, ts)
+        assert r["choice"] == int(r["sse4"] < r["sse6"])
+        chosen = r["s4"] if r["choice"] else r["s6"]
+        assert r["scale"] == chosen
+        sse, q = oracle.block_sse(blk, chosen, ts)
+        assert sse == min(r["sse4"], r["sse6"])
+        np.testing.assert_array_equal(q, r["codes"])
+        m4 += r["choice"]
+    assert 0 < m4 < len(x)  # both choices occur on generic data
+
+
+def test_no_magnitude_six_code_in_unsaturated_m4_blocks():
+    """x / eff4 <= 4 (1 + 2^-4)^2 < 5 when s6 is a normal E4M3 value and s4 is not
+    saturated, so an M=4 block never uses the code for 6."""
+    x = _random_blocks(3000, 12)
+    ts = float(np.abs(x).max() / 2688.0)
+    seen = 0
+    for blk in x:
+        r = oracle.fos_block(blk, ts)
+        if r["choice"] and oracle.e4m3_value(r["s6"]) >= 2.0 ** -6 and r["s4"] != 0x7E:
+            seen += 1
+            assert not np.any((r["codes"] & 7) == 7)
+    assert seen > 100
+
+
+def test_constant_and_zero_blocks():
+    # a constant block c with |c|/6 an E4M3 value is exact under both candidates
+    # (|c| -> 6 * s6 and, with s4 = 1.5 * s6, -> 4 * s4), so the tie keeps M=6
+    for c in (6.0, -3.0, 0.75):
+        r = oracle.fos_block(np.full(16, c, np.float32), 1.0)
+        assert oracle.e4m3_value(r["s6"]) == abs(c) / 6
+        assert oracle.e4m3_value(r["s4"]) == 1.5 * abs(c) / 6
+        assert r["sse6"] == 0.0 and r["sse4"] == 0.0 and r["choice"] == 0
+        assert np.all(r["codes"] == (15 if c < 0 else 7))
+    r = oracle.fos_block(np.zeros(16, np.float32), 0.01)
+    assert r["scale"] == 0 and r["choice"] == 0 and not r["codes"].any()
+
+
+# --------------------------------------------------------------- brute force ---
+
+def _grid_nearest_sse(x64, eff):
+    """Exact (binary64) SSE of the block when every element takes the nearest
+    of the 15 E2M1 grid values times eff (exhaustive search)."""
+    grid = np.array(sorted({oracle.e2m1_value(c) for c in range(16)}))
+    if eff == 0:
+        return float(np.sum(x64 ** 2))
+    cand = grid[None, :] * eff
+    d = np.min(np.abs(x64[:, None] - cand), axis=1)
+    return float(np.sum(d ** 2))
+
+
+def test_brute_force_scale_search_on_tiny_blocks():
+    ml = pytest.importorskip("ml_dtypes")
+    e4 = np.arange(127, dtype=np.uint8).view(ml.float8_e4m3fn).astype(np.float64)
+    x = _random_blocks(400, 13)
+    ts = float(np.float32(np.abs(x).max() / 2688.0))
+    for blk in x:
+        r = oracle.fos_block(blk, ts)
+        x64 = blk.astype(np.float64)
+        amax = float(np.float32(np.abs(blk).max()))
+        r6 = float(np.float32(np.float32(amax / np.float32(6)) / np.float32(ts)))
+        # (i) s6 is the E4M3 value nearest r6
+        dist = np.abs(e4 - r6)
+        assert dist[r["s6"]] == dist.min()
+        # (ii) the oracle's SSEs agree with exhaustive nearest-grid evaluation
+        b6 = _grid_nearest_sse(x64, e4[r["s6"]] * np.float64(np.float32(ts)))
+        b4 = _grid_nearest_sse(x64, e4[r["s4"]] * np.float64(np.float32(ts)))
+        tol = 1e-5 * max(b6, b4) + 1e-30
+        assert abs(r["sse6"] - b6) <= tol and abs(r["sse4"] - b4) <= tol
+        if abs(b4 - b6) > 2 * tol:
+            assert r["choice"] == int(b4 < b6)
+        # (iii) best over all 127 scales <= FourOverSix <= plain M=6
+        best = min(_grid_nearest_sse(x64, e * np.float64(np.float32(ts))) for e in e4)
+        fos = min(b4, b6)
+        assert best <= fos + tol and fos <= b6 + tol
+
+
+# ------------------------------------------------------------ whole tensors ---
+
+def test_quantize_fos_matches_blockwise_and_tensor_scale():
+    w = synth.weight_normal(8, 64, seed=5, outlier_frac=0.05)
+    q = oracle.quantize_fos(w)
+    wf = synth.bf16_bits_to_f32(w)
+    assert q["ts"] == float(np.float32(np.abs(wf).max()) / np.float32(2688.0))
+    for n in range(8):
+        for b in range(4):
+            r = oracle.fos_block(wf[n, 16 * b:16 * b + 16], q["ts"])
+            assert q["scales"][n, b] == r["scale"] and q["choice"][n, b] == r["choice"]
+            packed = [int(r["codes"][2 * j]) | (int(r["codes"][2 * j + 1]) << 4) for j in range(8)]
+            assert list(q["codes"][n, 8 * b:8 * b + 8]) == packed
+    assert q["m4_count"] == int(q["choice"].sum())
+
+
+def test_quantize_zero_tensor_and_nonfinite():
+    z = np.zeros((2, 32), np.uint16)
+    z[0, 3] = 0x8000  # -0
+    q = oracle.quantize_fos(z)
+    assert q["ts"] == 1.0 and not q["scales"].any() and not q["choice"].any()
+    assert q["codes"][0, 1] == 0x80 and q["codes"].sum() == 0x80
+    bad = np.zeros((1, 16), np.uint16)
+    bad[0, 5] = 0x7F80  # +inf
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.quantize_fos(bad)
+    assert e.value.status == 5
+    bad[0, 5] = 0x7FC1  # NaN
+    with pytest.raises(oracle.OracleError):
+        oracle.quantize_act(bad)
+
+
+def test_custom_divisor_avoids_saturation():
+    """Under D = 6*448 the block holding amax gets s6 = 448, so its M=4 candidate
+    saturates to 448 as well (a tie, so M=6).  Under D = 4*448 that block's s6 is
+    about 299 and its s4 (about 1.5x) stays a distinct, unsaturated value."""
+    w = synth.weight_normal(4, 256, seed=9, outlier_frac=0.02)
+    wf = synth.bf16_bits_to_f32(w)
+    n, k = np.unravel_index(np.argmax(np.abs(wf)), wf.shape)
+    blk = wf[n, 16 * (k // 16):16 * (k // 16) + 16]
+    a = oracle.quantize_fos(w)
+    ra = oracle.fos_block(blk, a["ts"])
+    assert ra["s6"] == 0x7E and ra["s4"] == 0x7E and ra["choice"] == 0
+    b = oracle.quantize_fos(w, divisor=4 * 448.0)
+    assert b["ts"] == float(np.float32(np.abs(wf).max()) / np.float32(1792.0))
+    rb = oracle.fos_block(blk, b["ts"])
+    assert oracle.e4m3_value(rb["s6"]) == 288.0 and rb["s4"] == 0x7E  # 432 ties up to 448
+    assert rb["s4"] != rb["s6"]
+
+
+def test_act_quant_is_m6_only():
+    x = synth.act_student_t(3, 128, seed=2)
+    q = oracle.quantize_act(x)
+    xf = synth.bf16_bits_to_f32(x)
+    for m in range(3):
+        for b in range(8):
+            blk = xf[m, 16 * b:16 * b + 16]
+            s = oracle.fos_block(blk, q["ts"])["s6"]
+            assert q["scales"][m, b] == s
+            _, codes = oracle.block_sse(blk, s, q["ts"])
+            packed = [int(codes[2 * j]) | (int(codes[2 * j + 1]) << 4) for j in range(8)]
+            assert list(q["codes"][m, 8 * b:8 * b + 8]) == packed
+
+
+def test_dequantised_weights_are_exact_in_bf16():
+    """value(code) * value(scale) has at most 6 significant bits and lies in
+    [2^-10, 2688], so it is exact in bfloat16 (the W4A16 kernel relies on this)."""
+    for c in range(16):
+        for s in range(127):
+            v = np.float32(oracle.e2m1_value(c) * oracle.e4m3_value(s))
+            b = synth.f32_to_bf16_bits(np.array([v]))
+            assert synth.bf16_bits_to_f32(b)[0] == v
+
+
+# ------------------------------------------------------------- scale layout ---
+
+def test_scales_to_mma_layout_hand_examples():
+    R, K = 130, 80  # 2 row tiles x 2 column tiles (5 blocks, padded to 8)
+    s = np.arange(R * (K // 16), dtype=np.uint32).reshape(R, K // 16)
+    s = (s % 251 + 1).astype(np.uint8)
+    out = oracle.scales_to_mma(s, K)
+    assert out.size == 2 * 2 * 512
+    assert out[0] == s[0, 0]
+    assert out[22] == s[33, 2]      # (33 % 32) * 16 + (33 // 32) * 4 + 2
+    assert out[511] == s[127, 3]    # 31 * 16 + 3 * 4 + 3
+    assert out[592] == s[5, 4]      # tile 1: 512 + 5 * 16
+    assert out[1552] == s[129, 4]   # tile 3: 1536 + 1 * 16
+    # every logical scale appears exactly once; padding is zero
+    assert np.count_nonzero(out) == R * (K // 16)
+    assert sorted(out[out > 0].tolist()) == sorted(s.ravel().tolist())
+
+
+# -------------------------------------------------------------------- GEMMs ---
+
+def _dequant_lib(codes, scales, ts):
+    ml = pytest.importorskip("ml_dtypes")
+    lo = codes & 0xF
+    hi = codes >> 4
+    nib = np.stack([lo, hi], axis=-1).reshape(codes.shape[0], -1)
+    v = nib.astype(np.uint8).view(ml.float4_e2m1fn).astype(np.float64)
+    s = scales.view(ml.float8_e4m3fn).astype(np.float64)
+    return v * np.repeat(s, 16, axis=1) * np.float64(ts)
+
+
+def test_gemm_w4a16_by_hand():
+    x = synth.f32_to_bf16_bits(np.array([[1.0, 2.0] + [0.0] * 14], np.float32))
+    codes = np.zeros((1, 8), np.uint8)
+    codes[0, 0] = 0x7 | (0xA << 4)  # element 0 -> 6, element 1 -> -1
+    scales = np.array([[0x38]], np.uint8)  # 1.0
+    y = oracle.gemm_w4a16(x, codes, scales, 0.5)
+    assert y[0, 0] == 1 * 6 * 0.5 + 2 * (-1) * 0.5  # = 2
+
+
+def test_gemm_w4a16_matches_library_matmul():
+    w = synth.weight_normal(48, 96, seed=21, outlier_frac=0.02)
+    x = synth.act_normal(5, 96, seed=22)
+    q = oracle.quantize_fos(w)
+    y = oracle.gemm_w4a16(x, q["codes"], q["scales"], q["ts"])
+    ref = synth.bf16_bits_to_f32(x).astype(np.float64) @ _dequant_lib(q["codes"], q["scales"], q["ts"]).T
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+    rows = oracle.gemm_w4a16_rows(x, [4, 1], q["codes"], q["scales"], q["ts"])
+    np.testing.assert_array_equal(rows, y[[4, 1]])
+
+
+def test_gemm_w4a4_matches_library_matmul():
+    w = synth.weight_normal(40, 64, seed=23, outlier_frac=0.02)
+    x = synth.act_student_t(6, 64, seed=24)
+    qw = oracle.quantize_fos(w)
+    qa = oracle.quantize_act(x)
+    y = oracle.gemm_w4a4(qa["codes"], qa["scales"], qa["ts"], qw["codes"], qw["scales"], qw["ts"])
+    ref = _dequant_lib(qa["codes"], qa["scales"], qa["ts"]) @ \
+        _dequant_lib(qw["codes"], qw["scales"], qw["ts"]).T
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_fos_error_never_worse_than_m6_on_a_tensor():
+    w = synth.weight_lognormal_rows(16, 256, seed=31)
+    q = oracle.quantize_fos(w)
+    wf = synth.bf16_bits_to_f32(w).astype(np.float64)
+    deq = _dequant_lib(q["codes"], q["scales"], q["ts"])
+    # an all-M6 quantisation of the same tensor
+    ts = q["ts"]
+    sse_fos = sse_m6 = 0.0
+    for n in range(16):
+        for b in range(16):
+            blk = wf[n, 16 * b:16 * b + 16].astype(np.float32)
+            r = oracle.fos_block(blk, ts)
+            sse_fos += min(r["sse4"], r["sse6"])
+            sse_m6 += r["sse6"]
+    assert sse_fos <= sse_m6
+    assert np.sum((wf - deq) ** 2) == pytest.approx(sse_fos, rel=1e-5)
