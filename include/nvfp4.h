@@ -1,0 +1,206 @@
+/*
+ * nvfp4.h -- C ABI of the GB300 (sm_103a) NVFP4 linear-layer library.
+ *
+ * The method: linear-layer weights are stored as NVFP4 (FP4 E2M1 codes, half a
+ * byte per element, plus an FP8 scale per block) and quantised with the
+ * FourOverSix rule, which lets every block pick between the usual M=6 scale
+ * and an M=4 scale of about 1.5x; GEMMs run as W4A16 (bf16 activations times
+ * dequantised weights) for small token counts and as W4A4 (activations
+ * quantised online, native block-scaled FP4 tensor-core MMA) above a
+ * crossover in M.  Sources: "SOAR 2026 Recap: From Compute Limits to the
+ * Open-Source Ecosystem", section "1. Quantization and GEMM dispatch";
+ * "SOAR Weekly Champion Notes 07 ... NVFP4 Quantization Improvements",
+ * sections "01 Background" and "02 FourOverSix".
+ *
+ * Formats (readings where the pages are silent; fixed by this library):
+ *   - W is [N, K] row-major bf16 (an nn.Linear weight, out x in); X is [M, K]
+ *     row-major bf16; Y is [M, N] row-major (bf16, or fp32 when requested).
+ *   - Blocks are 16 consecutive elements along K.  codes are [rows, K/2]
+ *     bytes, element 2j in the low nibble of byte j and 2j+1 in the high
+ *     nibble; code = sign << 3 | E2M1 magnitude bits.
+ *   - Block scales are E4M3 bytes.  "Logical" scales are [rows, K/16]
+ *     row-major.  "MMA" scales use the block-scaled tensor-core tiling: the
+ *     [rows, K/16] matrix is cut into 128 x 4 tiles (zero padded), tiles are
+ *     stored row-tile-major, 512 bytes each, with scale (r, c) of a tile at
+ *     byte (r % 32) * 16 + (r / 32) * 4 + c.  Size: nvfp4_scales_mma_bytes().
+ *   - One FP32 tensor scale ts = amax(|W|) / divisor (divisor 6 * 448 by
+ *     default; an all-zero tensor gets ts = 1).  A dequantised element is
+ *     value(code) * value(scale) * ts.
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library never allocates or frees device memory.  Scratch goes through
+ *     the caller's `workspace` (size from nvfp4_workspace_bytes()).
+ *   - Every call is asynchronous on `stream`.  Argument errors are returned
+ *     synchronously, before anything is launched.  A launch failure returns
+ *     NVFP4_ERR_CUDA (text in nvfp4_last_error()).  Errors found on the
+ *     device (a non-finite input) are recorded in a device status word and
+ *     reported by nvfp4_get_device_status().
+ *   - Pointers to tensors must be 16-byte aligned (NVFP4_ERR_ALIGN).
+ *   - The library keeps no state between calls except the crossover table
+ *     (nvfp4_set_crossover) and the device status word.
+ */
+#ifndef NVFP4_H_
+#define NVFP4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nvfp4_status {
+  NVFP4_OK = 0,
+  NVFP4_ERR_INVALID_ARG = 1, /* null pointer where one is required, bad enum */
+  NVFP4_ERR_SHAPE = 2,       /* sizes <= 0 where not allowed, K not a multiple of 16 (64 for GEMMs) */
+  NVFP4_ERR_ALIGN = 3,       /* a tensor pointer not 16-byte aligned */
+  NVFP4_ERR_WORKSPACE = 4,   /* workspace too small */
+  NVFP4_ERR_NONFINITE = 5,   /* an input held Inf or NaN (device-detected) */
+  NVFP4_ERR_TIMEOUT = 6,     /* a bounded device-side wait ran out (device-detected) */
+  NVFP4_ERR_CUDA = 7,        /* a CUDA runtime or driver call failed */
+  NVFP4_ERR_UNSUPPORTED = 8  /* no sm_100-family GPU, or a size the kernels do not handle */
+} nvfp4_status;
+
+/* Output element type of the GEMMs. */
+typedef enum nvfp4_out_dtype { NVFP4_OUT_BF16 = 0, NVFP4_OUT_F32 = 1 } nvfp4_out_dtype;
+
+/* Operation ids for nvfp4_workspace_bytes(). */
+typedef enum nvfp4_op {
+  NVFP4_OP_QUANTIZE_FOS = 0,
+  NVFP4_OP_QUANTIZE_ACT = 1,
+  NVFP4_OP_GEMM_W4A16 = 2,
+  NVFP4_OP_GEMM_W4A4 = 3,
+  NVFP4_OP_LINEAR = 4
+} nvfp4_op;
+
+#define NVFP4_DEFAULT_DIVISOR 2688.0f /* 6 (E2M1 max) * 448 (E4M3 max) */
+
+/* A quantised weight as the GEMMs read it.  All pointers are device pointers,
+ * owned by the caller and 16-byte aligned. */
+typedef struct nvfp4_weight {
+  const uint8_t* codes;      /* [N, K/2] packed E2M1 codes */
+  const uint8_t* scales_mma; /* nvfp4_scales_mma_bytes(N, K) bytes, MMA tiling */
+  const float* tensor_scale; /* one float */
+  int64_t N;
+  int64_t K;
+} nvfp4_weight;
+
+/* Bytes of an MMA-tiled scale matrix for `rows` rows of length K
+ * (= ceil(rows/128) * ceil(K/64) * 512).  Returns 0 for invalid sizes. */
+size_t nvfp4_scales_mma_bytes(int64_t rows, int64_t K);
+
+/* Workspace bytes that `op` needs for the given sizes (M is ignored by the
+ * quantiser of weights, N by the activation quantiser).  0 on bad sizes. */
+size_t nvfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
+
+/*
+ * FourOverSix NVFP4 weight quantisation ("SOAR Weekly Champion Notes 07",
+ * section "02 FourOverSix"; round-to-nearest only).
+ *
+ * For each 16-element block: s6 = E4M3((amax_block / 6) / ts),
+ * s4 = E4M3(value(s6) * 1.5); each candidate quantises the block with
+ * q = E2M1(x / (value(s) * ts)) and scores it by the binary32 sum of squared
+ * dequantisation errors (fixed tree order); the block keeps s4 only if its
+ * error is strictly smaller.  All steps are IEEE binary32, round to nearest
+ * even, no FMA contraction; E4M3 and E2M1 conversions saturate (448, 6).
+ *
+ *   W            in:  device bf16 [N, K]
+ *   N, K         N >= 1, K >= 16, K % 16 == 0
+ *   divisor      tensor-scale divisor; <= 0 or non-finite selects 6 * 448
+ *   codes        out: device [N, K/2]                          (required)
+ *   scales       out: device [N, K/16] logical E4M3 bytes       (nullable)
+ *   scales_mma   out: device, nvfp4_scales_mma_bytes(N, K) bytes (nullable;
+ *                     padding bytes are written as 0)
+ *   tensor_scale out: device, 1 float                          (required)
+ *   choice       out: device [N, K/16], 1 = block took M=4      (nullable)
+ *   m4_count     out: device, number of M=4 blocks (overwritten) (nullable)
+ *   workspace    device scratch of nvfp4_workspace_bytes(NVFP4_OP_QUANTIZE_FOS, 0, N, K)
+ * At least one of scales / scales_mma must be given.  On a non-finite input
+ * the device status word records NVFP4_ERR_NONFINITE and no output is written.
+ */
+nvfp4_status nvfp4_quantize_fos(const void* W, int64_t N, int64_t K, float divisor,
+                                uint8_t* codes, uint8_t* scales, uint8_t* scales_mma,
+                                float* tensor_scale, uint8_t* choice,
+                                unsigned long long* m4_count, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Online NVFP4 quantisation of activations for the W4A4 path (the pages give
+ * no activation rule; this library uses the standard M=6 scale only, with the
+ * same binary32 steps and tensor scale as the weight quantiser).
+ *
+ *   X            in:  device bf16 [M, K], M >= 1, K % 16 == 0
+ *   codes        out: device [M, K/2]                           (required)
+ *   scales       out: device [M, K/16] logical                  (nullable)
+ *   scales_mma   out: device, nvfp4_scales_mma_bytes(M, K) bytes (nullable)
+ *   tensor_scale out: device, 1 float                           (required)
+ */
+nvfp4_status nvfp4_quantize_act(const void* X, int64_t M, int64_t K, float divisor,
+                                uint8_t* codes, uint8_t* scales, uint8_t* scales_mma,
+                                float* tensor_scale, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream);
+
+/*
+ * W4A16 GEMM ("SOAR 2026 Recap", section "1. Quantization and GEMM dispatch":
+ * the path for M <= 48 on the pages' GPU):
+ *   Y[m, n] = ts * sum_k X[m, k] * value(code[n, k]) * value(scale[n, k/16]),
+ * bf16 activations, weights dequantised exactly to bf16, fp32 accumulation.
+ *   X      in:  device bf16 [M, K];  M >= 0 (M == 0 launches nothing)
+ *   W      in:  quantised weight; K % 64 == 0
+ *   Y      out: device [M, N] of out_dtype
+ */
+nvfp4_status nvfp4_gemm_w4a16(const void* X, int64_t M, const nvfp4_weight* W, void* Y,
+                              int out_dtype, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
+
+/*
+ * W4A4 GEMM (same section: the path above the crossover, "natively invoking
+ * NVFP4 MMA instructions"): block-scaled FP4 x FP4 tensor-core MMA with fp32
+ * accumulation,
+ *   Y[m, n] = ts_a * ts_w * sum_k value(qa[m,k]) value(sa[m,k/16]) value(qw[n,k]) value(sw[n,k/16]).
+ *   a_codes      in: device [M, K/2] (from nvfp4_quantize_act)
+ *   a_scales_mma in: device, nvfp4_scales_mma_bytes(M, K) bytes
+ *   a_tensor_scale in: device, 1 float
+ *   W            in: quantised weight; K % 64 == 0
+ *   Y            out: device [M, N] of out_dtype
+ */
+nvfp4_status nvfp4_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma,
+                             const float* a_tensor_scale, int64_t M, const nvfp4_weight* W,
+                             void* Y, int out_dtype, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream);
+
+/*
+ * NVFP4 linear layer with M-based dispatch (same section: "M <= 48 uses W4A16,
+ * M > 48 switches to W4A4; the runtime selects the lower-latency
+ * implementation").  M <= crossover(N, K) runs nvfp4_gemm_w4a16; otherwise
+ * nvfp4_quantize_act (into the workspace) then nvfp4_gemm_w4a4.
+ *   workspace  nvfp4_workspace_bytes(NVFP4_OP_LINEAR, M, N, K) bytes
+ */
+nvfp4_status nvfp4_linear(const void* X, int64_t M, const nvfp4_weight* W, void* Y,
+                          int out_dtype, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
+
+/* Crossover table: the largest M that still takes the W4A16 path for a
+ * weight of shape [N, K].  N == 0 and K == 0 set the default used for shapes
+ * without an entry.  Thread-safe.  The built-in default comes from a sweep on
+ * GB300 (see nvfp4_get_crossover(0, 0)). */
+nvfp4_status nvfp4_set_crossover(int64_t N, int64_t K, int64_t M_threshold);
+int64_t nvfp4_get_crossover(int64_t N, int64_t K);
+
+/* Synchronises `stream`, then returns and clears the device status word of the
+ * current device: NVFP4_OK, NVFP4_ERR_NONFINITE or NVFP4_ERR_TIMEOUT. */
+nvfp4_status nvfp4_get_device_status(cudaStream_t stream);
+
+/* Static text for a status code. */
+const char* nvfp4_status_string(nvfp4_status status);
+
+/* Text of the last NVFP4_ERR_CUDA / argument error on this thread. */
+const char* nvfp4_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_H_ */

@@ -1,0 +1,285 @@
+// api.cu -- the C ABI (include/nvfp4.h): argument checks, workspace layout,
+// dispatch between the W4A16 and W4A4 paths, device status word.
+#include <cmath>
+#include <cstdio>
+#include <map>
+#include <mutex>
+#include <string>
+#include <utility>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "nvfp4.h"
+
+// Device status word of this library (one per device): bit 0 = non-finite
+// input seen, bit 1 = a bounded wait ran out.
+static __device__ unsigned int g_device_status;
+
+namespace {
+
+thread_local std::string t_last_error;
+
+std::mutex g_mu;
+std::map<std::pair<int64_t, int64_t>, int64_t> g_crossover;
+// Largest M that takes the W4A16 path when no per-shape entry exists.
+int64_t g_default_crossover = 48;
+
+struct DeviceInfo {
+  bool ready = false;
+  nvfp4_status st = NVFP4_ERR_CUDA;
+  int num_sms = 0;
+  unsigned int* status = nullptr;
+};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+
+nvfp4_status fail(nvfp4_status st, const char* what) {
+  t_last_error = what;
+  return st;
+}
+
+nvfp4_status fail_cuda(cudaError_t err, const char* where) {
+  t_last_error = std::string(where) + ": " + cudaGetErrorString(err);
+  return NVFP4_ERR_CUDA;
+}
+
+// Per-device set-up, done once with that device current: SM count, a check
+// that this is an sm_103 GPU, and the device address of the status word.
+nvfp4_status device_info(const DeviceInfo** out) {
+  int dev = -1;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return fail_cuda(err, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(NVFP4_ERR_UNSUPPORTED, "device index out of range");
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return fail_cuda(err, "cudaDeviceGetAttribute");
+    if (major != 10 || minor != 3)
+      return fail(NVFP4_ERR_UNSUPPORTED, "this library is built for sm_103a (GB300) only");
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_device_status);
+    if (err != cudaSuccess) return fail_cuda(err, "cudaGetSymbolAddress(status)");
+    d.status = static_cast<unsigned int*>(p);
+    d.ready = true;
+  }
+  *out = &d;
+  return NVFP4_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+float effective_divisor(float d) { return (d > 0.0f && std::isfinite(d)) ? d : NVFP4_DEFAULT_DIVISOR; }
+
+constexpr int64_t kMaxElems = int64_t(1) << 40;
+
+bool weight_ok(const nvfp4_weight* W) {
+  return W != nullptr && W->codes != nullptr && W->scales_mma != nullptr && W->tensor_scale != nullptr;
+}
+
+nvfp4_status check_weight(const nvfp4_weight* W) {
+  if (!weight_ok(W)) return fail(NVFP4_ERR_INVALID_ARG, "weight descriptor or one of its pointers is null");
+  if (W->N <= 0 || W->K <= 0 || W->K % 64 != 0 || W->N > kMaxElems / W->K)
+    return fail(NVFP4_ERR_SHAPE, "weight needs N >= 1, K >= 64, K % 64 == 0");
+  if (!aligned(W->codes, 16) || !aligned(W->scales_mma, 16) || !aligned(W->tensor_scale, 4))
+    return fail(NVFP4_ERR_ALIGN, "weight pointers must be 16-byte aligned");
+  return NVFP4_OK;
+}
+
+nvfp4_status check_out_dtype(int out_dtype) {
+  if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_F32)
+    return fail(NVFP4_ERR_INVALID_ARG, "out_dtype must be NVFP4_OUT_BF16 or NVFP4_OUT_F32");
+  return NVFP4_OK;
+}
+
+nvfp4_status quantize_common(const void* X, int64_t rows, int64_t K, float divisor, bool fos, uint8_t* codes,
+                             uint8_t* scales, uint8_t* scales_mma, float* ts, uint8_t* choice,
+                             unsigned long long* m4_count, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (X == nullptr || codes == nullptr || ts == nullptr || (scales == nullptr && scales_mma == nullptr))
+    return fail(NVFP4_ERR_INVALID_ARG, "X, codes, tensor_scale and one of scales/scales_mma are required");
+  if (rows <= 0 || K < 16 || K % 16 != 0 || rows > kMaxElems / K)
+    return fail(NVFP4_ERR_SHAPE, "need rows >= 1, K >= 16, K % 16 == 0");
+  if (!aligned(X, 16) || !aligned(codes, 16) || !aligned(scales, 16) || !aligned(scales_mma, 16) ||
+      !aligned(choice, 16) || !aligned(ts, 4) || !aligned(m4_count, 8))
+    return fail(NVFP4_ERR_ALIGN, "tensor pointers must be 16-byte aligned");
+  if (ws == nullptr || ws_bytes < nvfp4::quant_workspace_bytes() || !aligned(ws, 16))
+    return fail(NVFP4_ERR_WORKSPACE, "workspace missing, unaligned or too small");
+  const DeviceInfo* d = nullptr;
+  nvfp4_status st = device_info(&d);
+  if (st != NVFP4_OK) return st;
+  cudaError_t err = nvfp4::launch_quantize(X, rows, K, effective_divisor(divisor), fos, codes, scales,
+                                           scales_mma, ts, choice, m4_count, ws, d->status, d->num_sms, stream);
+  if (err != cudaSuccess) return fail_cuda(err, "quantize launch");
+  return NVFP4_OK;
+}
+
+struct LinearWs {
+  size_t codes_off, scales_off, ts_off, quant_off, total;
+};
+
+LinearWs linear_ws_layout(int64_t M, int64_t K) {
+  LinearWs l;
+  l.codes_off = 0;
+  l.scales_off = align256((size_t)M * (size_t)(K / 2));
+  l.ts_off = l.scales_off + align256(nvfp4_scales_mma_bytes(M, K));
+  l.quant_off = l.ts_off + 256;
+  l.total = l.quant_off + align256(nvfp4::quant_workspace_bytes());
+  return l;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t nvfp4_scales_mma_bytes(int64_t rows, int64_t K) {
+  if (rows <= 0 || K <= 0 || K % 16 != 0) return 0;
+  return (size_t)((rows + 127) / 128) * (size_t)((K / 16 + 3) / 4) * 512;
+}
+
+size_t nvfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
+  (void)N;
+  if (K <= 0 || K % 16 != 0) return 0;
+  switch (op) {
+    case NVFP4_OP_QUANTIZE_FOS:
+    case NVFP4_OP_QUANTIZE_ACT: return nvfp4::quant_workspace_bytes();
+    case NVFP4_OP_GEMM_W4A16:
+    case NVFP4_OP_GEMM_W4A4: return 0;
+    case NVFP4_OP_LINEAR:
+      // sized for the W4A4 branch whatever the current crossover is
+      if (M <= 0) return 0;
+      return linear_ws_layout(M, K).total;
+    default: return 0;
+  }
+}
+
+nvfp4_status nvfp4_quantize_fos(const void* W, int64_t N, int64_t K, float divisor, uint8_t* codes,
+                                uint8_t* scales, uint8_t* scales_mma, float* tensor_scale, uint8_t* choice,
+                                unsigned long long* m4_count, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream) {
+  return quantize_common(W, N, K, divisor, true, codes, scales, scales_mma, tensor_scale, choice, m4_count,
+                         workspace, workspace_bytes, stream);
+}
+
+nvfp4_status nvfp4_quantize_act(const void* X, int64_t M, int64_t K, float divisor, uint8_t* codes,
+                                uint8_t* scales, uint8_t* scales_mma, float* tensor_scale, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+  return quantize_common(X, M, K, divisor, false, codes, scales, scales_mma, tensor_scale, nullptr, nullptr,
+                         workspace, workspace_bytes, stream);
+}
+
+nvfp4_status nvfp4_gemm_w4a16(const void* X, int64_t M, const nvfp4_weight* W, void* Y, int out_dtype,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  nvfp4_status st = check_weight(W);
+  if (st != NVFP4_OK) return st;
+  if ((st = check_out_dtype(out_dtype)) != NVFP4_OK) return st;
+  if (M < 0 || M > kMaxElems / W->K || M > kMaxElems / W->N) return fail(NVFP4_ERR_SHAPE, "bad M");
+  if (M == 0) return NVFP4_OK;
+  if (X == nullptr || Y == nullptr) return fail(NVFP4_ERR_INVALID_ARG, "X and Y are required");
+  if (!aligned(X, 16) || !aligned(Y, 16)) return fail(NVFP4_ERR_ALIGN, "X and Y must be 16-byte aligned");
+  const DeviceInfo* d = nullptr;
+  if ((st = device_info(&d)) != NVFP4_OK) return st;
+  cudaError_t err = nvfp4::launch_gemm_w4a16(X, M, W->codes, W->scales_mma, W->tensor_scale, W->N, W->K, Y,
+                                             out_dtype == NVFP4_OUT_F32, d->num_sms, stream);
+  if (err != cudaSuccess) return fail_cuda(err, "gemm_w4a16 launch");
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma, const float* a_tensor_scale,
+                             int64_t M, const nvfp4_weight* W, void* Y, int out_dtype, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  nvfp4_status st = check_weight(W);
+  if (st != NVFP4_OK) return st;
+  if ((st = check_out_dtype(out_dtype)) != NVFP4_OK) return st;
+  if (M < 0 || M > kMaxElems / W->K || M > kMaxElems / W->N) return fail(NVFP4_ERR_SHAPE, "bad M");
+  if (M == 0) return NVFP4_OK;
+  if (a_codes == nullptr || a_scales_mma == nullptr || a_tensor_scale == nullptr || Y == nullptr)
+    return fail(NVFP4_ERR_INVALID_ARG, "activation codes, scales, tensor scale and Y are required");
+  if (!aligned(a_codes, 16) || !aligned(a_scales_mma, 16) || !aligned(a_tensor_scale, 4) || !aligned(Y, 16))
+    return fail(NVFP4_ERR_ALIGN, "activation and output pointers must be 16-byte aligned");
+  const DeviceInfo* d = nullptr;
+  if ((st = device_info(&d)) != NVFP4_OK) return st;
+  cudaError_t err = nvfp4::launch_gemm_w4a4(a_codes, a_scales_mma, a_tensor_scale, M, W->codes, W->scales_mma,
+                                            W->tensor_scale, W->N, W->K, Y, out_dtype == NVFP4_OUT_F32,
+                                            d->status, d->num_sms, stream);
+  if (err == cudaErrorNotSupported) return fail(NVFP4_ERR_UNSUPPORTED, "gemm_w4a4: unsupported size");
+  if (err != cudaSuccess) return fail_cuda(err, "gemm_w4a4 launch");
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_linear(const void* X, int64_t M, const nvfp4_weight* W, void* Y, int out_dtype,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  nvfp4_status st = check_weight(W);
+  if (st != NVFP4_OK) return st;
+  // the tensor-core path needs at least one full 256-wide K stage
+  if (M <= nvfp4_get_crossover(W->N, W->K) || W->K < 256)
+    return nvfp4_gemm_w4a16(X, M, W, Y, out_dtype, workspace, workspace_bytes, stream);
+  if ((st = check_out_dtype(out_dtype)) != NVFP4_OK) return st;
+  if (M > kMaxElems / W->K) return fail(NVFP4_ERR_SHAPE, "bad M");
+  const LinearWs l = linear_ws_layout(M, W->K);
+  if (workspace == nullptr || workspace_bytes < l.total || !aligned(workspace, 256))
+    return fail(NVFP4_ERR_WORKSPACE, "linear: workspace missing, not 256-byte aligned or too small");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* a_codes = ws + l.codes_off;
+  uint8_t* a_smma = ws + l.scales_off;
+  float* a_ts = reinterpret_cast<float*>(ws + l.ts_off);
+  st = nvfp4_quantize_act(X, M, W->K, NVFP4_DEFAULT_DIVISOR, a_codes, nullptr, a_smma, a_ts, ws + l.quant_off,
+                          workspace_bytes - l.quant_off, stream);
+  if (st != NVFP4_OK) return st;
+  return nvfp4_gemm_w4a4(a_codes, a_smma, a_ts, M, W, Y, out_dtype, nullptr, 0, stream);
+}
+
+nvfp4_status nvfp4_set_crossover(int64_t N, int64_t K, int64_t M_threshold) {
+  if (N < 0 || K < 0 || M_threshold < 0) return fail(NVFP4_ERR_INVALID_ARG, "negative crossover argument");
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (N == 0 && K == 0) g_default_crossover = M_threshold;
+  else g_crossover[{N, K}] = M_threshold;
+  return NVFP4_OK;
+}
+
+int64_t nvfp4_get_crossover(int64_t N, int64_t K) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_crossover.find({N, K});
+  return it == g_crossover.end() ? g_default_crossover : it->second;
+}
+
+nvfp4_status nvfp4_get_device_status(cudaStream_t stream) {
+  cudaError_t err = cudaStreamSynchronize(stream);
+  if (err != cudaSuccess) return fail_cuda(err, "cudaStreamSynchronize");
+  unsigned int v = 0;
+  err = cudaMemcpyFromSymbol(&v, g_device_status, sizeof v);
+  if (err != cudaSuccess) return fail_cuda(err, "read status word");
+  const unsigned int zero = 0;
+  err = cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero);
+  if (err != cudaSuccess) return fail_cuda(err, "clear status word");
+  if (v & nvfp4::kStatusNonfinite) return NVFP4_ERR_NONFINITE;
+  if (v & nvfp4::kStatusTimeout) return NVFP4_ERR_TIMEOUT;
+  return NVFP4_OK;
+}
+
+const char* nvfp4_status_string(nvfp4_status s) {
+  switch (s) {
+    case NVFP4_OK: return "ok";
+    case NVFP4_ERR_INVALID_ARG: return "invalid argument";
+    case NVFP4_ERR_SHAPE: return "unsupported or inconsistent shape";
+    case NVFP4_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case NVFP4_ERR_WORKSPACE: return "workspace missing or too small";
+    case NVFP4_ERR_NONFINITE: return "non-finite input";
+    case NVFP4_ERR_TIMEOUT: return "device-side wait timed out";
+    case NVFP4_ERR_CUDA: return "CUDA error";
+    case NVFP4_ERR_UNSUPPORTED: return "unsupported device or size";
+  }
+  return "unknown status";
+}
+
+const char* nvfp4_last_error(void) { return t_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,33 @@
+// kernels.h -- host-side launchers of the NVFP4 kernels (internal to the library).
+#pragma once
+
+#include <algorithm>
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace nvfp4 {
+
+// Maximum number of per-CTA amax partials (sizes the quantiser workspace).
+constexpr int kMaxAmaxPartials = 1024;
+
+size_t quant_workspace_bytes();
+
+// Tensor amax + quantisation (FourOverSix when `fos`, else M=6 only).
+cudaError_t launch_quantize(const void* x, int64_t rows, int64_t K, float divisor, bool fos,
+                            uint8_t* codes, uint8_t* scales, uint8_t* scales_mma, float* ts,
+                            uint8_t* choice, unsigned long long* m4_count, void* workspace,
+                            unsigned int* status, int num_sms, cudaStream_t stream);
+
+// W4A16: Y[M, N] = X[M, K] * dequant(W)^T.
+cudaError_t launch_gemm_w4a16(const void* x, int64_t M, const uint8_t* codes,
+                              const uint8_t* scales_mma, const float* ts, int64_t N, int64_t K,
+                              void* y, bool out_f32, int num_sms, cudaStream_t stream);
+
+// W4A4: block-scaled FP4 tensor-core GEMM.
+cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma, const float* a_ts,
+                             int64_t M, const uint8_t* w_codes, const uint8_t* w_scales_mma,
+                             const float* w_ts, int64_t N, int64_t K, void* y, bool out_f32,
+                             unsigned int* status, int num_sms, cudaStream_t stream);
+
+}  // namespace nvfp4

@@ -77,6 +77,8 @@ def _load():
         lib.oracle_quantize_fos.argtypes = [u16p, i64, i64, ctypes.c_float, u8p, u8p, u8p, f32p,
                                             ctypes.POINTER(ctypes.c_uint64)]
         lib.oracle_quantize_fos.restype = ctypes.c_int
+        lib.oracle_quantize_rows.argtypes = [u16p, i64, i64, ctypes.c_float, ctypes.c_int, u8p, u8p, u8p]
+        lib.oracle_quantize_rows.restype = ctypes.c_uint64
         lib.oracle_quantize_act.argtypes = [u16p, i64, i64, ctypes.c_float, u8p, u8p, f32p]
         lib.oracle_quantize_act.restype = ctypes.c_int
         lib.oracle_scales_mma_bytes.argtypes = [i64, i64]
@@ -188,6 +190,32 @@ def quantize_fos(w_bits: np.ndarray, divisor: float = DEFAULT_DIVISOR) -> dict:
     if st:
         raise OracleError(st)
     return dict(codes=codes, scales=scales, choice=choice, ts=ts.value, m4_count=m4.value)
+
+
+def quantize_rows(x_bits: np.ndarray, ts: float, fos: bool, threads: int = 1) -> dict:
+    """Quantise every row of a bf16 matrix with a given tensor scale (FourOverSix
+    when `fos`, else M=6 only).  Rows are independent, so they may be split
+    across threads (the C call releases the GIL); the result does not depend on
+    the split."""
+    import concurrent.futures as cf
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    R, K = x_bits.shape
+    codes = np.zeros((R, K // 2), np.uint8)
+    scales = np.zeros((R, K // 16), np.uint8)
+    choice = np.zeros((R, K // 16), np.uint8)
+    lib = _load()
+    bounds = np.linspace(0, R, max(1, min(threads, R)) + 1).astype(np.int64)
+
+    def run(i):
+        a, b = int(bounds[i]), int(bounds[i + 1])
+        if a == b:
+            return 0
+        return lib.oracle_quantize_rows(_ptr(x_bits[a:b], ctypes.c_uint16), b - a, K, ts, int(fos),
+                                        _ptr(codes[a:b], ctypes.c_uint8), _ptr(scales[a:b], ctypes.c_uint8),
+                                        _ptr(choice[a:b], ctypes.c_uint8))
+    with cf.ThreadPoolExecutor(max_workers=len(bounds) - 1) as ex:
+        m4 = sum(ex.map(run, range(len(bounds) - 1)))
+    return dict(codes=codes, scales=scales, choice=choice, ts=ts, m4_count=int(m4))
 
 
 def quantize_act(x_bits: np.ndarray, divisor: float = DEFAULT_DIVISOR) -> dict:

@@ -216,6 +216,34 @@ static void pack_codes(const uint8_t q[16], uint8_t* out8) {
   for (int j = 0; j < 8; ++j) out8[j] = (uint8_t)((q[2 * j] & 15) | ((q[2 * j + 1] & 15) << 4));
 }
 
+/* Quantise rows of a bf16 matrix with a given tensor scale: FourOverSix when
+ * fos != 0, otherwise the standard M=6 scale only.  codes [rows, K/2],
+ * scales [rows, K/16], choice [rows, K/16] (nullable).  Returns the number of
+ * blocks that took M=4. */
+uint64_t oracle_quantize_rows(const uint16_t* X, int64_t rows, int64_t K, float ts, int fos,
+                              uint8_t* codes, uint8_t* scales, uint8_t* choice) {
+  uint64_t count = 0;
+  int64_t nb = K / 16;
+  for (int64_t n = 0; n < rows; ++n) {
+    for (int64_t b = 0; b < nb; ++b) {
+      float x[16];
+      for (int i = 0; i < 16; ++i) x[i] = oracle_bf16_value(X[n * K + b * 16 + i]);
+      uint8_t q[16], s, c = 0;
+      if (fos) {
+        oracle_fos_block(x, ts, q, &s, &c, NULL, NULL, NULL, NULL);
+      } else {
+        s = oracle_block_scale_m6(x, ts);
+        (void)oracle_block_sse(x, s, ts, q);
+      }
+      pack_codes(q, codes + n * (K / 2) + b * 8);
+      scales[n * nb + b] = s;
+      if (choice) choice[n * nb + b] = c;
+      count += c;
+    }
+  }
+  return count;
+}
+
 /* FourOverSix NVFP4 weight quantisation of W [N, K] (bf16 bits, row-major).
  * codes [N, K/2], scales [N, K/16] (E4M3 bytes, row-major), choice [N, K/16]
  * (nullable, 1 = M4), m4_count (nullable). */
@@ -227,20 +255,7 @@ int oracle_quantize_fos(const uint16_t* W, int64_t N, int64_t K, float divisor,
   int st = oracle_tensor_scale(W, N * K, divisor, &ts);
   if (st != OR_OK) return st;
   *ts_out = ts;
-  uint64_t count = 0;
-  int64_t nb = K / 16;
-  for (int64_t n = 0; n < N; ++n) {
-    for (int64_t b = 0; b < nb; ++b) {
-      float x[16];
-      for (int i = 0; i < 16; ++i) x[i] = oracle_bf16_value(W[n * K + b * 16 + i]);
-      uint8_t q[16], s, c;
-      oracle_fos_block(x, ts, q, &s, &c, NULL, NULL, NULL, NULL);
-      pack_codes(q, codes + n * (K / 2) + b * 8);
-      scales[n * nb + b] = s;
-      if (choice) choice[n * nb + b] = c;
-      count += c;
-    }
-  }
+  uint64_t count = oracle_quantize_rows(W, N, K, ts, 1, codes, scales, choice);
   if (m4_count) *m4_count = count;
   return OR_OK;
 }
@@ -253,18 +268,7 @@ int oracle_quantize_act(const uint16_t* X, int64_t M, int64_t K, float divisor,
   int st = oracle_tensor_scale(X, M * K, divisor, &ts);
   if (st != OR_OK) return st;
   *ts_out = ts;
-  int64_t nb = K / 16;
-  for (int64_t m = 0; m < M; ++m) {
-    for (int64_t b = 0; b < nb; ++b) {
-      float x[16];
-      for (int i = 0; i < 16; ++i) x[i] = oracle_bf16_value(X[m * K + b * 16 + i]);
-      uint8_t q[16];
-      uint8_t s = oracle_block_scale_m6(x, ts);
-      (void)oracle_block_sse(x, s, ts, q);
-      pack_codes(q, codes + m * (K / 2) + b * 8);
-      scales[m * nb + b] = s;
-    }
-  }
+  (void)oracle_quantize_rows(X, M, K, ts, 0, codes, scales, NULL);
   return OR_OK;
 }
 

@@ -1,0 +1,131 @@
+"""The C ABI without a GPU: the library builds, loads and exports every
+function include/nvfp4.h declares; host-only calls and argument checks work
+and return their status before anything touches the device."""
+import ctypes
+
+import pytest
+
+import nvfp4_weight_quantized_gb300 as nv
+from nvfp4_weight_quantized_gb300 import build as nvbuild
+
+
+@pytest.fixture(scope="module")
+def L():
+    nvbuild.build()
+    return nv.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = nv.declared_functions()
+    assert {"nvfp4_quantize_fos", "nvfp4_quantize_act", "nvfp4_gemm_w4a16", "nvfp4_gemm_w4a4",
+            "nvfp4_linear", "nvfp4_scales_mma_bytes", "nvfp4_workspace_bytes", "nvfp4_set_crossover",
+            "nvfp4_get_crossover", "nvfp4_get_device_status", "nvfp4_status_string",
+            "nvfp4_last_error"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in nvfp4.h but not exported"
+
+
+def test_scales_mma_bytes(L):
+    assert nv.nvfp4_scales_mma_bytes(128, 64) == 512
+    assert nv.nvfp4_scales_mma_bytes(129, 64) == 1024
+    assert nv.nvfp4_scales_mma_bytes(4096, 4096) == 32 * 64 * 512 == 4096 * 4096 // 16
+    assert nv.nvfp4_scales_mma_bytes(1, 80) == 2 * 512
+    assert nv.nvfp4_scales_mma_bytes(0, 64) == 0 and nv.nvfp4_scales_mma_bytes(4, 24) == 0
+
+
+def test_workspace_bytes(L):
+    assert nv.nvfp4_workspace_bytes(nv.OP_QUANTIZE_FOS, 0, 4096, 4096) >= 4096
+    assert nv.nvfp4_workspace_bytes(nv.OP_GEMM_W4A16, 8, 4096, 4096) == 0
+    lin = nv.nvfp4_workspace_bytes(nv.OP_LINEAR, 1024, 11008, 4096)
+    assert lin >= 1024 * 2048 + nv.nvfp4_scales_mma_bytes(1024, 4096)
+    assert nv.nvfp4_workspace_bytes(99, 1, 1, 64) == 0
+
+
+def test_crossover_table(L):
+    default = nv.nvfp4_get_crossover()
+    assert default >= 1
+    nv.nvfp4_set_crossover(4096, 4096, 17)
+    assert nv.nvfp4_get_crossover(4096, 4096) == 17
+    assert nv.nvfp4_get_crossover(4096, 11008) == default
+    with pytest.raises(nv.NVFP4Error):
+        nv.nvfp4_set_crossover(1, 1, -1)
+    nv.nvfp4_set_crossover(4096, 4096, default)
+
+
+def test_status_strings(L):
+    for s in range(9):
+        assert nv.nvfp4_status_string(s)
+    assert "unknown" in nv.nvfp4_status_string(123)
+
+
+FAKE = 0x100000  # a 16-byte aligned host-side integer; never dereferenced
+
+
+def _q(L, W=FAKE, N=4, K=64, codes=FAKE, scales=FAKE, smma=FAKE, ts=FAKE, choice=None, m4=None,
+       ws=FAKE, wsb=1 << 20):
+    return L.nvfp4_quantize_fos(W, N, K, 0.0, codes, scales, smma, ts, choice, m4, ws, wsb, None)
+
+
+def test_quantize_argument_errors(L):
+    assert _q(L, W=None) == nv.ERR_INVALID_ARG
+    assert _q(L, codes=None) == nv.ERR_INVALID_ARG
+    assert _q(L, ts=None) == nv.ERR_INVALID_ARG
+    assert _q(L, scales=None, smma=None) == nv.ERR_INVALID_ARG
+    assert _q(L, K=24) == nv.ERR_SHAPE
+    assert _q(L, K=0) == nv.ERR_SHAPE
+    assert _q(L, N=0) == nv.ERR_SHAPE
+    assert _q(L, N=-3) == nv.ERR_SHAPE
+    assert _q(L, W=FAKE + 8) == nv.ERR_ALIGN
+    assert _q(L, codes=FAKE + 4) == nv.ERR_ALIGN
+    assert _q(L, ts=FAKE + 2) == nv.ERR_ALIGN
+    assert _q(L, ws=None) == nv.ERR_WORKSPACE
+    assert _q(L, wsb=16) == nv.ERR_WORKSPACE
+    assert L.nvfp4_quantize_act(FAKE, 2, 40, 0.0, FAKE, None, FAKE, FAKE, FAKE, 1 << 20, None) == nv.ERR_SHAPE
+    assert L.nvfp4_last_error()
+
+
+def _w(codes=FAKE, smma=FAKE, ts=FAKE, N=256, K=512):
+    return nv._Weight(codes, smma, ts, N, K)
+
+
+def test_gemm_argument_errors(L):
+    g16 = L.nvfp4_gemm_w4a16
+    assert g16(FAKE, 4, None, FAKE, 0, None, 0, None) == nv.ERR_INVALID_ARG
+    assert g16(FAKE, 4, ctypes.byref(_w(codes=None)), FAKE, 0, None, 0, None) == nv.ERR_INVALID_ARG
+    assert g16(FAKE, 4, ctypes.byref(_w(K=48)), FAKE, 0, None, 0, None) == nv.ERR_SHAPE
+    assert g16(FAKE, 4, ctypes.byref(_w(N=0)), FAKE, 0, None, 0, None) == nv.ERR_SHAPE
+    assert g16(FAKE, 4, ctypes.byref(_w(codes=FAKE + 1)), FAKE, 0, None, 0, None) == nv.ERR_ALIGN
+    assert g16(FAKE, -1, ctypes.byref(_w()), FAKE, 0, None, 0, None) == nv.ERR_SHAPE
+    assert g16(FAKE, 4, ctypes.byref(_w()), FAKE, 7, None, 0, None) == nv.ERR_INVALID_ARG
+    assert g16(FAKE + 8, 4, ctypes.byref(_w()), FAKE, 0, None, 0, None) == nv.ERR_ALIGN
+    assert g16(None, 4, ctypes.byref(_w()), FAKE, 0, None, 0, None) == nv.ERR_INVALID_ARG
+    # M == 0 is a no-op that succeeds without touching the device
+    assert g16(None, 0, ctypes.byref(_w()), None, 0, None, 0, None) == nv.OK
+    g4 = L.nvfp4_gemm_w4a4
+    assert g4(None, FAKE, FAKE, 4, ctypes.byref(_w()), FAKE, 0, None, 0, None) == nv.ERR_INVALID_ARG
+    assert g4(FAKE, FAKE, FAKE + 2, 4, ctypes.byref(_w()), FAKE, 0, None, 0, None) == nv.ERR_ALIGN
+    assert g4(FAKE, FAKE, FAKE, 0, ctypes.byref(_w()), None, 0, None, 0, None) == nv.OK
+
+
+def test_linear_workspace_errors(L):
+    nv.nvfp4_set_crossover(256, 512, 8)
+    try:
+        lin = L.nvfp4_linear
+        # above the crossover the W4A4 branch needs the workspace
+        assert lin(FAKE, 100, ctypes.byref(_w()), FAKE, 0, None, 0, None) == nv.ERR_WORKSPACE
+        assert lin(FAKE, 100, ctypes.byref(_w()), FAKE, 0, FAKE + 16, 1 << 30, None) == nv.ERR_WORKSPACE
+        assert lin(FAKE, 100, ctypes.byref(_w()), FAKE, 0, FAKE, 16, None) == nv.ERR_WORKSPACE
+    finally:
+        nv.nvfp4_set_crossover(256, 512, nv.nvfp4_get_crossover())
+
+
+def test_product_path_has_no_oracle_dependency():
+    """The binding and the CUDA sources never load the oracle."""
+    import glob
+    import os
+    import re
+    pkg = os.path.dirname(nv.__file__)
+    pat = re.compile(r"^\s*(import\s+oracle|from\s+oracle)|liboracle|nvfp4_oracle|oracle/", re.M)
+    for path in glob.glob(os.path.join(pkg, "**", "*"), recursive=True):
+        if path.endswith((".py", ".cu", ".cuh", ".h")):
+            assert not pat.search(open(path).read()), path

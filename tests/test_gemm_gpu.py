@@ -1,0 +1,152 @@
+"""W4A16 and W4A4 GEMMs on the GPU against the binary64 oracle.
+
+The GEMMs are fed operands quantised by the oracle, so these tests check the
+GEMM kernels alone (the quantisers have their own bit-exact tests)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from nvfp4_testutil import THREADS, assert_gemm_close, oracle_w4a16, oracle_w4a4, to_dev, y_to_np
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+import nvfp4_weight_quantized_gb300 as nv  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from nvfp4_weight_quantized_gb300 import build
+    build.build()
+    nv.lib()
+
+
+def oracle_weight(w_bits):
+    ts = oracle.tensor_scale(w_bits)
+    return oracle.quantize_rows(w_bits, ts, True, THREADS)
+
+
+def oracle_act(x_bits):
+    ts = oracle.tensor_scale(x_bits)
+    return oracle.quantize_rows(x_bits, ts, False, THREADS)
+
+
+def dev_weight(ref, K):
+    N = ref["codes"].shape[0]
+    return nv.NVFP4Weight(
+        codes=torch.from_numpy(ref["codes"]).cuda(),
+        scales_mma=torch.from_numpy(oracle.scales_to_mma(ref["scales"], K)).cuda(),
+        tensor_scale=torch.tensor([ref["ts"]], dtype=torch.float32).cuda(), N=N, K=K)
+
+
+def dev_act(ref, K):
+    M = ref["codes"].shape[0]
+    return nv.NVFP4Act(
+        codes=torch.from_numpy(ref["codes"]).cuda(),
+        scales_mma=torch.from_numpy(oracle.scales_to_mma(ref["scales"], K)).cuda(),
+        tensor_scale=torch.tensor([ref["ts"]], dtype=torch.float32).cuda(), M=M, K=K)
+
+
+def sample_rows(n, k, seed):
+    rng = np.random.default_rng(seed)
+    if k >= n:
+        return np.arange(n)
+    s = set(rng.choice(n, size=k - 4, replace=False).tolist()) | {0, 1, n - 2, n - 1}
+    return np.array(sorted(s))
+
+
+def run_w4a16(x_bits, wref, K, out_dtype=nv.OUT_BF16, n_rows=None):
+    W = dev_weight(wref, K)
+    y = nv.nvfp4_gemm_w4a16(to_dev(x_bits), W, out_dtype)
+    torch.cuda.synchronize()
+    y = y_to_np(y)
+    ref = oracle_w4a16(x_bits, wref["codes"], wref["scales"], wref["ts"], n_rows=n_rows)
+    if n_rows is not None:
+        y = y[:, n_rows]
+    return assert_gemm_close(y, ref, bf16=out_dtype == nv.OUT_BF16, what=f"w4a16 M={x_bits.shape[0]}")
+
+
+def run_w4a4(x_bits, wref, K, out_dtype=nv.OUT_BF16, m_rows=None, n_rows=None):
+    aref = oracle_act(x_bits)
+    W = dev_weight(wref, K)
+    A = dev_act(aref, K)
+    y = y_to_np(nv.nvfp4_gemm_w4a4(A, W, out_dtype))
+    torch.cuda.synchronize()
+    ref = oracle_w4a4(aref["codes"], aref["scales"], aref["ts"], wref["codes"], wref["scales"], wref["ts"],
+                      m_rows=m_rows, n_rows=n_rows)
+    if m_rows is not None:
+        y = y[m_rows]
+    if n_rows is not None:
+        y = y[:, n_rows]
+    return assert_gemm_close(y, ref, bf16=out_dtype == nv.OUT_BF16, what=f"w4a4 M={x_bits.shape[0]}")
+
+
+# ----------------------------------------------------------------- W4A16 ---
+
+def test_w4a16_tiny_case():
+    w, x = synth.tiny_case()
+    wref = oracle_weight(w)
+    for od in (nv.OUT_BF16, nv.OUT_F32):
+        run_w4a16(x, wref, 512, od)
+
+
+@pytest.mark.parametrize("shape", [(200, 320), (1, 64), (129, 1024), (256, 4160)])
+@pytest.mark.parametrize("M", [1, 5, 13, 64, 70, 129])
+def test_w4a16_ragged(shape, M):
+    N, K = shape
+    wref = oracle_weight(synth.weight_normal(N, K, seed=N + K, outlier_frac=0.01))
+    x = synth.act_normal(M, K, seed=M)
+    run_w4a16(x, wref, K, nv.OUT_F32)
+    run_w4a16(x, wref, K, nv.OUT_BF16)
+
+
+def test_w4a16_decode_shapes():
+    wref = oracle_weight(synth.decode_weight())
+    cols = sample_rows(4096, 384, 1)
+    for M in synth.DECODE_M:
+        worst = run_w4a16(synth.decode_act(M), wref, 4096, nv.OUT_BF16, n_rows=cols)
+        worst32 = run_w4a16(synth.decode_act(M), wref, 4096, nv.OUT_F32, n_rows=cols)
+        print(f"decode M={M}: worst normwise rel err bf16 {worst:.2e} fp32 {worst32:.2e}")
+
+
+def test_w4a16_mlp_shapes():
+    gate_up, down = synth.mlp_weights()
+    for w, K, seed in ((gate_up, 4096, 310), (down, 11008, 311)):
+        wref = oracle_weight(w)
+        cols = sample_rows(w.shape[0], 256, seed)
+        for M in synth.MLP_M:
+            x = synth.act_normal(M, K, seed=seed * 10 + M)
+            run_w4a16(x, wref, K, nv.OUT_BF16, n_rows=cols)
+
+
+def test_w4a16_zero_rows():
+    wref = oracle_weight(synth.weight_normal(64, 256, seed=4))
+    x = np.zeros((3, 256), np.uint16)
+    W = dev_weight(wref, 256)
+    y = nv.nvfp4_gemm_w4a16(to_dev(x), W, nv.OUT_F32)
+    assert float(y.abs().max()) == 0.0
+    y0 = nv.nvfp4_gemm_w4a16(to_dev(np.zeros((0, 256), np.uint16)), W)
+    assert y0.shape == (0, 64)
+
+
+# ------------------------------------------------------------------ W4A4 ---
+
+@pytest.mark.parametrize("shape", [(256, 256), (200, 320), (300, 512), (520, 1024)])
+@pytest.mark.parametrize("M", [1, 5, 128, 130])
+def test_w4a4_small(shape, M):
+    N, K = shape
+    wref = oracle_weight(synth.weight_normal(N, K, seed=N * 3 + K, outlier_frac=0.01))
+    x = synth.act_student_t(M, K, seed=M + 1000)
+    run_w4a4(x, wref, K, nv.OUT_F32)
+    run_w4a4(x, wref, K, nv.OUT_BF16)
+
+
+def test_w4a4_prefill_shapes():
+    wref = oracle_weight(synth.prefill_weight())
+    cols = sample_rows(11008, 256, 2)
+    for M in synth.PREFILL_M:
+        x = synth.prefill_act(M)
+        rows = None if M <= 256 else sample_rows(M, 64, M)
+        worst = run_w4a4(x, wref, 4096, nv.OUT_BF16, m_rows=rows, n_rows=cols)
+        print(f"prefill M={M}: worst normwise rel err {worst:.2e}")

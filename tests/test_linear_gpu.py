@@ -1,0 +1,66 @@
+"""nvfp4_linear: the M-based dispatch between the W4A16 and W4A4 paths, end
+to end from bf16 activations, against the oracle and against the two paths
+called directly."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from nvfp4_testutil import THREADS, assert_gemm_close, oracle_w4a16, oracle_w4a4, to_dev, y_to_np
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+import nvfp4_weight_quantized_gb300 as nv  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from nvfp4_weight_quantized_gb300 import build
+    build.build()
+    nv.lib()
+
+
+def test_dispatch_follows_crossover():
+    N, K = 384, 1024
+    w = synth.weight_normal(N, K, seed=91, outlier_frac=0.01)
+    W = nv.nvfp4_quantize_fos(to_dev(w))
+    old = nv.nvfp4_get_crossover(N, K)
+    nv.nvfp4_set_crossover(N, K, 40)
+    try:
+        for M in (1, 40, 41, 200):
+            x = synth.act_student_t(M, K, seed=M)
+            X = to_dev(x)
+            y = nv.nvfp4_linear(X, W, nv.OUT_F32)
+            if M <= 40:
+                direct = nv.nvfp4_gemm_w4a16(X, W, nv.OUT_F32)
+            else:
+                direct = nv.nvfp4_gemm_w4a4(nv.nvfp4_quantize_act(X), W, nv.OUT_F32)
+            torch.cuda.synchronize()
+            assert torch.equal(y, direct), M
+            # end to end against the oracle on the same path
+            wts = oracle.tensor_scale(w)
+            wref = oracle.quantize_rows(w, wts, True, THREADS)
+            if M <= 40:
+                ref = oracle_w4a16(x, wref["codes"], wref["scales"], wref["ts"])
+            else:
+                aref = oracle.quantize_rows(x, oracle.tensor_scale(x), False, THREADS)
+                ref = oracle_w4a4(aref["codes"], aref["scales"], aref["ts"], wref["codes"], wref["scales"],
+                                  wref["ts"])
+            assert_gemm_close(y_to_np(y), ref, bf16=False, what=f"linear M={M}")
+    finally:
+        nv.nvfp4_set_crossover(N, K, old)
+
+
+def test_linear_small_k_always_takes_w4a16():
+    N, K = 64, 128  # below one 256-wide K stage of the tensor-core kernel
+    w = synth.weight_normal(N, K, seed=5)
+    W = nv.nvfp4_quantize_fos(to_dev(w))
+    x = to_dev(synth.act_normal(300, K, seed=6))
+    y = nv.nvfp4_linear(x, W, nv.OUT_F32)
+    assert torch.equal(y, nv.nvfp4_gemm_w4a16(x, W, nv.OUT_F32))
+
+
+def test_default_crossover_is_sane():
+    c = nv.nvfp4_get_crossover()
+    assert 1 <= c <= 4096

@@ -1,0 +1,161 @@
+"""Quantisers on the GPU against the CPU oracle: bit-exact codes, scales
+(logical and MMA tiling), M=4/M=6 choices, M=4 counts and tensor scales."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from nvfp4_testutil import THREADS, to_dev, to_np_u8
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+import nvfp4_weight_quantized_gb300 as nv  # noqa: E402
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from nvfp4_weight_quantized_gb300 import build
+    build.build()
+    nv.lib()
+
+
+def _f32_bits(v):
+    return np.float32(v).view(np.uint32)
+
+
+def check_fos(w_bits, divisor=None):
+    N, K = w_bits.shape
+    q = nv.nvfp4_quantize_fos(to_dev(w_bits), 0.0 if divisor is None else divisor)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_get_device_status() == nv.OK
+    ts = oracle.tensor_scale(w_bits, oracle.DEFAULT_DIVISOR if divisor is None else divisor)
+    ref = oracle.quantize_rows(w_bits, ts, True, THREADS)
+    assert _f32_bits(q.tensor_scale.item()) == _f32_bits(ts)
+    np.testing.assert_array_equal(to_np_u8(q.codes), ref["codes"])
+    np.testing.assert_array_equal(to_np_u8(q.scales), ref["scales"])
+    np.testing.assert_array_equal(to_np_u8(q.choice), ref["choice"])
+    np.testing.assert_array_equal(to_np_u8(q.scales_mma), oracle.scales_to_mma(ref["scales"], K))
+    assert int(q.m4_count.item()) == ref["m4_count"]
+    return ref
+
+
+def check_act(x_bits):
+    M, K = x_bits.shape
+    q = nv.nvfp4_quantize_act(to_dev(x_bits), logical_scales=True)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_get_device_status() == nv.OK
+    ts = oracle.tensor_scale(x_bits)
+    ref = oracle.quantize_rows(x_bits, ts, False, THREADS)
+    assert _f32_bits(q.tensor_scale.item()) == _f32_bits(ts)
+    np.testing.assert_array_equal(to_np_u8(q.codes), ref["codes"])
+    np.testing.assert_array_equal(to_np_u8(q.scales), ref["scales"])
+    np.testing.assert_array_equal(to_np_u8(q.scales_mma), oracle.scales_to_mma(ref["scales"], K))
+    return ref
+
+
+def test_tiny_case():
+    w, _ = synth.tiny_case()
+    ref = check_fos(w)
+    assert 0 < ref["m4_count"] < ref["choice"].size
+
+
+def test_decode_weight_4096x4096():
+    ref = check_fos(synth.decode_weight())
+    print(f"decode weight: M=4 fraction {ref['m4_count'] / ref['choice'].size:.4f}")
+
+
+def test_mlp_weights():
+    gate_up, down = synth.mlp_weights()
+    for name, w in (("gate_up", gate_up), ("down", down)):
+        ref = check_fos(w)
+        print(f"{name}: M=4 fraction {ref['m4_count'] / ref['choice'].size:.4f}")
+
+
+@pytest.mark.parametrize("which", range(4), ids=[s[0] for s in synth.MODEL_LAYER_SHAPES])
+def test_model_layer0(which):
+    check_fos(synth.model_layer_weight(0, which))
+
+
+@pytest.mark.parametrize("shape", [(1, 16), (3, 48), (129, 80), (300, 1040), (7, 4112), (2, 16 * 1031)])
+def test_ragged_shapes(shape):
+    N, K = shape
+    check_fos(synth.weight_normal(N, K, seed=N * 7 + K, outlier_frac=0.02))
+    check_act(synth.act_student_t(N, K, seed=N * 11 + K))
+
+
+def test_custom_divisor():
+    w = synth.weight_normal(64, 512, seed=77, outlier_frac=0.02)
+    check_fos(w, divisor=4 * 448.0)
+    check_fos(w, divisor=1000.0)
+
+
+def _golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([c.strip() for c in line.split("|")])
+    return rows
+
+
+def test_worked_examples_on_gpu():
+    """Every hand-computed block with ts = 1 inside one tensor (an extra block
+    holding 2688 = 6 * 448 makes the tensor scale exactly 1)."""
+    rows = [r for r in _golden_rows("fos_worked_examples.txt") if float(r[1]) == 1.0]
+    vals = [[float(v) for v in r[2].split()] for r in rows] + [[2688.0] + [0.0] * 15]
+    w = synth.f32_to_bf16_bits(np.array(vals, np.float32).reshape(1, -1))
+    assert (synth.bf16_bits_to_f32(w).reshape(-1, 16) == np.array(vals, np.float32)).all()
+    check_fos(w)
+    q = nv.nvfp4_quantize_fos(to_dev(w))
+    codes, scales, choice = to_np_u8(q.codes)[0], to_np_u8(q.scales)[0], to_np_u8(q.choice)[0]
+    for b, r in enumerate(rows):
+        assert scales[b] == int(r[8], 16), r[0]
+        assert choice[b] == int(r[7]), r[0]
+        assert list(codes[8 * b:8 * b + 8]) == [int(x, 16) for x in r[9].split()], r[0]
+
+
+def test_exact_ties_on_the_e2m1_grid():
+    """With ts = 1 and power-of-two block scales every E2M1 midpoint is hit
+    exactly, which exercises round-half-to-even in the hardware conversion."""
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    blocks = []
+    for e in range(-6, 7):  # block amax 6 * 2^e -> s6 = 2^e exactly
+        s = 2.0 ** e
+        blk = [6 * s] + [m * s for m in mids] + [-m * s for m in mids] + [0.0]
+        blocks.append(blk)
+    blocks.append([2688.0] + [0.0] * 15)
+    w = synth.f32_to_bf16_bits(np.array(blocks, np.float32).reshape(1, -1))
+    check_fos(w)
+    x = synth.f32_to_bf16_bits(np.array(blocks, np.float32).reshape(2, -1))
+    check_act(x)
+
+
+def test_zero_and_negative_zero():
+    z = np.zeros((4, 64), np.uint16)
+    z[1, 5] = 0x8000
+    z[3, 63] = 0x8000
+    ref = check_fos(z)
+    assert ref["ts"] == 1.0
+
+
+def test_nonfinite_input_sets_device_status():
+    w = synth.weight_normal(32, 64, seed=3)
+    w[7, 9] = 0x7F80  # +inf
+    W = to_dev(w)
+    nv.nvfp4_quantize_fos(W)
+    assert nv.nvfp4_get_device_status() == nv.ERR_NONFINITE
+    assert nv.nvfp4_get_device_status() == nv.OK  # reading clears it
+    w[7, 9] = 0xFFC1  # NaN
+    nv.nvfp4_quantize_act(to_dev(w))
+    assert nv.nvfp4_get_device_status() == nv.ERR_NONFINITE
+
+
+def test_activation_quantiser_prefill_shapes():
+    for M in (64, 256, 1024):
+        check_act(synth.prefill_act(M))
