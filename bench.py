@@ -1,0 +1,495 @@
+"""Benchmark of the NVFP4 linear-layer path on GB300.
+
+One step = one pass of the whole hot path over the decode-shaped workload
+(weight [4096, 4096] bf16, N(0, 0.02^2) with 0.5% outliers x8; activations
+[M, 4096] bf16 N(0, 1) for M in 1, 2, 4, 8, 16, 32, 48):
+  1. FourOverSix quantisation of the bf16 weight (tensor amax + per-block
+     M=4/M=6 selection, codes + MMA-tiled scales),
+  2. nvfp4_linear for every M, which dispatches on the measured crossover to
+     the W4A16 GEMM or to activation quantisation + the W4A4 tensor-core GEMM.
+value = algorithmic bytes of the step / step time (GB/s).  Every kernel reads
+cold data: weights rotate through buffers totalling several times the L2.
+The step is captured in a CUDA graph; kernels are timed with CUDA events on
+the launching stream.  The W4A4 throughput on the prefill workload
+(activations [M, 4096] 0.5*Student-t(4), weight [11008, 4096]) is reported
+alongside.
+
+--impl reference times the CPU oracle (test infrastructure) on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+N_DEC = K_DEC = 4096
+DECODE_M = synth.DECODE_M
+METRIC = "NVFP4 linear: W4A16 GB/s (M<=48), W4A4 TFLOPS (M>48), % of roofline"
+WORKLOAD = "decode-shaped NVFP4 linear: W[4096,4096] bf16 N(0,0.02^2) 0.5% outliers x8; " \
+           "FourOverSix quantise + linear at M in {1,2,4,8,16,32,48}"
+ROT_SLOTS = 64           # quantised-weight slots (9.4 MB each)
+ROT_W = 12               # bf16 weight copies (32 MB each)
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def q_bytes(N, K):   # quantiser: bf16 read once + codes + MMA scales written
+    return N * K * 2 + N * K // 2 + N * K // 16
+
+
+def w4a16_bytes(M, N, K):   # weights (codes + scales) + X + Y
+    return N * K // 2 + N * K // 16 + M * K * 2 + M * N * 2
+
+
+def actq_bytes(M, K):
+    return M * K * 2 + M * K // 2 + M * K // 16
+
+
+def w4a4_bytes(M, N, K):
+    return N * K // 2 + N * K // 16 + M * K // 2 + M * K // 16 + M * N * 2
+
+
+# ------------------------------------------------------------- clock sampler
+
+class ClockSampler:
+    FIELDS = "clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown," \
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown," \
+             "clocks_event_reasons.sw_power_cap,power.draw"
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- our arm ---
+
+def traffic_from_profiles(kernel_key: str, src_file: str):
+    """DRAM bytes per launch of `kernel_key` from the committed ncu summary, or
+    None when the summary is missing or was taken on a different source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_key}.traffic.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if "=" in line and not line.startswith("#"):
+                    k, v = line.strip().split("=", 1)
+                    kv[k.strip()] = v.strip()
+        with open(src_file, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        if kv.get("source_sha") != sha:
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import nvfp4_weight_quantized_gb300 as nv
+    from nvfp4_weight_quantized_gb300 import build
+    build.build()
+    nv.lib()
+
+    hbm_peak, bf16_peak, peak_src = peaks()
+    N, K = N_DEC, K_DEC
+    w_bits = synth.decode_weight()
+    W0 = torch.from_numpy(w_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    Ws = [W0] + [W0.clone() for _ in range(ROT_W - 1)]
+    q0 = nv.nvfp4_quantize_fos(W0, logical_scales=False, choice=True)
+    m4_fraction = float(q0.m4_count.item()) / (N * K // 16)
+    slots = [nv.NVFP4Weight(q0.codes.clone(), q0.scales_mma.clone(), q0.tensor_scale.clone(), N, K)
+             for _ in range(ROT_SLOTS)]
+    qws = torch.empty(nv.nvfp4_workspace_bytes(nv.OP_QUANTIZE_FOS, 0, N, K), dtype=torch.uint8, device=dev)
+    Xs = {M: torch.from_numpy(synth.decode_act(M).view(np.int16)).view(torch.bfloat16).to(dev)
+          for M in DECODE_M}
+    Ys = {M: torch.empty((M, N), dtype=torch.bfloat16, device=dev) for M in DECODE_M}
+    lws = {M: torch.empty(max(nv.nvfp4_workspace_bytes(nv.OP_LINEAR, M, N, K), 256), dtype=torch.uint8,
+                          device=dev) for M in DECODE_M}
+    cross = nv.nvfp4_get_crossover(N, K)
+    paths = {M: ("w4a16" if M <= cross else "w4a4") for M in DECODE_M}
+    launches_per_step = 2 + sum(1 if paths[M] == "w4a16" else 3 for M in DECODE_M)
+
+    stream = torch.cuda.Stream(device=dev)
+    steps_per_cycle = ROT_SLOTS // (len(DECODE_M) + 1)  # 8: slot rotation period
+
+    def quant_into(slot, src):
+        d = slot
+        st = nv.lib().nvfp4_quantize_fos(src.data_ptr(), N, K, 0.0, d.codes.data_ptr(), None,
+                                         d.scales_mma.data_ptr(), d.tensor_scale.data_ptr(), None, None,
+                                         qws.data_ptr(), qws.numel(), stream.cuda_stream)
+        assert st == 0, nv.nvfp4_status_string(st)
+
+    def linear(M, slot):
+        nv.nvfp4_linear(Xs[M], slot, out=Ys[M], workspace=lws[M], stream=stream)
+
+    def step_ops(s):
+        base = (s % steps_per_cycle) * (len(DECODE_M) + 1)
+        quant_into(slots[base], Ws[s % ROT_W])
+        for j, M in enumerate(DECODE_M):
+            linear(M, slots[base + 1 + j])
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    W_steps = max(args.warmup, 3)
+    K_steps = args.steps
+    with torch.cuda.stream(stream):
+        for s in range(steps_per_cycle):  # eager warm-up (also sets kernel attributes)
+            step_ops(s)
+    stream.synchronize()
+    # one graph per position in the slot-rotation cycle
+    graphs = [capture(lambda s=s: step_ops(s)) for s in range(steps_per_cycle)]
+    # per-kernel graphs (for per-kernel durations): each call on its own cold slot
+    reps = 16
+    g_quant = capture(lambda: [quant_into(slots[(i * 9) % ROT_SLOTS], Ws[i % ROT_W]) for i in range(reps)])
+    g_lin = {M: capture(lambda M=M: [linear(M, slots[(i * 9 + 1) % ROT_SLOTS]) for i in range(reps)])
+             for M in DECODE_M}
+    torch.cuda.synchronize()
+
+    def timed(g, n=1):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):  # replay() launches on the current stream
+            e0.record(stream)
+            for _ in range(n):
+                g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) * 1e-3 / n
+
+    with torch.cuda.stream(stream):
+        for s in range(W_steps):
+            graphs[s % steps_per_cycle].replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for s in range(W_steps, W_steps + K_steps):
+            graphs[s % steps_per_cycle].replay()
+        t_end.record(stream)
+    t_end.synchronize()
+    # per-kernel durations, still inside the sampled window
+    q_avg = statistics.median(timed(g_quant) for _ in range(5)) / reps
+    lin_avg = {M: statistics.median(timed(g_lin[M]) for _ in range(5)) / reps for M in DECODE_M}
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    elapsed = t_start.elapsed_time(t_end) * 1e-3
+    if world > 1:
+        t = torch.tensor([elapsed], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+
+    step_bytes = q_bytes(N, K) + sum(
+        w4a16_bytes(M, N, K) if paths[M] == "w4a16" else actq_bytes(M, K) + w4a4_bytes(M, N, K)
+        for M in DECODE_M)
+    ms_per_step = elapsed / K_steps * 1e3
+    value = step_bytes * K_steps * world / elapsed / 1e9
+
+    # dominant kernel family of the step
+    w16_time = sum(lin_avg[M] for M in DECODE_M if paths[M] == "w4a16")
+    w16_bytes = sum(w4a16_bytes(M, N, K) for M in DECODE_M if paths[M] == "w4a16")
+    if w16_time >= q_avg and w16_time > 0:
+        dom = "gemm_w4a16"
+        achieved = w16_bytes / w16_time / 1e9
+        traffic = traffic_from_profiles("w4a16_decode", os.path.join(ROOT, "nvfp4_weight_quantized_gb300",
+                                                                     "csrc", "gemm_w4a16.cu"))
+        launches = sum(1 for M in DECODE_M if paths[M] == "w4a16")
+        if traffic is not None:
+            traffic = traffic  # bytes per launch averaged over the M sweep
+    else:
+        dom = "quantize_fos"
+        achieved = q_bytes(N, K) / q_avg / 1e9
+        traffic = traffic_from_profiles("quantize_fos_decode", os.path.join(
+            ROOT, "nvfp4_weight_quantized_gb300", "csrc", "quant.cu"))
+        launches = 2
+
+    detail = {
+        "quantize_fos_us": round(q_avg * 1e6, 2),
+        "quantize_fos_gbs": round(q_bytes(N, K) / q_avg / 1e9, 1),
+        "m4_block_fraction": round(m4_fraction, 4),
+        "crossover_m": cross,
+        "linear": {str(M): {"path": paths[M], "us": round(lin_avg[M] * 1e6, 2),
+                            "gbs": round((w4a16_bytes(M, N, K) if paths[M] == "w4a16" else
+                                          actq_bytes(M, K) + w4a4_bytes(M, N, K)) / lin_avg[M] / 1e9, 1),
+                            "frac_hbm": round((w4a16_bytes(M, N, K) if paths[M] == "w4a16" else
+                                               actq_bytes(M, K) + w4a4_bytes(M, N, K)) / lin_avg[M] / 1e9
+                                              / hbm_peak, 3)}
+                   for M in DECODE_M},
+    }
+    if not args.no_prefill and rank == 0:
+        detail["w4a4_prefill"] = prefill_sweep(nv, dev, stream)
+
+    e2e = measure_e2e(nv, dev, stream, w_bits, args, step_bytes, paths) if rank == 0 else None
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(sample_rows=args.cpu_rows)
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K_steps,
+        "warmup": W_steps, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp4(e2m1)+e4m3 weights, bf16 act, fp32 acc",
+        "data": "synthetic (seeded numpy PCG64), stands in for real model weights and prompts",
+        "config": {"workload": WORKLOAD, "N": N, "K": K, "M": list(DECODE_M),
+                   "parallelism": f"replicas x{world} (no collective)",
+                   "l2": f"inputs larger than L2: {ROT_W} bf16 weight copies and {ROT_SLOTS} quantised "
+                         f"weight slots rotate (about {(ROT_W * N * K * 2 + ROT_SLOTS * 9437184) / 1e9:.2f} GB)",
+                   "timing": "CUDA graph per step, CUDA events on the launching stream around the replays; "
+                  "per-kernel durations from graphs of 16 calls on cold weight slots"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                     else "fallback 6.8 TB/s", "launches_per_step": launches},
+        "gpu_launches": launches_per_step * K_steps,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "detail": detail,
+    }
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def prefill_sweep(nv, dev, stream):
+    """W4A4 GEMM TFLOPS on the prefill workload (graph of 5 launches each)."""
+    import torch
+    N, K = 11008, 4096
+    wp = torch.from_numpy(synth.prefill_weight().view(np.int16)).view(torch.bfloat16).to(dev)
+    qp = nv.nvfp4_quantize_fos(wp, logical_scales=False, choice=False)
+    res = {}
+    for M in (1024, 4096, 16384):
+        X = torch.from_numpy(synth.prefill_act(M).view(np.int16)).view(torch.bfloat16).to(dev)
+        a = nv.nvfp4_quantize_act(X)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        reps = 5
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                nv.nvfp4_gemm_w4a4(a, qp, out=Y, stream=stream)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for r in range(reps):
+                nv.nvfp4_gemm_w4a4(a, qp, out=Y, stream=stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):  # replay() launches on the current stream
+            g.replay()
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        t = e0.elapsed_time(e1) * 1e-3 / reps
+        res[str(M)] = {"gemm_us": round(t * 1e6, 1), "tflops": round(2 * M * N * K / t / 1e12, 1)}
+    return res
+
+
+def measure_e2e(nv, dev, stream, w_bits, args, step_bytes, paths):
+    """Same step through the public API with host buffers: pinned host ->
+    device copies of the weight and activations, the calls, device -> host
+    copies of the quantised weight and every output, all inside the timed
+    region."""
+    import torch
+    N, K = N_DEC, K_DEC
+    hW = torch.from_numpy(w_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hX = {M: torch.from_numpy(synth.decode_act(M).view(np.int16)).view(torch.bfloat16).pin_memory()
+          for M in DECODE_M}
+    dW = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    dX = {M: torch.empty((M, K), dtype=torch.bfloat16, device=dev) for M in DECODE_M}
+    q = nv.nvfp4_quantize_fos(dW.copy_(hW), logical_scales=False, choice=False)
+    hQc = torch.empty(q.codes.shape, dtype=torch.uint8).pin_memory()
+    hQs = torch.empty(q.scales_mma.shape, dtype=torch.uint8).pin_memory()
+    hY = {M: torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for M in DECODE_M}
+    Y = {M: torch.empty((M, N), dtype=torch.bfloat16, device=dev) for M in DECODE_M}
+    ws = torch.empty(nv.nvfp4_workspace_bytes(nv.OP_QUANTIZE_FOS, 0, N, K), dtype=torch.uint8, device=dev)
+    lws = {M: torch.empty(max(nv.nvfp4_workspace_bytes(nv.OP_LINEAR, M, N, K), 256), dtype=torch.uint8,
+                          device=dev) for M in DECODE_M}
+    h2d = hW.numel() * 2 + sum(hX[M].numel() * 2 for M in DECODE_M)
+    d2h = hQc.numel() + hQs.numel() + sum(hY[M].numel() * 2 for M in DECODE_M)
+
+    def step():
+        dW.copy_(hW, non_blocking=True)
+        for M in DECODE_M:
+            dX[M].copy_(hX[M], non_blocking=True)
+        st = nv.lib().nvfp4_quantize_fos(dW.data_ptr(), N, K, 0.0, q.codes.data_ptr(), None,
+                                         q.scales_mma.data_ptr(), q.tensor_scale.data_ptr(), None, None,
+                                         ws.data_ptr(), ws.numel(), stream.cuda_stream)
+        assert st == 0
+        for M in DECODE_M:
+            nv.nvfp4_linear(dX[M], q, out=Y[M], workspace=lws[M], stream=stream)
+        hQc.copy_(q.codes, non_blocking=True)
+        hQs.copy_(q.scales_mma, non_blocking=True)
+        for M in DECODE_M:
+            hY[M].copy_(Y[M], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+    e1.synchronize()
+    t = e0.elapsed_time(e1) * 1e-3 / args.steps
+    return {"value": round(step_bytes / t / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(t * 1e3, 4)}
+
+
+# ------------------------------------------------------------ CPU oracle ---
+
+def cpu_sample(sample_rows: int):
+    """One bounded oracle pass over `sample_rows` weight rows of the decode
+    workload: quantise those rows (tensor scale from the whole tensor) and
+    compute those output columns of every linear.  Returns (seconds, bytes)."""
+    import oracle
+    w = synth.decode_weight()
+    ts = oracle.tensor_scale(w)
+    rows = w[:sample_rows]
+    t0 = time.perf_counter()
+    q = oracle.quantize_rows(rows, ts, True, threads=1)
+    for M in DECODE_M:
+        oracle.gemm_w4a16(synth.decode_act(M), q["codes"], q["scales"], ts)
+    dt = time.perf_counter() - t0
+    frac = sample_rows / N_DEC
+    nbytes = q_bytes(N_DEC, K_DEC) * frac + sum(w4a16_bytes(M, N_DEC, K_DEC) * frac for M in DECODE_M)
+    return dt, nbytes
+
+
+def cpu_baseline(sample_rows: int = 512):
+    dt, nbytes = cpu_sample(sample_rows)
+    return {"value": round(nbytes / dt / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{sample_rows} of 4096 weight rows: quantise those rows and compute those output "
+                      f"columns for every M (binary64 reference GEMM), single thread, "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    rows = args.cpu_rows_reference
+    for _ in range(args.warmup):
+        cpu_sample(rows)
+    times, nbytes = [], 0
+    for _ in range(args.steps):
+        dt, nbytes = cpu_sample(rows)
+        times.append(dt)
+    t = sum(times)
+    value = nbytes * args.steps / t / 1e9
+    sample = f"{rows} of 4096 weight rows per step (quantise + every M of the binary64 GEMM), single thread"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 quantiser, f64 GEMM",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "N": N_DEC, "K": K_DEC, "M": list(DECODE_M)},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-rows", type=int, default=1024)
+    ap.add_argument("--cpu-rows-reference", type=int, default=64)
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
