@@ -182,6 +182,35 @@ nvfp4_status nvfp4_linear(const void* X, int64_t M, const nvfp4_weight* W, void*
                           int out_dtype, void* workspace, size_t workspace_bytes,
                           cudaStream_t stream);
 
+/* Size of the scratch array built into the library for nvfp4_linear_noalloc
+ * (32 MiB, held on every GPU that loads the library until the process exits). */
+#define NVFP4_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * nvfp4_linear without a caller-provided workspace, for callers that cannot
+ * allocate device memory: code running while a CUDA graph is being captured
+ * (where cudaMalloc is not allowed), plugins inside a host framework that owns
+ * every allocation, embedded runtimes with no device allocator.  The paper has
+ * no counterpart; this is a convenience of this library.
+ *
+ * Same arguments and result as nvfp4_linear, minus the workspace.  The W4A4
+ * branch keeps its scratch (the online-quantised activations) in a fixed
+ * NVFP4_NOALLOC_SCRATCH_BYTES array inside the library; a call whose scratch
+ * need (nvfp4_workspace_bytes(NVFP4_OP_LINEAR, M, N, K)) exceeds it returns
+ * NVFP4_ERR_WORKSPACE with the sizes in nvfp4_last_error().  Roughly, the W4A4
+ * branch needs M * (K/2 + K/16) bytes, so at K = 4096 up to about 14,500 rows
+ * fit; the W4A16 branch needs none.  No allocator is called.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any stream
+ * capture.  All calls share the one array and it keeps the previous call's
+ * contents (nothing in it needs to start at zero): calls that may overlap on
+ * the GPU -- on different streams, or from different threads -- race on it
+ * and must be serialised by the caller.
+ */
+nvfp4_status nvfp4_linear_noalloc(const void* X, int64_t M, const nvfp4_weight* W, void* Y,
+                                  int out_dtype, cudaStream_t stream);
+
 /* Crossover table: the largest M that still takes the W4A16 path for a
  * weight of shape [N, K].  N == 0 and K == 0 set the default used for shapes
  * without an entry.  Thread-safe.  The built-in default comes from a sweep on

@@ -22,7 +22,7 @@ import torch
 __all__ = [
     "NVFP4Error", "NVFP4Weight", "NVFP4Act", "lib", "library_path", "declared_functions",
     "nvfp4_scales_mma_bytes", "nvfp4_workspace_bytes", "nvfp4_quantize_fos", "nvfp4_quantize_act",
-    "nvfp4_gemm_w4a16", "nvfp4_gemm_w4a4", "nvfp4_linear", "nvfp4_set_crossover",
+    "nvfp4_gemm_w4a16", "nvfp4_gemm_w4a4", "nvfp4_linear", "nvfp4_linear_noalloc", "nvfp4_set_crossover",
     "nvfp4_get_crossover", "nvfp4_get_device_status", "nvfp4_status_string",
 ]
 
@@ -71,6 +71,7 @@ def lib() -> ctypes.CDLL:
             "nvfp4_gemm_w4a16": (st, [vp, i64, wp, vp, ctypes.c_int, vp, sz, vp]),
             "nvfp4_gemm_w4a4": (st, [vp, vp, vp, i64, wp, vp, ctypes.c_int, vp, sz, vp]),
             "nvfp4_linear": (st, [vp, i64, wp, vp, ctypes.c_int, vp, sz, vp]),
+            "nvfp4_linear_noalloc": (st, [vp, i64, wp, vp, ctypes.c_int, vp]),
             "nvfp4_set_crossover": (st, [i64, i64, i64]),
             "nvfp4_get_crossover": (i64, [i64, i64]),
             "nvfp4_get_device_status": (st, [vp]),
@@ -252,4 +253,21 @@ def nvfp4_linear(X: torch.Tensor, W: NVFP4Weight, out_dtype: int = OUT_BF16,
     d = W.descriptor()
     _check(lib().nvfp4_linear(X.data_ptr(), M, ctypes.byref(d), Y.data_ptr(), out_dtype, ws.data_ptr(),
                               ws.numel(), _stream(stream)), "nvfp4_linear")
+    return Y
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def nvfp4_linear_noalloc(X: torch.Tensor, W: NVFP4Weight, out_dtype: int = OUT_BF16,
+                         out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """nvfp4_linear with the library's built-in scratch instead of a workspace,
+    for callers that cannot allocate device memory (the output tensor is still
+    the caller's)."""
+    _require_cuda(X, out)
+    M = X.shape[0]
+    Y = _out(M, W.N, out_dtype, X.device, out)
+    d = W.descriptor()
+    _check(lib().nvfp4_linear_noalloc(X.data_ptr(), M, ctypes.byref(d), Y.data_ptr(), out_dtype,
+                                      _stream(stream)), "nvfp4_linear_noalloc")
     return Y

@@ -134,6 +134,10 @@ LinearWs linear_ws_layout(int64_t M, int64_t K) {
 
 }  // namespace
 
+namespace nvfp4 {
+void set_last_error(const char* what) { t_last_error = what; }
+}  // namespace nvfp4
+
 extern "C" {
 
 size_t nvfp4_scales_mma_bytes(int64_t rows, int64_t K) {

@@ -13,6 +13,9 @@ constexpr int kMaxAmaxPartials = 1024;
 
 size_t quant_workspace_bytes();
 
+// Records the text nvfp4_last_error() returns on this thread.
+void set_last_error(const char* what);
+
 // Tensor amax + quantisation (FourOverSix when `fos`, else M=6 only).
 cudaError_t launch_quantize(const void* x, int64_t rows, int64_t K, float divisor, bool fos,
                             uint8_t* codes, uint8_t* scales, uint8_t* scales_mma, float* ts,
