@@ -190,7 +190,8 @@ nvfp4_status nvfp4_gemm_w4a16(const void* X, int64_t M, const nvfp4_weight* W, v
   const DeviceInfo* d = nullptr;
   if ((st = device_info(&d)) != NVFP4_OK) return st;
   cudaError_t err = nvfp4::launch_gemm_w4a16(X, M, W->codes, W->scales_mma, W->tensor_scale, W->N, W->K, Y,
-                                             out_dtype == NVFP4_OUT_F32, d->num_sms, stream);
+                                             out_dtype == NVFP4_OUT_F32, d->status, d->num_sms, stream);
+  if (err == cudaErrorNotSupported) return fail(NVFP4_ERR_UNSUPPORTED, "gemm_w4a16: unsupported size");
   if (err != cudaSuccess) return fail_cuda(err, "gemm_w4a16 launch");
   return NVFP4_OK;
 }

@@ -87,6 +87,16 @@ __device__ __forceinline__ uint4 ld_cached_u4(const void* p) {
   return v;
 }
 
+// Programmatic dependent launch (kernels are launched with
+// cudaLaunchAttributeProgrammaticStreamSerialization): griddep_wait() blocks
+// until the previous grid in the stream has completed and its writes are
+// visible; griddep_launch_dependents() lets the next grid start launching
+// (it still waits for this grid to complete before reading its results).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -137,6 +137,7 @@ w4a4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 
   if (warp == 0 && lane == 0) {
     // ---------------- producer ----------------
+    griddep_wait();  // inputs may be written by the previous kernel in the stream
     for (int ks = 0; ks < kt; ++ks) {
       const int s = ks % kStages;
       const uint32_t round = (uint32_t)(ks / kStages);
@@ -186,6 +187,7 @@ w4a4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       commit(&sm.empty[s]);
     }
     if (!failed) commit(&sm.acc);
+    griddep_launch_dependents();
   }
   __syncwarp();
 
@@ -265,9 +267,17 @@ cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma
   auto kern = out_f32 ? w4a4_kernel<true> : w4a4_kernel<false>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
-  kern<<<grid, kThreads, smem, stream>>>(ma, mb, a_scales_mma, w_scales_mma, a_ts, w_ts, M, N, K, y, status);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, ma, mb, a_scales_mma, w_scales_mma, a_ts, w_ts, M, N, K, y, status);
 }
 
 }  // namespace nvfp4

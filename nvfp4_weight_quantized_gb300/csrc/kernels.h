@@ -25,7 +25,8 @@ cudaError_t launch_quantize(const void* x, int64_t rows, int64_t K, float diviso
 // W4A16: Y[M, N] = X[M, K] * dequant(W)^T.
 cudaError_t launch_gemm_w4a16(const void* x, int64_t M, const uint8_t* codes,
                               const uint8_t* scales_mma, const float* ts, int64_t N, int64_t K,
-                              void* y, bool out_f32, int num_sms, cudaStream_t stream);
+                              void* y, bool out_f32, unsigned int* status, int num_sms,
+                              cudaStream_t stream);
 
 // W4A4: block-scaled FP4 tensor-core GEMM.
 cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma, const float* a_ts,

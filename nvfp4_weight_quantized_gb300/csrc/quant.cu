@@ -45,6 +45,7 @@ __global__ void __launch_bounds__(kThreads)
 amax_partial_kernel(const uint4* __restrict__ x, int64_t n_vec, uint32_t* __restrict__ partial,
                     unsigned long long* __restrict__ counter_to_clear) {
   __shared__ uint32_t red[kThreads / 32];
+  griddep_wait();
   uint32_t m2 = 0;  // two running maxima of bf16 magnitude bits, one per half
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -67,6 +68,7 @@ amax_partial_kernel(const uint4* __restrict__ x, int64_t n_vec, uint32_t* __rest
     m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
     m2 = __vmaxu2(m2, v.w & 0x7FFF7FFFu);
   }
+  griddep_launch_dependents();
   uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
   m = block_reduce_max(m, red);
   if (threadIdx.x == 0) {
@@ -75,32 +77,113 @@ amax_partial_kernel(const uint4* __restrict__ x, int64_t n_vec, uint32_t* __rest
   }
 }
 
-// Quantise one 16-element block with scale value `sv` (binary32 value of the
-// E4M3 byte) and tensor scale ts.  ax[] holds |x|.  Returns the block SSE in
-// the fixed tree order; mags[] receive the E2M1 magnitude codes.
-__device__ __forceinline__ float block_sse(const float (&ax)[16], float sv, float ts,
-                                           uint32_t (&mags)[16]) {
-  const float eff = __fmul_rn(sv, ts);
+// ---- packed binary32 pairs (sm_100-family f32x2 arithmetic, IEEE RN) ----
+typedef unsigned long long f2;
+
+__device__ __forceinline__ f2 pk(float a, float b) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk(f2 v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+  f2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Packed E2M1 pair (byte) -> the two values as a binary32 pair (exact).
+__device__ __forceinline__ f2 e2m1x2_to_f2(uint32_t byte) {
+  uint32_t h;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h) : "r"(byte));
+  float lo, hi;
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi) : "r"(h));
+  return pk(lo, hi);
+}
+
+__device__ __forceinline__ uint32_t pack4(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+  return __byte_perm(__byte_perm(b0, b1, 0x0040u), __byte_perm(b2, b3, 0x0040u), 0x5410u);
+}
+
+// One candidate scale, exact reference path: IEEE binary32 division per
+// element.  x[] are the magnitudes |x| (the code's sign is the sign of x and
+// is attached by the caller; the squared error of a signed value equals that
+// of its magnitude bit for bit); eff = value(scale) * ts.  Returns the block
+// SSE in the fixed tree order and the 16 magnitude codes packed 8 per word,
+// element 0 in the lowest nibble.
+__device__ __noinline__ float cand_exact(const float (&x)[16], float eff, uint32_t (&codes)[2]) {
   float e[16];
-  if (eff == 0.0f) {
+  codes[0] = codes[1] = 0u;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      mags[i] = 0u;
-      e[i] = __fmul_rn(ax[i], ax[i]);
+  for (int i = 0; i < 16; i += 2) {
+    uint32_t p;
+    float xh0, xh1;
+    if (eff == 0.0f) {  // every value quantises to zero
+      p = 0u;
+      xh0 = xh1 = 0.0f;
+    } else {
+      const float r0 = fminf(__fdiv_rn(x[i], eff), 6.0f), r1 = fminf(__fdiv_rn(x[i + 1], eff), 6.0f);
+      p = cvt_e2m1x2(r1, r0);
+      upk(e2m1x2_to_f2(p), xh0, xh1);
+      xh0 = __fmul_rn(xh0, eff);
+      xh1 = __fmul_rn(xh1, eff);
     }
-  } else {
+    codes[i >> 3] |= p << (4 * (i & 7));
+    const float d0 = __fsub_rn(x[i], xh0), d1 = __fsub_rn(x[i + 1], xh1);
+    e[i] = __fmul_rn(d0, d0);
+    e[i + 1] = __fmul_rn(d1, d1);
+  }
+  float a[8], b[4];
 #pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-      float r0 = fminf(__fdiv_rn(ax[i], eff), 6.0f);
-      float r1 = fminf(__fdiv_rn(ax[i + 1], eff), 6.0f);
-      uint32_t p = cvt_e2m1x2(r1, r0);
-      mags[i] = p & 7u;
-      mags[i + 1] = (p >> 4) & 7u;
-      float d0 = __fsub_rn(ax[i], __fmul_rn(e2m1_mag_to_f32(mags[i]), eff));
-      float d1 = __fsub_rn(ax[i + 1], __fmul_rn(e2m1_mag_to_f32(mags[i + 1]), eff));
-      e[i] = __fmul_rn(d0, d0);
-      e[i + 1] = __fmul_rn(d1, d1);
-    }
+  for (int j = 0; j < 8; ++j) a[j] = __fadd_rn(e[j], e[j + 8]);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) b[j] = __fadd_rn(a[j], a[j + 4]);
+  return __fadd_rn(__fadd_rn(b[0], b[2]), __fadd_rn(b[1], b[3]));
+}
+
+// Same result as cand_exact, fast path.  With r = RN(1/eff), the products
+// x * RN(r * (1 -/+ 2^-20)) bracket RN(x / eff) for every element; when the
+// two brackets convert to the same E2M1 code, that code is the code of
+// RN(x / eff) because the conversion is monotone.  If any element of the block
+// is not decided that way (a quotient within ~2^-20 of a rounding midpoint),
+// or eff is outside the safe range, the exact path is taken.  x[] and x2[j]
+// (elements 2j, 2j+1) hold magnitudes; bmax = max |x|.
+__device__ __forceinline__ float cand(const float (&x)[16], const f2 (&x2)[8], float bmax, float eff,
+                                      uint32_t (&codes)[2]) {
+  if (!(eff >= 0x1p-100f)) return cand_exact(x, eff, codes);
+  const float r = __frcp_rn(eff);
+  if (!(__fmul_rn(bmax, r) < 0x1p100f)) return cand_exact(x, eff, codes);
+  const float rlo = __fmul_rn(r, 0.99999904632568359375f);  // 1 - 2^-20
+  const float rhi = __fmul_rn(r, 1.00000095367431640625f);  // 1 + 2^-20
+  const f2 rl2 = pk(rlo, rlo), rh2 = pk(rhi, rhi);
+  uint32_t bl[8], bh[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float l0, l1, h0, h1;
+    upk(mul2(x2[j], rl2), l0, l1);
+    upk(mul2(x2[j], rh2), h0, h1);
+    bl[j] = cvt_e2m1x2(l1, l0);
+    bh[j] = cvt_e2m1x2(h1, h0);
+  }
+  codes[0] = pack4(bl[0], bl[1], bl[2], bl[3]);
+  codes[1] = pack4(bl[4], bl[5], bl[6], bl[7]);
+  const uint32_t hi0 = pack4(bh[0], bh[1], bh[2], bh[3]);
+  const uint32_t hi1 = pack4(bh[4], bh[5], bh[6], bh[7]);
+  if ((codes[0] ^ hi0) | (codes[1] ^ hi1)) return cand_exact(x, eff, codes);
+  // errors with scalar round-to-nearest intrinsics: these are never fused into
+  // multiply-adds, so every step rounds once as written
+  float e[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float v0, v1;
+    upk(e2m1x2_to_f2(bl[j]), v0, v1);
+    const float d0 = __fsub_rn(x[2 * j], __fmul_rn(v0, eff));
+    const float d1 = __fsub_rn(x[2 * j + 1], __fmul_rn(v1, eff));
+    e[2 * j] = __fmul_rn(d0, d0);
+    e[2 * j + 1] = __fmul_rn(d1, d1);
   }
   float a[8], b[4];
 #pragma unroll
@@ -117,6 +200,7 @@ quant_kernel(const uint4* __restrict__ x, int64_t rows, int64_t K, const uint32_
              uint8_t* __restrict__ scales_mma, float* __restrict__ ts_out, uint8_t* __restrict__ choice,
              unsigned long long* __restrict__ m4_count, unsigned int* __restrict__ status) {
   __shared__ uint32_t red[kThreads / 32];
+  griddep_wait();  // the partials come from the amax kernel just before
   uint32_t am = 0;
   for (int i = threadIdx.x; i < n_partial; i += blockDim.x) am = max(am, partial[i]);
   am = block_reduce_max(am, red);
@@ -132,56 +216,73 @@ quant_kernel(const uint4* __restrict__ x, int64_t rows, int64_t K, const uint32_
   const int64_t ct = (kb + 3) >> 2;
   const int64_t nblk = rows * kb;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  // (row, block column) of this thread's block, advanced by the grid stride
+  // without a division inside the loop
+  const int64_t stride_r = stride / kb, stride_c = stride - stride_r * kb;
+  int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  int64_t r = blk / kb, c = blk - r * kb;
   uint32_t n_m4 = 0;
-  for (int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; blk < nblk; blk += stride) {
+  for (; blk < nblk; blk += stride) {
     const uint4 v0 = ld_stream_u4(x + 2 * blk);
     const uint4 v1 = ld_stream_u4(x + 2 * blk + 1);
     const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    float ax[16];
-    uint32_t sign = 0;  // bit i = sign of element i
-    float bmax = 0.0f;
+    float xv[16];  // magnitudes
+    f2 x2[8];
+    uint32_t m2 = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      ax[2 * j] = __uint_as_float((w[j] & 0x7FFFu) << 16);
-      ax[2 * j + 1] = __uint_as_float(w[j] & 0x7FFF0000u);
-      sign |= ((w[j] >> 15) & 1u) << (2 * j);
-      sign |= ((w[j] >> 31) & 1u) << (2 * j + 1);
-      bmax = fmaxf(bmax, fmaxf(ax[2 * j], ax[2 * j + 1]));
+      const uint32_t a = w[j] & 0x7FFF7FFFu;
+      xv[2 * j] = __uint_as_float(a << 16);
+      xv[2 * j + 1] = __uint_as_float(a & 0xFFFF0000u);
+      x2[j] = pk(xv[2 * j], xv[2 * j + 1]);
+      m2 = __vmaxu2(m2, a);
     }
+    // sign bits of the 16 codes: byte j of sgn[h] gets the signs of elements
+    // 8h+2j (bit 3) and 8h+2j+1 (bit 7), i.e. bit 15 and bit 31 of word 4h+j
+    uint32_t sgn[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t g1 = __byte_perm(__byte_perm(w[4 * h], w[4 * h + 1], 0x0051u),
+                                      __byte_perm(w[4 * h + 2], w[4 * h + 3], 0x0051u), 0x5410u);
+      const uint32_t g3 = __byte_perm(__byte_perm(w[4 * h], w[4 * h + 1], 0x0073u),
+                                      __byte_perm(w[4 * h + 2], w[4 * h + 3], 0x0073u), 0x5410u);
+      sgn[h] = ((g1 >> 4) & 0x08080808u) | (g3 & 0x80808080u);
+    }
+    const float bmax = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
     // s6 = E4M3((amax_block / 6) / ts)
     const float r6 = __fdiv_rn(__fdiv_rn(bmax, 6.0f), ts);
     const uint32_t s6 = cvt_e4m3x2(0.0f, r6) & 0xFFu;
-    uint32_t mags[16];
+    const float s6v = e4m3_to_f32(s6);
+    uint32_t cw[2];
+    const float sse6 = cand(xv, x2, bmax, __fmul_rn(s6v, ts), cw);
     uint32_t s = s6;
     if (kFos) {
-      const float s6v = e4m3_to_f32(s6);
       const uint32_t s4 = cvt_e4m3x2(0.0f, __fmul_rn(s6v, 1.5f)) & 0xFFu;
-      uint32_t mags4[16];
-      const float sse6 = block_sse(ax, s6v, ts, mags);
-      const float sse4 = block_sse(ax, e4m3_to_f32(s4), ts, mags4);
-      const bool m4 = sse4 < sse6;
-      if (m4) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) mags[i] = mags4[i];
-        s = s4;
-        ++n_m4;
+      bool m4 = false;
+      if (s4 != s6) {  // equal scales tie, and a tie keeps M=6
+        uint32_t cw4[2];
+        const float sse4 = cand(xv, x2, bmax, __fmul_rn(e4m3_to_f32(s4), ts), cw4);
+        m4 = sse4 < sse6;
+        if (m4) {
+          cw[0] = cw4[0];
+          cw[1] = cw4[1];
+          s = s4;
+          ++n_m4;
+        }
       }
       if (choice != nullptr) choice[blk] = m4 ? 1 : 0;
-    } else {
-      (void)block_sse(ax, e4m3_to_f32(s6), ts, mags);
     }
-    uint32_t lo = 0, hi = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) lo |= (mags[i] | (((sign >> i) & 1u) << 3)) << (4 * i);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) hi |= (mags[8 + i] | (((sign >> (8 + i)) & 1u) << 3)) << (4 * i);
-    *reinterpret_cast<uint2*>(codes + 8 * blk) = make_uint2(lo, hi);
+    *reinterpret_cast<uint2*>(codes + 8 * blk) = make_uint2(cw[0] | sgn[0], cw[1] | sgn[1]);
     if (scales != nullptr) scales[blk] = (uint8_t)s;
-    if (scales_mma != nullptr) {
-      const int64_t r = blk / kb, c = blk - r * kb;
-      scales_mma[scale_mma_offset(r, c, ct)] = (uint8_t)s;
+    if (scales_mma != nullptr) scales_mma[scale_mma_offset(r, c, ct)] = (uint8_t)s;
+    r += stride_r;
+    c += stride_c;
+    if (c >= kb) {
+      c -= kb;
+      ++r;
     }
   }
+  griddep_launch_dependents();
   // zero the padding of the MMA scale tiling (rows up to a multiple of 128,
   // scale columns up to a multiple of 4)
   if (scales_mma != nullptr) {
@@ -220,22 +321,28 @@ cudaError_t launch_quantize(const void* x, int64_t rows, int64_t K, float diviso
   int g1 = (int)std::min<int64_t>((n_vec + kThreads * 4 - 1) / (kThreads * 4), (int64_t)num_sms * 4);
   g1 = std::max(1, std::min(g1, kMaxAmaxPartials));
   uint32_t* partial = static_cast<uint32_t*>(workspace);
-  amax_partial_kernel<<<g1, kThreads, 0, stream>>>(static_cast<const uint4*>(x), n_vec, partial,
-                                                   fos ? m4_count : nullptr);
-  cudaError_t err = cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(g1);
+  cudaError_t err = cudaLaunchKernelEx(&cfg, amax_partial_kernel, static_cast<const uint4*>(x), n_vec, partial,
+                                       fos ? m4_count : (unsigned long long*)nullptr);
   if (err != cudaSuccess) return err;
   const int64_t nblk = rows * (K / 16);
   int g2 = (int)std::min<int64_t>((nblk + kThreads - 1) / kThreads, (int64_t)num_sms * 8);
-  g2 = std::max(g2, 1);
+  cfg.gridDim = dim3(std::max(g2, 1));
   if (fos)
-    quant_kernel<true><<<g2, kThreads, 0, stream>>>(static_cast<const uint4*>(x), rows, K, partial, g1,
-                                                    divisor, codes, scales, scales_mma, ts, choice,
-                                                    m4_count, status);
-  else
-    quant_kernel<false><<<g2, kThreads, 0, stream>>>(static_cast<const uint4*>(x), rows, K, partial, g1,
-                                                     divisor, codes, scales, scales_mma, ts, nullptr,
-                                                     nullptr, status);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, quant_kernel<true>, static_cast<const uint4*>(x), rows, K,
+                              (const uint32_t*)partial, g1, divisor, codes, scales, scales_mma, ts, choice,
+                              m4_count, status);
+  return cudaLaunchKernelEx(&cfg, quant_kernel<false>, static_cast<const uint4*>(x), rows, K,
+                            (const uint32_t*)partial, g1, divisor, codes, scales, scales_mma, ts,
+                            (uint8_t*)nullptr, (unsigned long long*)nullptr, status);
 }
 
 }  // namespace nvfp4
