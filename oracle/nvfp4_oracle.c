@@ -34,10 +34,14 @@
  *       s4  = E4M3(value(s6) * 1.5)
  *       eff = value(s) * ts
  *       q_i = E2M1(x_i / eff)   (q_i = signed zero when eff == 0)
- *       e_i = (x_i - value(q_i) * eff)^2
- *       SSE = ((e_j + e_j+8) pairwise, then +4, +2, +1)  -- a fixed tree
+ *       d_i = x_i - value(q_i) * eff        rounded once (exact product)
+ *       a_j = d_j * d_j + RN(d_j+8 * d_j+8)  rounded once, j < 8
+ *       b_j = a_j + a_j+4,  c_j = b_j + b_j+2,  SSE = c_0 + c_1
  *     and the block keeps s4 iff SSE4 < SSE6 (ties keep M=6).  Comparing
- *     sums is the same as comparing means: division by 16 is exact.
+ *     sums is the same as comparing means: division by 16 is exact.  The
+ *     error and the first level of the square-sum are single-rounding
+ *     (fused) operations: the pages fix no precision or order for the block
+ *     MSE, and this form is the more exact one.
  *   - E4M3 and E2M1 conversions round to nearest, ties to the even code, and
  *     saturate to the largest finite value (448 and 6).  The sign of a code
  *     is the sign of x (so negative values that round to zero give -0).
@@ -137,26 +141,25 @@ uint8_t oracle_e4m3_encode(float v) {
 /* ------------------------------------------------------------------------ */
 
 /* Quantise 16 values with block scale byte s and tensor scale ts; return the
- * block's sum of squared dequantisation errors in the fixed binary32 tree
- * order.  q receives one code per element. */
+ * block's sum of squared dequantisation errors in the fixed binary32 order
+ * described at the top of this file.  q receives one code per element. */
 float oracle_block_sse(const float x[16], uint8_t s, float ts, uint8_t q[16]) {
   float eff = (float)oracle_e4m3_value(s) * ts;
-  float e[16];
+  float d[16];
   for (int i = 0; i < 16; ++i) {
-    float xhat;
     if (eff == 0.0f) {
       q[i] = signbit(x[i]) ? 8 : 0;
-      xhat = 0.0f;
+      d[i] = x[i];
     } else {
       float r = x[i] / eff;
       q[i] = oracle_e2m1_encode(r);
-      xhat = (float)oracle_e2m1_value(q[i]) * eff;
+      /* x - value * eff with one rounding (value * eff is exact in double,
+       * and fmaf rounds the exact result once) */
+      d[i] = fmaf(-(float)oracle_e2m1_value(q[i]), eff, x[i]);
     }
-    float d = x[i] - xhat;
-    e[i] = d * d;
   }
   float a[8], b[4], c[2];
-  for (int j = 0; j < 8; ++j) a[j] = e[j] + e[j + 8];
+  for (int j = 0; j < 8; ++j) a[j] = fmaf(d[j], d[j], d[j + 8] * d[j + 8]);
   for (int j = 0; j < 4; ++j) b[j] = a[j] + a[j + 4];
   for (int j = 0; j < 2; ++j) c[j] = b[j] + b[j + 2];
   return c[0] + c[1];
