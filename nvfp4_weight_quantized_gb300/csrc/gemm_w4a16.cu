@@ -48,8 +48,12 @@ constexpr int kChunkK = 64;          // K per dequant chunk (4 MMAs of K = 16)
 constexpr int kMaxTok = 64;          // tokens per CTA = MMA N (multiple of 16)
 constexpr int kASlots = 4;           // TMEM A buffers (one chunk each)
 constexpr int kDqWarps = 8;          // two dequant warps per 32-lane TMEM quarter
+// Two MMA-issuing warps: one tcgen05.mma stream is bound by its issuer's
+// latency (~110 cycles per K=16 MMA with A in TMEM), and two streams into two
+// accumulators overlap on the tensor core.  Warp kMmaWarp + p issues the
+// chunks with c % 2 == p into accumulator p.
 constexpr int kProducerWarp = kDqWarps, kMmaWarp = kDqWarps + 1;
-constexpr int kThreads = 32 * (kDqWarps + 2);
+constexpr int kThreads = 32 * (kDqWarps + 3);
 constexpr uint32_t kTmemCols = 256;
 // Two accumulators (even / odd K chunks) so consecutive MMAs do not wait on
 // each other's accumulation; the epilogue adds them.
@@ -68,7 +72,7 @@ struct Barriers {
   uint64_t empty[4];
   uint64_t a_full[kASlots];
   uint64_t a_free[kASlots];
-  uint64_t acc;
+  uint64_t acc[2];
   uint32_t tmem_base;
 };
 
@@ -226,13 +230,14 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_con
     prefetch_tmap(&tmap_x);
     for (int s = 0; s < stages; ++s) {
       mbar_init(&bar.full[s], 1);
-      mbar_init(&bar.empty[s], 1);
+      mbar_init(&bar.empty[s], 2);  // one commit per MMA issuer
     }
     for (int a = 0; a < kASlots; ++a) {
       mbar_init(&bar.a_full[a], 4);  // one arrival per dequant warp of a chunk's warp set
       mbar_init(&bar.a_free[a], 1);
     }
-    mbar_init(&bar.acc, 1);
+    mbar_init(&bar.acc[0], 1);
+    mbar_init(&bar.acc[1], 1);
     fence_mbar_init();
     griddep_wait();  // inputs may be written by the previous kernel in the stream
     for (; issued < min(nst, stages); ++issued) issue_stage(issued);
@@ -257,10 +262,12 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_con
       for (int i = max(0, nst - stages); i < nst && !failed; ++i)
         if (!mbar_wait(&bar.full[i % stages], (uint32_t)(i / stages) & 1u)) failed = true;
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp >= kMmaWarp) {
     if (lane == 0) {
-      // ---------------- MMA issuer ----------------
+      // ---------------- MMA issuers (chunks of one parity each) ----------------
+      const int par = warp - kMmaWarp;
       const uint32_t idesc = idesc_bf16(n_tok);
+      const uint32_t dacc = tmem + kAccCol + 64u * par;
       int c = 0;
       for (int i = 0; i < nst && !failed; ++i) {
         const int s = i % stages;
@@ -269,7 +276,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_con
           break;
         }
         const int chunks = min(4, nchunk - 4 * (st_begin + i));
-        for (int q = 0; q < chunks; ++q, ++c) {
+        for (int q = 0; q < chunks && !failed; ++q, ++c) {
+          if ((c & 1) != par) continue;
           const int slot = c % kASlots;
           if (!mbar_wait(&bar.a_full[slot], (uint32_t)(c / kASlots) & 1u)) {
             failed = true;
@@ -277,15 +285,18 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_con
           }
           fence_after_sync();
           const uint64_t bdesc = smem_desc(sbase + L.x(s, q), 0, 1024, 2);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ts(tmem + kAccCol + 64u * (c & 1), tmem + kACol + 32u * slot + 8u * kk, bdesc + 2ull * kk,
-                        idesc, ((c >> 1) | kk) != 0);
+          const uint32_t a = tmem + kACol + 32u * slot;
+          mma_bf16_ts(dacc, a, bdesc, idesc, c >= 2);
+          mma_bf16_ts(dacc, a + 8u, bdesc + 2ull, idesc, 1u);
+          mma_bf16_ts(dacc, a + 16u, bdesc + 4ull, idesc, 1u);
+          mma_bf16_ts(dacc, a + 24u, bdesc + 6ull, idesc, 1u);
           commit(&bar.a_free[slot]);
         }
         commit(&bar.empty[s]);
       }
-      if (!failed) commit(&bar.acc);
+      // the stage buffers are released when both issuers are done with them:
+      // each issuer commits to the stage's empty barrier (count 2)
+      if (!failed) commit(&bar.acc[par]);
       griddep_launch_dependents();
     }
   } else {
@@ -337,7 +348,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_con
   float* red = reinterpret_cast<float*>(base);  // [n_tok][BM] partial tile (split-K)
   bool acc_ok = true;
   if (warp < 4) {
-    acc_ok = __all_sync(0xffffffffu, !failed && (nst == 0 || mbar_wait(&bar.acc, 0)));
+    acc_ok = __all_sync(0xffffffffu, !failed && (nst == 0 || (mbar_wait(&bar.acc[0], 0) && mbar_wait(&bar.acc[1], 0))));
     fence_after_sync();
     const int row = threadIdx.x;
     const int64_t n = n0 + row;

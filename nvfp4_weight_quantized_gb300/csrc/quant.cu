@@ -94,6 +94,17 @@ __device__ __forceinline__ f2 mul2(f2 a, f2 b) {
   return d;
 }
 
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+  f2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+  f2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 // Packed E2M1 pair (byte) -> the two values as a binary32 pair (exact).
 __device__ __forceinline__ f2 e2m1x2_to_f2(uint32_t byte) {
   uint32_t h;
@@ -108,89 +119,72 @@ __device__ __forceinline__ uint32_t pack4(uint32_t b0, uint32_t b1, uint32_t b2,
   return __byte_perm(__byte_perm(b0, b1, 0x0040u), __byte_perm(b2, b3, 0x0040u), 0x5410u);
 }
 
-// One candidate scale, exact reference path: IEEE binary32 division per
-// element.  x[] are the magnitudes |x| (the code's sign is the sign of x and
-// is attached by the caller; the squared error of a signed value equals that
-// of its magnitude bit for bit); eff = value(scale) * ts.  Returns the block
-// SSE in the fixed tree order and the 16 magnitude codes packed 8 per word,
-// element 0 in the lowest nibble.
-__device__ __noinline__ float cand_exact(const float (&x)[16], float eff, uint32_t (&codes)[2]) {
-  float e[16];
-  codes[0] = codes[1] = 0u;
-#pragma unroll
-  for (int i = 0; i < 16; i += 2) {
-    uint32_t p;
-    float xh0, xh1;
-    if (eff == 0.0f) {  // every value quantises to zero
-      p = 0u;
-      xh0 = xh1 = 0.0f;
-    } else {
-      const float r0 = fminf(__fdiv_rn(x[i], eff), 6.0f), r1 = fminf(__fdiv_rn(x[i + 1], eff), 6.0f);
-      p = cvt_e2m1x2(r1, r0);
-      upk(e2m1x2_to_f2(p), xh0, xh1);
-      xh0 = __fmul_rn(xh0, eff);
-      xh1 = __fmul_rn(xh1, eff);
-    }
-    codes[i >> 3] |= p << (4 * (i & 7));
-    const float d0 = __fsub_rn(x[i], xh0), d1 = __fsub_rn(x[i + 1], xh1);
-    e[i] = __fmul_rn(d0, d0);
-    e[i + 1] = __fmul_rn(d1, d1);
-  }
-  float a[8], b[4];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) a[j] = __fadd_rn(e[j], e[j + 8]);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) b[j] = __fadd_rn(a[j], a[j + 4]);
-  return __fadd_rn(__fadd_rn(b[0], b[2]), __fadd_rn(b[1], b[3]));
+// E2M1 codes of two magnitudes from the IEEE binary32 quotients x / eff.
+__device__ __forceinline__ uint32_t exact_pair(float x0, float x1, float eff) {
+  return cvt_e2m1x2(fminf(__fdiv_rn(x1, eff), 6.0f), fminf(__fdiv_rn(x0, eff), 6.0f));
 }
 
-// Same result as cand_exact, fast path.  With r = RN(1/eff), the products
-// x * RN(r * (1 -/+ 2^-20)) bracket RN(x / eff) for every element; when the
-// two brackets convert to the same E2M1 code, that code is the code of
-// RN(x / eff) because the conversion is monotone.  If any element of the block
-// is not decided that way (a quotient within ~2^-20 of a rounding midpoint),
-// or eff is outside the safe range, the exact path is taken.  x[] and x2[j]
-// (elements 2j, 2j+1) hold magnitudes; bmax = max |x|.
-__device__ __forceinline__ float cand(const float (&x)[16], const f2 (&x2)[8], float bmax, float eff,
-                                      uint32_t (&codes)[2]) {
-  if (!(eff >= 0x1p-100f)) return cand_exact(x, eff, codes);
-  const float r = __frcp_rn(eff);
-  if (!(__fmul_rn(bmax, r) < 0x1p100f)) return cand_exact(x, eff, codes);
-  const float rlo = __fmul_rn(r, 0.99999904632568359375f);  // 1 - 2^-20
-  const float rhi = __fmul_rn(r, 1.00000095367431640625f);  // 1 + 2^-20
-  const f2 rl2 = pk(rlo, rlo), rh2 = pk(rhi, rhi);
-  uint32_t bl[8], bh[8];
+// One candidate scale for a block of 16 magnitudes (x2[j] = elements 2j,
+// 2j+1); eff = value(scale) * ts, bmax = max |x|.  Returns the block SSE and
+// the 16 magnitude codes packed 8 per word (element 0 in the lowest nibble);
+// the caller attaches the signs (the squared error of x equals that of |x|).
+//
+// Codes: with r = RN(1/eff), the products x * RN(r * (1 -/+ 2^-20)) bracket
+// RN(x / eff); when both ends convert to the same E2M1 code, that is the code
+// of RN(x / eff) (the conversion is monotone).  A pair whose ends differ (its
+// quotient lies within ~2^-20 of a rounding midpoint -- common, since x and
+// eff often share small factors) takes the IEEE division instead, as does a
+// whole block whose eff is outside the range where the bracket is safe.
+// Errors: d = RN(x - value * eff) (one fused step), then
+// a_j = RN(d_j^2 + RN(d_j+8^2)), b_j = a_j + a_j+4, c_j = b_j + b_j+2,
+// SSE = c_0 + c_1.  A product only ever feeds the addend of an explicit fma,
+// so no compiler contraction can change the rounding.
+__device__ __forceinline__ float cand(const f2 (&x2)[8], float bmax, float eff, uint32_t (&codes)[2]) {
+  uint32_t bl[8];
+  if (eff == 0.0f) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    float l0, l1, h0, h1;
-    upk(mul2(x2[j], rl2), l0, l1);
-    upk(mul2(x2[j], rh2), h0, h1);
-    bl[j] = cvt_e2m1x2(l1, l0);
-    bh[j] = cvt_e2m1x2(h1, h0);
+    for (int j = 0; j < 8; ++j) bl[j] = 0u;
+  } else {
+    const float r = __frcp_rn(eff);
+    if (eff >= 0x1p-100f && __fmul_rn(bmax, r) < 0x1p100f) {
+      const float rlo = __fmul_rn(r, 0.99999904632568359375f);  // 1 - 2^-20
+      const float rhi = __fmul_rn(r, 1.00000095367431640625f);  // 1 + 2^-20
+      const f2 rl2 = pk(rlo, rlo), rh2 = pk(rhi, rhi);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float l0, l1, h0, h1;
+        upk(mul2(x2[j], rl2), l0, l1);
+        upk(mul2(x2[j], rh2), h0, h1);
+        uint32_t cl = cvt_e2m1x2(l1, l0);
+        if (__builtin_expect(cl != cvt_e2m1x2(h1, h0), 0)) {
+          float x0, x1;
+          upk(x2[j], x0, x1);
+          cl = exact_pair(x0, x1, eff);
+        }
+        bl[j] = cl;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float x0, x1;
+        upk(x2[j], x0, x1);
+        bl[j] = exact_pair(x0, x1, eff);
+      }
+    }
   }
   codes[0] = pack4(bl[0], bl[1], bl[2], bl[3]);
   codes[1] = pack4(bl[4], bl[5], bl[6], bl[7]);
-  const uint32_t hi0 = pack4(bh[0], bh[1], bh[2], bh[3]);
-  const uint32_t hi1 = pack4(bh[4], bh[5], bh[6], bh[7]);
-  if ((codes[0] ^ hi0) | (codes[1] ^ hi1)) return cand_exact(x, eff, codes);
-  // errors with scalar round-to-nearest intrinsics: these are never fused into
-  // multiply-adds, so every step rounds once as written
-  float e[16];
+  const f2 neff2 = pk(-eff, -eff);
+  f2 d[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    float v0, v1;
-    upk(e2m1x2_to_f2(bl[j]), v0, v1);
-    const float d0 = __fsub_rn(x[2 * j], __fmul_rn(v0, eff));
-    const float d1 = __fsub_rn(x[2 * j + 1], __fmul_rn(v1, eff));
-    e[2 * j] = __fmul_rn(d0, d0);
-    e[2 * j + 1] = __fmul_rn(d1, d1);
-  }
-  float a[8], b[4];
+  for (int j = 0; j < 8; ++j) d[j] = fma2(e2m1x2_to_f2(bl[j]), neff2, x2[j]);
+  f2 a[4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) a[j] = __fadd_rn(e[j], e[j + 8]);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) b[j] = __fadd_rn(a[j], a[j + 4]);
-  return __fadd_rn(__fadd_rn(b[0], b[2]), __fadd_rn(b[1], b[3]));
+  for (int j = 0; j < 4; ++j) a[j] = fma2(d[j], d[j], mul2(d[4 + j], d[4 + j]));  // (a_2j, a_2j+1)
+  const f2 b0 = add2(a[0], a[2]), b1 = add2(a[1], a[3]);                           // (b_0,b_1), (b_2,b_3)
+  float c0, c1;
+  upk(add2(b0, b1), c0, c1);
+  return __fadd_rn(c0, c1);
 }
 
 template <bool kFos>
@@ -226,15 +220,12 @@ quant_kernel(const uint4* __restrict__ x, int64_t rows, int64_t K, const uint32_
     const uint4 v0 = ld_stream_u4(x + 2 * blk);
     const uint4 v1 = ld_stream_u4(x + 2 * blk + 1);
     const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    float xv[16];  // magnitudes
-    f2 x2[8];
+    f2 x2[8];  // magnitudes, elements (2j, 2j+1)
     uint32_t m2 = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const uint32_t a = w[j] & 0x7FFF7FFFu;
-      xv[2 * j] = __uint_as_float(a << 16);
-      xv[2 * j + 1] = __uint_as_float(a & 0xFFFF0000u);
-      x2[j] = pk(xv[2 * j], xv[2 * j + 1]);
+      x2[j] = pk(__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u));
       m2 = __vmaxu2(m2, a);
     }
     // sign bits of the 16 codes: byte j of sgn[h] gets the signs of elements
@@ -254,14 +245,14 @@ quant_kernel(const uint4* __restrict__ x, int64_t rows, int64_t K, const uint32_
     const uint32_t s6 = cvt_e4m3x2(0.0f, r6) & 0xFFu;
     const float s6v = e4m3_to_f32(s6);
     uint32_t cw[2];
-    const float sse6 = cand(xv, x2, bmax, __fmul_rn(s6v, ts), cw);
+    const float sse6 = cand(x2, bmax, __fmul_rn(s6v, ts), cw);
     uint32_t s = s6;
     if (kFos) {
       const uint32_t s4 = cvt_e4m3x2(0.0f, __fmul_rn(s6v, 1.5f)) & 0xFFu;
       bool m4 = false;
       if (s4 != s6) {  // equal scales tie, and a tie keeps M=6
         uint32_t cw4[2];
-        const float sse4 = cand(xv, x2, bmax, __fmul_rn(e4m3_to_f32(s4), ts), cw4);
+        const float sse4 = cand(x2, bmax, __fmul_rn(e4m3_to_f32(s4), ts), cw4);
         m4 = sse4 < sse6;
         if (m4) {
           cw[0] = cw4[0];
