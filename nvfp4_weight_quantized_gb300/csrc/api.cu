@@ -20,9 +20,13 @@ namespace {
 thread_local std::string t_last_error;
 
 std::mutex g_mu;
-std::map<std::pair<int64_t, int64_t>, int64_t> g_crossover;
-// Largest M that takes the W4A16 path when no per-shape entry exists.
-int64_t g_default_crossover = 48;
+// Largest M that still takes the W4A16 path, per weight shape (N, K), and for
+// shapes without an entry.  Built-in values: the crossover of graph-timed
+// W4A16 vs activation quantisation + W4A4 measured on GB300 with
+// nvfp4_weight_quantized_gb300.tune (sweep M = 1..256); re-run it to retune.
+std::map<std::pair<int64_t, int64_t>, int64_t> g_crossover = {
+    {{4096, 4096}, 64}, {{11008, 4096}, 16}, {{22016, 4096}, 8}, {{4096, 11008}, 16}};
+int64_t g_default_crossover = 16;
 
 struct DeviceInfo {
   bool ready = false;

@@ -7,18 +7,21 @@
 // two per byte, one UE4M3 scale per 16 elements along K, fp32 accumulation in
 // tensor memory (TMEM).
 //
-// One CTA computes a 128 x 256 output tile (A rows = tokens, B rows = weight
-// rows) with 4 warps:
-//   warp 0, one lane  -- producer: per 256-wide K stage, TMA loads of the A and
+// Persistent kernel, one CTA per SM, looping over 128 x BN output tiles
+// (A rows = tokens, B rows = weight rows), 10 warps:
+//   warp 8, one lane  -- producer: per 256-wide K stage, TMA loads of the A and
 //                        B code tiles (128-byte swizzle) and bulk copies of the
 //                        matching scale tiles (already in the MMA tiling);
-//   warp 1, one lane  -- MMA issuer: tcgen05.cp of the scales into TMEM, four
-//                        K=64 MMAs per stage, tcgen05.commit to free the stage;
-//   all 4 warps       -- epilogue: tcgen05.ld of the accumulator, times
-//                        ts_a * ts_w, convert, store.
-// A 4-stage shared-memory ring keeps TMA, the MMAs and the next loads in
-// flight together.  Every mbarrier wait is bounded; a wait that runs out sets
-// the library's status word (NVFP4_ERR_TIMEOUT) and the CTA winds down.
+//   warps 4-7         -- scale loaders: copy the stage's scale tiles from shared
+//                        memory into TMEM with tcgen05.st (lane = tile row);
+//   warp 9, one lane  -- MMA issuer: four K=64 MMAs per stage and nothing
+//                        else (an MMA stream is bound by its issuer's latency);
+//   warps 0-3         -- epilogue: tcgen05.ld of the accumulator, scale by
+//                        ts_a * ts_w, convert, store, release the accumulator.
+// BN = 256 for large M; BN = 64 when M fits one tile so that a skinny GEMM
+// still spreads over every SM.  Every mbarrier wait is bounded; a wait that
+// runs out sets the library's status word (NVFP4_ERR_TIMEOUT) and the CTA
+// winds down.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -34,50 +37,75 @@ namespace {
 
 using namespace sm100;
 
-constexpr int BM = 128;             // tokens per tile (MMA M)
-constexpr int BN = 256;             // weight rows per tile (MMA N)
+constexpr int BM = 128;             // tokens per tile (MMA M = TMEM lanes)
 constexpr int BK = 256;             // FP4 elements per stage (128 bytes per row)
 constexpr int kStages = 4;
-constexpr int kThreads = 128;
-constexpr int kABytes = BM * BK / 2;                          // 16 KB
-constexpr int kBBytes = BN * BK / 2;                          // 32 KB
-constexpr int kSfaBytes = (BM / 128) * (BK / 64) * kScaleTileBytes;  // 2 KB
-constexpr int kSfbBytes = (BN / 128) * (BK / 64) * kScaleTileBytes;  // 4 KB
+constexpr int kEpiWarps = 4, kSfWarps = 4;
+constexpr int kProducerWarp = kEpiWarps + kSfWarps, kMmaWarp = kProducerWarp + 1;
+constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCol = 0;                       // 256 fp32 columns
-constexpr uint32_t kSfaCol = 256;                     // 16 columns per stage
-constexpr uint32_t kSfbCol = kSfaCol + 16 * kStages;  // 32 columns per stage
-static_assert(kSfbCol + 32 * kStages <= kTmemCols, "TMEM budget");
+constexpr int kABytes = BM * BK / 2;                      // 16 KB
+constexpr int kSfaBytes = (BK / 64) * kScaleTileBytes;    // 2 KB: 4 atoms (one per K=64 MMA)
 
+template <int BN>
+struct Cfg {
+  static constexpr int kBBytes = BN * BK / 2;
+  static constexpr int kSfbTiles = (BN + 127) / 128;                        // 128-row scale tiles
+  static constexpr int kSfbBytes = kSfbTiles * (BK / 64) * kScaleTileBytes;
+  static constexpr uint32_t kAccCol = 0;                                    // BN fp32 columns
+  static constexpr uint32_t kSfaCols = 16;                                  // 4 MMAs x 4 columns
+  static constexpr uint32_t kSfbCols = 16 * kSfbTiles;                      // 4 MMAs x 4 columns per tile
+  static constexpr uint32_t kSfCol = BN;                                    // per-stage scale columns
+  static constexpr uint32_t kSfStageCols = kSfaCols + kSfbCols;
+  static_assert(kSfCol + kStages * kSfStageCols <= kTmemCols, "TMEM budget");
+  // instruction descriptor, kind::mxf4nvf4: A and B E2M1 (format code 1 in
+  // bits 7-9 and 10-12), both K-major, N >> 3 in bits 17-22, scale type
+  // UE4M3 (bit 23 = 0), M >> 7 in bits 27-28, scale-factor ids 0, dense
+  static constexpr uint32_t kIdesc =
+      (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 7) << 27);
+};
+
+template <int BN>
 struct __align__(1024) Smem {
   uint8_t a[kStages][kABytes];
-  uint8_t b[kStages][kBBytes];
+  uint8_t b[kStages][Cfg<BN>::kBBytes];
   uint8_t sfa[kStages][kSfaBytes];
-  uint8_t sfb[kStages][kSfbBytes];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t acc;
+  uint8_t sfb[kStages][Cfg<BN>::kSfbBytes];
+  uint64_t full[kStages];     // TMA landed
+  uint64_t sf_full[kStages];  // scales in TMEM (4 loader warps)
+  uint64_t empty[kStages];    // MMAs of the stage done
+  uint64_t acc_full;          // tile accumulated
+  uint64_t acc_free;          // epilogue drained the accumulator (4 warps)
   uint32_t tmem_base;
 };
 
-// Instruction descriptor for kind::mxf4nvf4: A and B E2M1 (format code 1 in
-// bits 7-9 and 10-12), both K-major, N >> 3 in bits 17-22, scale type UE4M3
-// (bit 23 = 0), M >> 7 in bits 27-28, scale-factor ids 0, dense.
-constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 7) << 27);
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 template <bool kF32>
 __device__ __forceinline__ void store_row32(void* y, int64_t row_off, int64_t n, int64_t N, const uint32_t (&v)[32],
                                             float alpha, bool vec_ok) {
-  float f[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]) * alpha;
   if (kF32) {
     float* out = static_cast<float*>(y) + row_off + n;
     if (vec_ok && n + 32 <= N) {
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(out + i) = make_float4(f[i], f[i + 1], f[i + 2], f[i + 3]);
+      for (int i = 0; i < 32; i += 4)
+        *reinterpret_cast<float4*>(out + i) =
+            make_float4(__uint_as_float(v[i]) * alpha, __uint_as_float(v[i + 1]) * alpha,
+                        __uint_as_float(v[i + 2]) * alpha, __uint_as_float(v[i + 3]) * alpha);
     } else {
-      for (int i = 0; i < 32 && n + i < N; ++i) out[i] = f[i];
+      for (int i = 0; i < 32 && n + i < N; ++i) out[i] = __uint_as_float(v[i]) * alpha;
     }
   } else {
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(y) + row_off + n;
@@ -85,10 +113,13 @@ __device__ __forceinline__ void store_row32(void* y, int64_t row_off, int64_t n,
 #pragma unroll
       for (int i = 0; i < 32; i += 8) {
         uint4 p;
-        __nv_bfloat162 h0 = __floats2bfloat162_rn(f[i], f[i + 1]);
-        __nv_bfloat162 h1 = __floats2bfloat162_rn(f[i + 2], f[i + 3]);
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(f[i + 4], f[i + 5]);
-        __nv_bfloat162 h3 = __floats2bfloat162_rn(f[i + 6], f[i + 7]);
+        __nv_bfloat162 h0 = __floats2bfloat162_rn(__uint_as_float(v[i]) * alpha, __uint_as_float(v[i + 1]) * alpha);
+        __nv_bfloat162 h1 =
+            __floats2bfloat162_rn(__uint_as_float(v[i + 2]) * alpha, __uint_as_float(v[i + 3]) * alpha);
+        __nv_bfloat162 h2 =
+            __floats2bfloat162_rn(__uint_as_float(v[i + 4]) * alpha, __uint_as_float(v[i + 5]) * alpha);
+        __nv_bfloat162 h3 =
+            __floats2bfloat162_rn(__uint_as_float(v[i + 6]) * alpha, __uint_as_float(v[i + 7]) * alpha);
         p.x = *reinterpret_cast<uint32_t*>(&h0);
         p.y = *reinterpret_cast<uint32_t*>(&h1);
         p.z = *reinterpret_cast<uint32_t*>(&h2);
@@ -96,122 +127,215 @@ __device__ __forceinline__ void store_row32(void* y, int64_t row_off, int64_t n,
         *reinterpret_cast<uint4*>(out + i) = p;
       }
     } else {
-      for (int i = 0; i < 32 && n + i < N; ++i) out[i] = __float2bfloat16_rn(f[i]);
+      for (int i = 0; i < 32 && n + i < N; ++i) out[i] = __float2bfloat16_rn(__uint_as_float(v[i]) * alpha);
     }
   }
 }
 
-template <bool kF32>
+template <int BN, bool kF32>
 __global__ void __launch_bounds__(kThreads, 1)
 w4a4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
             const uint8_t* __restrict__ a_smma, const uint8_t* __restrict__ b_smma,
             const float* __restrict__ a_ts, const float* __restrict__ b_ts, int64_t M, int64_t N, int64_t K,
             void* __restrict__ y, unsigned int* __restrict__ status) {
+  using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem<BN>& sm = *reinterpret_cast<Smem<BN>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t m_tile = blockIdx.y, n_tile = blockIdx.x;
-  const int64_t m0 = m_tile * BM, n0 = n_tile * BN;
   const int kb64 = (int)(K / 64);                 // 64-wide K blocks = scale column tiles per row tile
-  const int kt = (kb64 + 3) / 4;                  // K stages
+  const int kt = (kb64 + 3) / 4;                  // K stages per tile
   const int64_t b_row_tiles = (N + 127) / 128;    // row tiles present in the weight scale tiling
-  const int64_t sfb_left = b_row_tiles - n0 / 128;
-  const int nsfb = sfb_left < 2 ? (int)sfb_left : 2;
+  const int64_t m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN - 1) / BN;
+  const int64_t n_work = m_tiles * n_tiles;
 
-  if (threadIdx.x == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.sf_full[s], kSfWarps);
       mbar_init(&sm.empty[s], 1);
     }
-    mbar_init(&sm.acc, 1);
+    mbar_init(&sm.acc_full, 1);
+    mbar_init(&sm.acc_free, kEpiWarps);
     fence_mbar_init();
     prefetch_tmap(&tmap_a);
     prefetch_tmap(&tmap_b);
   }
-  if (warp == 1) tmem_alloc(&sm.tmem_base, kTmemCols);
+  if (warp == 0) tmem_alloc(&sm.tmem_base, kTmemCols);
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
   bool failed = false;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- producer ----------------
-    griddep_wait();  // inputs may be written by the previous kernel in the stream
-    for (int ks = 0; ks < kt; ++ks) {
-      const int s = ks % kStages;
-      const uint32_t round = (uint32_t)(ks / kStages);
-      if (ks >= kStages && !mbar_wait(&sm.empty[s], (round - 1) & 1u)) {
-        failed = true;
-        break;
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      // ---------------- producer ----------------
+      griddep_wait();  // inputs may be written by the previous kernel in the stream
+      int g = 0;       // stage counter across this CTA's tiles
+      for (int64_t w = blockIdx.x; w < n_work && !failed; w += gridDim.x) {
+        const int64_t m_tile = w / n_tiles, n_tile = w - m_tile * n_tiles;
+        const int64_t n0 = n_tile * BN;
+        const int64_t sfb_left = b_row_tiles - n0 / 128;
+        const int nsfb = sfb_left < C::kSfbTiles ? (int)sfb_left : C::kSfbTiles;
+        for (int ks = 0; ks < kt; ++ks, ++g) {
+          const int s = g % kStages;
+          if (g >= kStages && !mbar_wait(&sm.empty[s], (uint32_t)(g / kStages - 1) & 1u)) {
+            failed = true;
+            break;
+          }
+          const int kk_n = min(4, kb64 - 4 * ks);
+          const uint32_t sf_bytes = (uint32_t)kk_n * kScaleTileBytes;
+          mbar_arrive_expect_tx(&sm.full[s], kABytes + C::kBBytes + sf_bytes * (1 + nsfb));
+          tma_load_2d(sm.a[s], &tmap_a, ks * (BK / 2), (int)(m_tile * BM), &sm.full[s]);
+          tma_load_2d(sm.b[s], &tmap_b, ks * (BK / 2), (int)n0, &sm.full[s]);
+          bulk_load(sm.sfa[s], a_smma + (m_tile * kb64 + 4 * ks) * kScaleTileBytes, sf_bytes, &sm.full[s]);
+          for (int rt = 0; rt < nsfb; ++rt)
+            bulk_load(sm.sfb[s] + rt * (BK / 64) * kScaleTileBytes,
+                      b_smma + ((n0 / 128 + rt) * kb64 + 4 * ks) * kScaleTileBytes, sf_bytes, &sm.full[s]);
+        }
       }
-      const int kk_n = min(4, kb64 - 4 * ks);
-      const uint32_t sf_bytes = (uint32_t)kk_n * kScaleTileBytes;
-      mbar_arrive_expect_tx(&sm.full[s], kABytes + kBBytes + sf_bytes * (1 + nsfb));
-      tma_load_2d(sm.a[s], &tmap_a, ks * (BK / 2), (int)m0, &sm.full[s]);
-      tma_load_2d(sm.b[s], &tmap_b, ks * (BK / 2), (int)n0, &sm.full[s]);
-      bulk_load(sm.sfa[s], a_smma + (m_tile * kb64 + 4 * ks) * kScaleTileBytes, sf_bytes, &sm.full[s]);
-      for (int rt = 0; rt < nsfb; ++rt)
-        bulk_load(sm.sfb[s] + rt * (kSfbBytes / 2), b_smma + ((n0 / 128 + rt) * kb64 + 4 * ks) * kScaleTileBytes,
-                  sf_bytes, &sm.full[s]);
+      // let every load this thread issued land before the CTA can exit
+      for (int i = max(0, g - kStages); i < g && !failed; ++i)
+        if (!mbar_wait(&sm.full[i % kStages], (uint32_t)(i / kStages) & 1u)) failed = true;
     }
-    // let every load this thread issued land before the CTA can exit
-    for (int ks = max(0, kt - kStages); ks < kt && !failed; ++ks)
-      if (!mbar_wait(&sm.full[ks % kStages], (uint32_t)(ks / kStages) & 1u)) failed = true;
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer ----------------
-    for (int ks = 0; ks < kt; ++ks) {
-      const int s = ks % kStages;
-      if (!mbar_wait(&sm.full[s], (uint32_t)(ks / kStages) & 1u)) {
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      int g = 0, t = 0;
+      for (int64_t w = blockIdx.x; w < n_work && !failed; w += gridDim.x, ++t) {
+        const int64_t n0 = (w % n_tiles) * BN;
+        // rows of a 64-wide tile that starts in the upper half of a 128-row
+        // scale tile sit in TMEM columns 2-3 of each 4-column group
+        const uint32_t sfb_sub = (BN == 64 && (n0 & 127) == 64) ? 2u : 0u;
+        if (t > 0 && !mbar_wait(&sm.acc_free, (uint32_t)(t - 1) & 1u)) {
+          failed = true;
+          break;
+        }
+        fence_after_sync();
+        for (int ks = 0; ks < kt; ++ks, ++g) {
+          const int s = g % kStages;
+          if (!mbar_wait(&sm.sf_full[s], (uint32_t)(g / kStages) & 1u)) {
+            failed = true;
+            break;
+          }
+          fence_after_sync();
+          const int kk_n = min(4, kb64 - 4 * ks);
+          const uint32_t sfa_t = tmem + C::kSfCol + C::kSfStageCols * s;
+          const uint32_t sfb_t = sfa_t + C::kSfaCols + sfb_sub;
+          const uint64_t adesc = smem_desc(smem_addr(sm.a[s]), 0, 1024, 2);
+          const uint64_t bdesc = smem_desc(smem_addr(sm.b[s]), 0, 1024, 2);
+          for (int kk = 0; kk < kk_n; ++kk)
+            // advancing the start address by 32 bytes selects the next 64 FP4
+            // elements inside the 128-byte swizzle atom
+            mma_mxf4nvf4(tmem + C::kAccCol, adesc + 2ull * kk, bdesc + 2ull * kk, C::kIdesc, sfa_t + 4 * kk,
+                         sfb_t + 4 * C::kSfbTiles * kk, (ks | kk) != 0);
+          commit(&sm.empty[s]);
+        }
+        if (!failed) commit(&sm.acc_full);
+      }
+      griddep_launch_dependents();
+    }
+  } else if (warp >= kEpiWarps) {
+    // ---------------- scale loaders: shared memory -> TMEM ----------------
+    // Each 512-byte scale atom holds 32 chunks of 16 bytes; chunk i goes to
+    // lane i of every 32-lane quarter (the layout the MMA reads: row r of the
+    // tile at lane r % 32 of any quarter, column r / 32), 4 columns per atom.
+    // Atom order in TMEM: A: 4 * kk; B: 16 + 4 * (kSfbTiles * kk + rt).
+    const uint32_t lane_base = (uint32_t)((warp - kEpiWarps) * 32) << 16;
+    int g = 0;
+    for (int64_t w = blockIdx.x; w < n_work && !failed; w += gridDim.x) {
+      for (int ks = 0; ks < kt; ++ks, ++g) {
+        const int s = g % kStages;
+        if (!mbar_wait(&sm.full[s], (uint32_t)(g / kStages) & 1u)) {
+          failed = true;
+          break;
+        }
+        // the TMEM scale slot of stage s is free once the MMAs of its previous
+        // round completed (that is what empty[s] signals)
+        if (g >= kStages && !mbar_wait(&sm.empty[s], (uint32_t)(g / kStages - 1) & 1u)) {
+          failed = true;
+          break;
+        }
+        const uint32_t col = tmem + lane_base + C::kSfCol + C::kSfStageCols * s;
+        uint32_t r[16];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint4 v = *reinterpret_cast<const uint4*>(sm.sfa[s] + kk * kScaleTileBytes + lane * 16);
+          r[4 * kk] = v.x;
+          r[4 * kk + 1] = v.y;
+          r[4 * kk + 2] = v.z;
+          r[4 * kk + 3] = v.w;
+        }
+        tmem_st_x16(col, r);
+#pragma unroll
+        for (int h = 0; h < C::kSfbTiles * 4; h += 4) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int idx = h + q;  // = kSfbTiles * kk + rt
+            const int kk = idx / C::kSfbTiles, rt = idx % C::kSfbTiles;
+            const uint4 v = *reinterpret_cast<const uint4*>(sm.sfb[s] + rt * (BK / 64) * kScaleTileBytes +
+                                                            kk * kScaleTileBytes + lane * 16);
+            r[4 * q] = v.x;
+            r[4 * q + 1] = v.y;
+            r[4 * q + 2] = v.z;
+            r[4 * q + 3] = v.w;
+          }
+          tmem_st_x16(col + C::kSfaCols + 4 * h, r);
+        }
+        tmem_wait_st();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.sf_full[s]);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 0-3; TMEM lanes 32w..32w+31 = tile rows) ----------------
+    const float alpha = __fmul_rn(*a_ts, *b_ts);
+    const bool vec_ok = kF32 ? (N % 4 == 0) : (N % 8 == 0);
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    int t = 0;
+    for (int64_t w = blockIdx.x; w < n_work; w += gridDim.x, ++t) {
+      const int64_t m_tile = w / n_tiles, n_tile = w - m_tile * n_tiles;
+      const int64_t row = m_tile * BM + warp * 32 + lane, n0 = n_tile * BN;
+      // warp-uniform, since tcgen05.ld is a warp-collective instruction
+      const bool ok = __all_sync(0xffffffffu, !failed && mbar_wait(&sm.acc_full, (uint32_t)t & 1u));
+      if (!ok) {
         failed = true;
         break;
       }
       fence_after_sync();
-      const int kk_n = min(4, kb64 - 4 * ks);
-      const uint32_t sfa_t = tmem + kSfaCol + 16u * s, sfb_t = tmem + kSfbCol + 32u * s;
-      const uint32_t sfa_s = smem_addr(sm.sfa[s]), sfb_s = smem_addr(sm.sfb[s]);
-      for (int kk = 0; kk < kk_n; ++kk) {
-        cp_32x128b_warpx4(sfa_t + 4 * kk, smem_desc(sfa_s + kk * kScaleTileBytes, 0, 128, 0));
-        for (int rt = 0; rt < nsfb; ++rt)
-          cp_32x128b_warpx4(sfb_t + 8 * kk + 4 * rt,
-                            smem_desc(sfb_s + rt * (kSfbBytes / 2) + kk * kScaleTileBytes, 0, 128, 0));
-      }
-      const uint64_t adesc = smem_desc(smem_addr(sm.a[s]), 0, 1024, 2);
-      const uint64_t bdesc = smem_desc(smem_addr(sm.b[s]), 0, 1024, 2);
-      for (int kk = 0; kk < kk_n; ++kk) {
-        // advancing the start address by 32 bytes selects the next 64 FP4
-        // elements inside the 128-byte swizzle atom
-        mma_mxf4nvf4(tmem + kAccCol, adesc + 2ull * kk, bdesc + 2ull * kk, kIdesc, sfa_t + 4 * kk, sfb_t + 8 * kk,
-                     (ks | kk) != 0);
-      }
-      commit(&sm.empty[s]);
-    }
-    if (!failed) commit(&sm.acc);
-    griddep_launch_dependents();
-  }
-  __syncwarp();
-
-  // ---------------- epilogue ----------------
-  // warp-uniform, since tcgen05.ld is a warp-collective instruction
-  const bool acc_ok = __all_sync(0xffffffffu, !failed && mbar_wait(&sm.acc, 0));
-  fence_after_sync();
-  if (acc_ok) {
-    const float alpha = __fmul_rn(*a_ts, *b_ts);
-    const int64_t row = m0 + warp * 32 + lane;
-    const bool vec_ok = kF32 ? (N % 4 == 0) : (N % 8 == 0);
+      if (BN <= 64) {
+        // small tile: drain it all, hand the accumulator back, then store
+        uint32_t v[BN / 32][32];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) tmem_ld_32x32b_x32(tmem + lane_base + C::kAccCol + 32 * c, v[c]);
+        tmem_wait_ld();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.acc_free);
+        if (row < M) {
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c)
+            if (n0 + 32 * c < N) store_row32<kF32>(y, row * N, n0 + 32 * c, N, v[c], alpha, vec_ok);
+        }
+      } else {
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      uint32_t v[32];
-      tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + kAccCol + c, v);
-      tmem_wait_ld();
-      if (row < M && n0 + c < N) store_row32<kF32>(y, row * N, n0 + c, N, v, alpha, vec_ok);
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + lane_base + C::kAccCol + 32 * c, v);
+          tmem_wait_ld();
+          if (row < M && n0 + 32 * c < N) store_row32<kF32>(y, row * N, n0 + 32 * c, N, v, alpha, vec_ok);
+        }
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.acc_free);
+      }
     }
-  } else if (lane == 0) {
-    atomicOr(status, kStatusTimeout);
+    if (failed && lane == 0) atomicOr(status, kStatusTimeout);
   }
   fence_before_sync();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 0) {
     fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -249,35 +373,48 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_by
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int BN>
+cudaError_t launch_bn(const uint8_t* a_codes, const uint8_t* a_smma, const float* a_ts, int64_t M,
+                      const uint8_t* w_codes, const uint8_t* w_smma, const float* w_ts, int64_t N, int64_t K,
+                      void* y, bool out_f32, unsigned int* status, int num_sms, cudaStream_t stream) {
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, a_codes, (uint64_t)M, (uint64_t)K / 2, BM) ||
+      !make_map(&mb, w_codes, (uint64_t)N, (uint64_t)K / 2, BN))
+    return cudaErrorInvalidValue;
+  // one CTA per SM: each allocates all 512 TMEM columns, which the block
+  // scheduler does not count, so ask for enough shared memory that a second
+  // CTA never lands on the same SM (228 KB per SM)
+  const size_t smem = std::max<size_t>(sizeof(Smem<BN>) + 1024, 120u * 1024u);
+  auto kern = out_f32 ? w4a4_kernel<BN, true> : w4a4_kernel<BN, false>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  const int64_t work = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::min<int64_t>(work, num_sms));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, ma, mb, a_smma, w_smma, a_ts, w_ts, M, N, K, y, status);
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma, const float* a_ts, int64_t M,
                              const uint8_t* w_codes, const uint8_t* w_scales_mma, const float* w_ts, int64_t N,
                              int64_t K, void* y, bool out_f32, unsigned int* status, int num_sms,
                              cudaStream_t stream) {
-  (void)num_sms;
   if (M <= 0) return cudaSuccess;
-  if (K < BK || K % 64 != 0 || (M + BM - 1) / BM > 65535 || M > INT32_MAX || N > INT32_MAX)
-    return cudaErrorNotSupported;
-  CUtensorMap ma, mb;
-  if (!make_map(&ma, a_codes, (uint64_t)M, (uint64_t)K / 2, BM) ||
-      !make_map(&mb, w_codes, (uint64_t)N, (uint64_t)K / 2, BN))
-    return cudaErrorInvalidValue;
-  const size_t smem = sizeof(Smem) + 1024;
-  auto kern = out_f32 ? w4a4_kernel<true> : w4a4_kernel<false>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, ma, mb, a_scales_mma, w_scales_mma, a_ts, w_ts, M, N, K, y, status);
+  if (K < BK || K % 64 != 0 || M > INT32_MAX || N > INT32_MAX) return cudaErrorNotSupported;
+  if (M <= BM)
+    return launch_bn<64>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, out_f32, status,
+                         num_sms, stream);
+  return launch_bn<256>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, out_f32, status,
+                        num_sms, stream);
 }
 
 }  // namespace nvfp4
