@@ -177,6 +177,10 @@ def run_ours(args):
     Ys = {M: torch.empty((M, N), dtype=torch.bfloat16, device=dev) for M in DECODE_M}
     lws = {M: torch.empty(max(nv.nvfp4_workspace_bytes(nv.OP_LINEAR, M, N, K), 256), dtype=torch.uint8,
                           device=dev) for M in DECODE_M}
+    # weights are quantised once per slot and only read by the GEMMs of a
+    # step (the quantiser of a step writes a slot no GEMM of that step reads),
+    # so the GEMMs may start streaming them before the previous kernel ends
+    nv.nvfp4_set_weight_prefetch(True)
     cross = nv.nvfp4_get_crossover(N, K)
     paths = {M: ("w4a16" if M <= cross else "w4a4") for M in DECODE_M}
     launches_per_step = 2 + sum(1 if paths[M] == "w4a16" else 3 for M in DECODE_M)
@@ -474,6 +478,29 @@ def run_reference(args):
     }))
 
 
+def profile_case(which: str, m_decode: int):
+    """One launch of each hot kernel on a small case, for a profiler capture:
+    the FourOverSix quantiser and W4A16 at M = m_decode on the decode weight
+    [4096, 4096], activation quantisation + W4A4 at M = 2048 on the prefill
+    weight [11008, 4096].  Prints the device status; times nothing."""
+    import torch
+    import nvfp4_weight_quantized_gb300 as nv
+    from nvfp4_weight_quantized_gb300 import build
+    build.build()
+    dev = torch.device("cuda")
+    bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
+    if which in ("all", "quant", "w4a16"):
+        q = nv.nvfp4_quantize_fos(bf(synth.decode_weight()), logical_scales=False, choice=False)
+        if which in ("all", "w4a16"):
+            nv.nvfp4_gemm_w4a16(bf(synth.decode_act(m_decode)), q)
+    if which in ("all", "w4a4"):
+        qp = nv.nvfp4_quantize_fos(bf(synth.prefill_weight()), logical_scales=False, choice=False)
+        a = nv.nvfp4_quantize_act(bf(synth.prefill_act(2048)))
+        nv.nvfp4_gemm_w4a4(a, qp)
+    torch.cuda.synchronize()
+    print("profile case", which, "status", nv.nvfp4_status_string(nv.nvfp4_get_device_status()))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -484,8 +511,13 @@ def main():
     ap.add_argument("--cpu-rows-reference", type=int, default=64)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", choices=["all", "quant", "w4a16", "w4a4"],
+                    help="launch each hot kernel once on a small case (for ncu) and exit")
+    ap.add_argument("--profile-m", type=int, default=16, help="decode M of --profile-case")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.profile_case:
+        profile_case(args.profile_case, args.profile_m)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

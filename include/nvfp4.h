@@ -150,6 +150,10 @@ nvfp4_status nvfp4_quantize_act(const void* X, int64_t M, int64_t K, float divis
  *   X      in:  device bf16 [M, K];  M >= 0 (M == 0 launches nothing)
  *   W      in:  quantised weight; K % 64 == 0
  *   Y      out: device [M, N] of out_dtype
+ * Two kernels implement it: for M <= nvfp4_get_w4a16_rf_max_m() the weights
+ * are dequantised in registers and multiplied with warp-level MMAs (decode
+ * sizes), above that they are dequantised into tensor memory for tcgen05
+ * MMAs.  Both give the same result up to fp32 summation order.
  */
 nvfp4_status nvfp4_gemm_w4a16(const void* X, int64_t M, const nvfp4_weight* W, void* Y,
                               int out_dtype, void* workspace, size_t workspace_bytes,
@@ -217,6 +221,22 @@ nvfp4_status nvfp4_linear_noalloc(const void* X, int64_t M, const nvfp4_weight* 
  * GB300 (see nvfp4_get_crossover(0, 0)). */
 nvfp4_status nvfp4_set_crossover(int64_t N, int64_t K, int64_t M_threshold);
 int64_t nvfp4_get_crossover(int64_t N, int64_t K);
+
+/* Largest M for which nvfp4_gemm_w4a16 uses its register-file kernel
+ * (0 ..= 64; default 64).  A tuning knob: both kernels compute the same
+ * product.  Thread-safe; returns NVFP4_ERR_INVALID_ARG outside the range. */
+nvfp4_status nvfp4_set_w4a16_rf_max_m(int64_t M);
+int64_t nvfp4_get_w4a16_rf_max_m(void);
+
+/* Weight prefetch (default off).  When on, the W4A16 kernels start reading
+ * the weight codes and scales before the previous kernel in the stream has
+ * finished (programmatic dependent launch), hiding the HBM latency behind it;
+ * the activations are still read, and the output written, only after it.
+ * Turn it on only when no work queued on the stream before a GEMM call can
+ * still be writing that call's weight buffers -- true when weights are
+ * quantised once and then only read, as in inference.  Thread-safe. */
+nvfp4_status nvfp4_set_weight_prefetch(int enable);
+int nvfp4_get_weight_prefetch(void);
 
 /* Synchronises `stream`, then returns and clears the device status word of the
  * current device: NVFP4_OK, NVFP4_ERR_NONFINITE or NVFP4_ERR_TIMEOUT. */

@@ -23,7 +23,9 @@ __all__ = [
     "NVFP4Error", "NVFP4Weight", "NVFP4Act", "lib", "library_path", "declared_functions",
     "nvfp4_scales_mma_bytes", "nvfp4_workspace_bytes", "nvfp4_quantize_fos", "nvfp4_quantize_act",
     "nvfp4_gemm_w4a16", "nvfp4_gemm_w4a4", "nvfp4_linear", "nvfp4_linear_noalloc", "nvfp4_set_crossover",
-    "nvfp4_get_crossover", "nvfp4_get_device_status", "nvfp4_status_string",
+    "nvfp4_get_crossover", "nvfp4_set_w4a16_rf_max_m", "nvfp4_get_w4a16_rf_max_m", "nvfp4_set_weight_prefetch",
+    "nvfp4_get_weight_prefetch", "nvfp4_get_device_status",
+    "nvfp4_status_string",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -74,6 +76,10 @@ def lib() -> ctypes.CDLL:
             "nvfp4_linear_noalloc": (st, [vp, i64, wp, vp, ctypes.c_int, vp]),
             "nvfp4_set_crossover": (st, [i64, i64, i64]),
             "nvfp4_get_crossover": (i64, [i64, i64]),
+            "nvfp4_set_w4a16_rf_max_m": (st, [i64]),
+            "nvfp4_get_w4a16_rf_max_m": (i64, []),
+            "nvfp4_set_weight_prefetch": (st, [ctypes.c_int]),
+            "nvfp4_get_weight_prefetch": (ctypes.c_int, []),
             "nvfp4_get_device_status": (st, [vp]),
             "nvfp4_status_string": (ctypes.c_char_p, [st]),
             "nvfp4_last_error": (ctypes.c_char_p, []),
@@ -132,6 +138,24 @@ def nvfp4_set_crossover(N: int, K: int, m_threshold: int) -> None:
 
 def nvfp4_get_crossover(N: int = 0, K: int = 0) -> int:
     return lib().nvfp4_get_crossover(N, K)
+
+
+def nvfp4_set_w4a16_rf_max_m(m: int) -> None:
+    """Largest M that nvfp4_gemm_w4a16 sends to its register-file kernel."""
+    _check(lib().nvfp4_set_w4a16_rf_max_m(m), "nvfp4_set_w4a16_rf_max_m")
+
+
+def nvfp4_get_w4a16_rf_max_m() -> int:
+    return lib().nvfp4_get_w4a16_rf_max_m()
+
+
+def nvfp4_set_weight_prefetch(enable: bool) -> None:
+    """Let GEMM kernels read static weights before the previous kernel ends."""
+    _check(lib().nvfp4_set_weight_prefetch(1 if enable else 0), "nvfp4_set_weight_prefetch")
+
+
+def nvfp4_get_weight_prefetch() -> bool:
+    return bool(lib().nvfp4_get_weight_prefetch())
 
 
 def nvfp4_get_device_status(stream=None) -> int:

@@ -1,6 +1,7 @@
 // api.cu -- the C ABI (include/nvfp4.h): argument checks, workspace layout,
 // dispatch between the W4A16 and W4A4 paths, device status word.
 #include <cmath>
+#include <atomic>
 #include <cstdio>
 #include <map>
 #include <mutex>
@@ -23,10 +24,16 @@ std::mutex g_mu;
 // Largest M that still takes the W4A16 path, per weight shape (N, K), and for
 // shapes without an entry.  Built-in values: the crossover of graph-timed
 // W4A16 vs activation quantisation + W4A4 measured on GB300 with
-// nvfp4_weight_quantized_gb300.tune (sweep M = 1..256); re-run it to retune.
+// nvfp4_weight_quantized_gb300.tune (sweep M = 1..256, cold weights, weight
+// prefetch on); re-run it to retune.
 std::map<std::pair<int64_t, int64_t>, int64_t> g_crossover = {
-    {{4096, 4096}, 64}, {{11008, 4096}, 16}, {{22016, 4096}, 8}, {{4096, 11008}, 16}};
-int64_t g_default_crossover = 16;
+    {{4096, 4096}, 64}, {{11008, 4096}, 48}, {{22016, 4096}, 32}, {{4096, 11008}, 64}};
+int64_t g_default_crossover = 48;
+// Largest M that nvfp4_gemm_w4a16 sends to the register-file kernel.
+std::atomic<int64_t> g_w4a16_rf_max_m{64};
+// Whether GEMM kernels may read the weights before the previous kernel in the
+// stream has finished (nvfp4_set_weight_prefetch).
+std::atomic<bool> g_weight_prefetch{false};
 
 struct DeviceInfo {
   bool ready = false;
@@ -193,8 +200,13 @@ nvfp4_status nvfp4_gemm_w4a16(const void* X, int64_t M, const nvfp4_weight* W, v
   if (!aligned(X, 16) || !aligned(Y, 16)) return fail(NVFP4_ERR_ALIGN, "X and Y must be 16-byte aligned");
   const DeviceInfo* d = nullptr;
   if ((st = device_info(&d)) != NVFP4_OK) return st;
-  cudaError_t err = nvfp4::launch_gemm_w4a16(X, M, W->codes, W->scales_mma, W->tensor_scale, W->N, W->K, Y,
-                                             out_dtype == NVFP4_OUT_F32, d->status, d->num_sms, stream);
+  const bool rf = M <= g_w4a16_rf_max_m.load(std::memory_order_relaxed);
+  cudaError_t err =
+      rf ? nvfp4::launch_gemm_w4a16_rf(X, M, W->codes, W->scales_mma, W->tensor_scale, W->N, W->K, Y,
+                                       out_dtype == NVFP4_OUT_F32, g_weight_prefetch.load(std::memory_order_relaxed),
+                                       d->status, d->num_sms, stream)
+         : nvfp4::launch_gemm_w4a16(X, M, W->codes, W->scales_mma, W->tensor_scale, W->N, W->K, Y,
+                                    out_dtype == NVFP4_OUT_F32, d->status, d->num_sms, stream);
   if (err == cudaErrorNotSupported) return fail(NVFP4_ERR_UNSUPPORTED, "gemm_w4a16: unsupported size");
   if (err != cudaSuccess) return fail_cuda(err, "gemm_w4a16 launch");
   return NVFP4_OK;
@@ -253,6 +265,21 @@ nvfp4_status nvfp4_set_crossover(int64_t N, int64_t K, int64_t M_threshold) {
   else g_crossover[{N, K}] = M_threshold;
   return NVFP4_OK;
 }
+
+nvfp4_status nvfp4_set_w4a16_rf_max_m(int64_t M) {
+  if (M < 0 || M > nvfp4::w4a16_rf_max_tokens()) return fail(NVFP4_ERR_INVALID_ARG, "w4a16 rf max M out of range");
+  g_w4a16_rf_max_m.store(M, std::memory_order_relaxed);
+  return NVFP4_OK;
+}
+
+int64_t nvfp4_get_w4a16_rf_max_m(void) { return g_w4a16_rf_max_m.load(std::memory_order_relaxed); }
+
+nvfp4_status nvfp4_set_weight_prefetch(int enable) {
+  g_weight_prefetch.store(enable != 0, std::memory_order_relaxed);
+  return NVFP4_OK;
+}
+
+int nvfp4_get_weight_prefetch(void) { return g_weight_prefetch.load(std::memory_order_relaxed) ? 1 : 0; }
 
 int64_t nvfp4_get_crossover(int64_t N, int64_t K) {
   std::lock_guard<std::mutex> lk(g_mu);

@@ -44,12 +44,25 @@ def test_workspace_bytes(L):
 def test_crossover_table(L):
     default = nv.nvfp4_get_crossover()
     assert default >= 1
+    saved = nv.nvfp4_get_crossover(4096, 4096)
     nv.nvfp4_set_crossover(4096, 4096, 17)
     assert nv.nvfp4_get_crossover(4096, 4096) == 17
-    assert nv.nvfp4_get_crossover(4096, 11008) == default
+    assert nv.nvfp4_get_crossover(12345, 4096) == default
     with pytest.raises(nv.NVFP4Error):
         nv.nvfp4_set_crossover(1, 1, -1)
-    nv.nvfp4_set_crossover(4096, 4096, default)
+    nv.nvfp4_set_crossover(4096, 4096, saved)
+
+
+def test_w4a16_kernel_knob(L):
+    saved = nv.nvfp4_get_w4a16_rf_max_m()
+    assert 0 <= saved <= 64
+    nv.nvfp4_set_w4a16_rf_max_m(0)
+    assert nv.nvfp4_get_w4a16_rf_max_m() == 0
+    for bad in (-1, 65):
+        with pytest.raises(nv.NVFP4Error):
+            nv.nvfp4_set_w4a16_rf_max_m(bad)
+    nv.nvfp4_set_w4a16_rf_max_m(saved)
+    assert nv.nvfp4_get_w4a16_rf_max_m() == saved
 
 
 def test_status_strings(L):

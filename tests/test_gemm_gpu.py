@@ -101,6 +101,46 @@ def test_w4a16_ragged(shape, M):
     run_w4a16(x, wref, K, nv.OUT_BF16)
 
 
+@pytest.mark.parametrize("M", [1, 8, 9, 17, 24, 31, 40, 48, 56, 64])
+def test_w4a16_both_kernels(M):
+    """The register-file kernel (every token-tile width it is built for) and
+    the tensor-memory kernel, forced in turn, both match the oracle."""
+    N, K = 328, 1344
+    wref = oracle_weight(synth.weight_normal(N, K, seed=77, outlier_frac=0.01))
+    x = synth.act_normal(M, K, seed=500 + M)
+    saved = nv.nvfp4_get_w4a16_rf_max_m()
+    try:
+        for rf in (64, 0):
+            nv.nvfp4_set_w4a16_rf_max_m(rf)
+            run_w4a16(x, wref, K, nv.OUT_F32)
+            run_w4a16(x, wref, K, nv.OUT_BF16)
+    finally:
+        nv.nvfp4_set_w4a16_rf_max_m(saved)
+
+
+def test_w4a16_weight_prefetch_chain():
+    """Back-to-back GEMMs with weight prefetch on (each kernel starts reading
+    its weights while the previous one runs) give the same results."""
+    shapes = [(384, 1024), (200, 2048), (640, 1024)]
+    wrefs = [oracle_weight(synth.weight_normal(N, K, seed=900 + i, outlier_frac=0.01))
+             for i, (N, K) in enumerate(shapes)]
+    Ws = [dev_weight(w, K) for w, (N, K) in zip(wrefs, shapes)]
+    torch.cuda.synchronize()
+    saved = nv.nvfp4_get_weight_prefetch()
+    try:
+        nv.nvfp4_set_weight_prefetch(True)
+        for M in (1, 16, 40):
+            xs = [synth.act_normal(M, K, seed=950 + M + i) for i, (N, K) in enumerate(shapes)]
+            ys = [nv.nvfp4_gemm_w4a16(to_dev(x), W, nv.OUT_F32) for x, W in zip(xs, Ws)]
+            torch.cuda.synchronize()
+            for x, y, w in zip(xs, ys, wrefs):
+                ref = oracle_w4a16(x, w["codes"], w["scales"], w["ts"])
+                assert_gemm_close(y_to_np(y), ref, bf16=False, what=f"prefetch M={M}")
+    finally:
+        nv.nvfp4_set_weight_prefetch(saved)
+    assert nv.nvfp4_get_device_status() == 0
+
+
 def test_w4a16_decode_shapes():
     wref = oracle_weight(synth.decode_weight())
     cols = sample_rows(4096, 384, 1)
