@@ -27,6 +27,27 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// L2 policies: the amax pass marks the tensor "evict last" so that the
+// quantisation pass that follows finds it in L2 when it fits (a 4096 x 4096
+// bf16 weight is 32 MiB of the 126 MiB L2); that pass reads it "evict first".
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint4 ld_u4_policy(const void* ptr, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr), "l"(policy));
+  return v;
+}
+
 __device__ __forceinline__ uint32_t block_reduce_max(uint32_t v, uint32_t* red) {
   v = __reduce_max_sync(0xffffffffu, v);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -47,12 +68,13 @@ amax_partial_kernel(const uint4* __restrict__ x, int64_t n_vec, uint32_t* __rest
   __shared__ uint32_t red[kThreads / 32];
   griddep_wait();
   uint32_t m2 = 0;  // two running maxima of bf16 magnitude bits, one per half
+  const uint64_t pol = l2_policy_evict_last();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   for (; i + 3 * stride < n_vec; i += 4 * stride) {
     uint4 v[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = ld_stream_u4(x + i + u * stride);
+    for (int u = 0; u < 4; ++u) v[u] = ld_u4_policy(x + i + u * stride, pol);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       m2 = __vmaxu2(m2, v[u].x & 0x7FFF7FFFu);
@@ -62,7 +84,7 @@ amax_partial_kernel(const uint4* __restrict__ x, int64_t n_vec, uint32_t* __rest
     }
   }
   for (; i < n_vec; i += stride) {
-    uint4 v = ld_stream_u4(x + i);
+    uint4 v = ld_u4_policy(x + i, pol);
     m2 = __vmaxu2(m2, v.x & 0x7FFF7FFFu);
     m2 = __vmaxu2(m2, v.y & 0x7FFF7FFFu);
     m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
@@ -129,7 +151,8 @@ __device__ __forceinline__ uint32_t exact_pair(float x0, float x1, float eff) {
 // the 16 magnitude codes packed 8 per word (element 0 in the lowest nibble);
 // the caller attaches the signs (the squared error of x equals that of |x|).
 //
-// Codes: with r = RN(1/eff), the products x * RN(r * (1 -/+ 2^-20)) bracket
+// Codes: with r ~ 1/eff (the hardware reciprocal approximation, relative
+// error below 2^-22), the products x * RN(r * (1 -/+ 2^-20)) bracket
 // RN(x / eff); when both ends convert to the same E2M1 code, that is the code
 // of RN(x / eff) (the conversion is monotone).  A pair whose ends differ (its
 // quotient lies within ~2^-20 of a rounding midpoint -- common, since x and
@@ -145,7 +168,8 @@ __device__ __forceinline__ float cand(const f2 (&x2)[8], float bmax, float eff, 
 #pragma unroll
     for (int j = 0; j < 8; ++j) bl[j] = 0u;
   } else {
-    const float r = __frcp_rn(eff);
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(eff));
     if (eff >= 0x1p-100f && __fmul_rn(bmax, r) < 0x1p100f) {
       const float rlo = __fmul_rn(r, 0.99999904632568359375f);  // 1 - 2^-20
       const float rhi = __fmul_rn(r, 1.00000095367431640625f);  // 1 + 2^-20
@@ -205,6 +229,9 @@ quant_kernel(const uint4* __restrict__ x, int64_t rows, int64_t K, const uint32_
   const float amax = __uint_as_float(am << 16);
   const float ts = amax == 0.0f ? 1.0f : __fdiv_rn(amax, divisor);
   if (blockIdx.x == 0 && threadIdx.x == 0) *ts_out = ts;
+  // the bracketed s6 needs 6 * ts (and so its reciprocal) in the normal range
+  const bool fast6 = __fmul_rn(6.0f, ts) >= 0x1p-126f;
+  const float inv6ts = fast6 ? __frcp_rn(__fmul_rn(6.0f, ts)) : 0.0f;
 
   const int64_t kb = K >> 4;
   const int64_t ct = (kb + 3) >> 2;
@@ -216,9 +243,19 @@ quant_kernel(const uint4* __restrict__ x, int64_t rows, int64_t K, const uint32_
   int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   int64_t r = blk / kb, c = blk - r * kb;
   uint32_t n_m4 = 0;
+  const uint64_t pol = l2_policy_evict_first();
+  // the next block's 32 bytes are loaded while this one is processed
+  uint4 n0 = make_uint4(0, 0, 0, 0), n1 = n0;
+  if (blk < nblk) {
+    n0 = ld_u4_policy(x + 2 * blk, pol);
+    n1 = ld_u4_policy(x + 2 * blk + 1, pol);
+  }
   for (; blk < nblk; blk += stride) {
-    const uint4 v0 = ld_stream_u4(x + 2 * blk);
-    const uint4 v1 = ld_stream_u4(x + 2 * blk + 1);
+    const uint4 v0 = n0, v1 = n1;
+    if (blk + stride < nblk) {
+      n0 = ld_u4_policy(x + 2 * (blk + stride), pol);
+      n1 = ld_u4_policy(x + 2 * (blk + stride) + 1, pol);
+    }
     const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
     f2 x2[8];  // magnitudes, elements (2j, 2j+1)
     uint32_t m2 = 0;
@@ -240,9 +277,18 @@ quant_kernel(const uint4* __restrict__ x, int64_t rows, int64_t K, const uint32_
       sgn[h] = ((g1 >> 4) & 0x08080808u) | (g3 & 0x80808080u);
     }
     const float bmax = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
-    // s6 = E4M3((amax_block / 6) / ts)
-    const float r6 = __fdiv_rn(__fdiv_rn(bmax, 6.0f), ts);
-    const uint32_t s6 = cvt_e4m3x2(0.0f, r6) & 0xFFu;
+    // s6 = E4M3((amax_block / 6) / ts).  bmax * inv6ts is within 2^-21 of the
+    // twice-rounded quotient (relative; tiny quotients are far below the
+    // smallest E4M3 step either way), so the two ends of a 2^-20 bracket
+    // convert to the same E4M3 code unless the quotient is within ~2^-20 of
+    // a rounding midpoint -- then the quotient is formed as written.
+    uint32_t s6;
+    {
+      const float q = __fmul_rn(bmax, inv6ts);
+      const uint32_t c2 = cvt_e4m3x2(__fmul_rn(q, 1.00000095367431640625f), __fmul_rn(q, 0.99999904632568359375f));
+      s6 = c2 & 0xFFu;
+      if (__builtin_expect(!fast6 || s6 != (c2 >> 8), 0)) s6 = cvt_e4m3x2(0.0f, __fdiv_rn(__fdiv_rn(bmax, 6.0f), ts)) & 0xFFu;
+    }
     const float s6v = e4m3_to_f32(s6);
     uint32_t cw[2];
     const float sse6 = cand(x2, bmax, __fmul_rn(s6v, ts), cw);

@@ -136,6 +136,40 @@ def test_exact_ties_on_the_e2m1_grid():
     check_act(x)
 
 
+def test_block_scale_ties_on_the_e4m3_grid():
+    """Blocks whose amax / 6 / ts is exactly an E4M3 rounding midpoint (and
+    one bf16 step either side), with ts a power of two: the M=6 scale must
+    round ties to even exactly as the oracle's binary32 steps do."""
+    vals = []
+    for e in range(-6, 9):          # normal E4M3 binades 2^-6 .. 2^8
+        for m in range(8):
+            lo = 2.0 ** e * (1 + m / 8)
+            hi = 2.0 ** e * (1 + (m + 1) / 8)
+            if hi <= 448:
+                vals.append((lo + hi) / 2)
+    for m in range(1, 8):           # subnormal steps m * 2^-9
+        vals.append((m + 0.5) * 2.0 ** -9)
+    ts = 2.0 ** -5
+    amax = 2688 * ts                # tensor scale exactly ts
+    blocks = []
+    for v in vals:
+        b = np.float32(6 * v * ts)
+        for delta in (-1, 0, 1):    # one bf16 step below / at / above the midpoint
+            bits = synth.f32_to_bf16_bits(np.array([b], np.float32))[0].astype(np.int64) + delta
+            blk = np.zeros(16, np.uint16)
+            blk[0] = np.uint16(bits)
+            blk[5] = synth.f32_to_bf16_bits(np.array([b * np.float32(0.3)], np.float32))[0]
+            blocks.append(blk)
+    head = np.zeros(16, np.uint16)
+    head[0] = synth.f32_to_bf16_bits(np.array([amax], np.float32))[0]
+    blocks.append(head)
+    rows = (len(blocks) + 7) // 8
+    while len(blocks) < rows * 8:
+        blocks.append(np.zeros(16, np.uint16))
+    w = np.stack(blocks).reshape(rows, 8 * 16)
+    check_fos(w)
+
+
 def test_zero_and_negative_zero():
     z = np.zeros((4, 64), np.uint16)
     z[1, 5] = 0x8000
