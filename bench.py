@@ -276,10 +276,10 @@ def run_ours(args):
     w16_time = sum(lin_avg[M] for M in DECODE_M if paths[M] == "w4a16")
     w16_bytes = sum(w4a16_bytes(M, N, K) for M in DECODE_M if paths[M] == "w4a16")
     if w16_time >= q_avg and w16_time > 0:
-        dom = "gemm_w4a16"
+        dom = "gemm_w4a16 (w4a16_rf_kernel)"
         achieved = w16_bytes / w16_time / 1e9
         traffic = traffic_from_profiles("w4a16_decode", os.path.join(ROOT, "nvfp4_weight_quantized_gb300",
-                                                                     "csrc", "gemm_w4a16.cu"))
+                                                                     "csrc", "gemm_w4a16_rf.cu"))
         launches = sum(1 for M in DECODE_M if paths[M] == "w4a16")
         if traffic is not None:
             traffic = traffic  # bytes per launch averaged over the M sweep
@@ -378,6 +378,9 @@ def measure_e2e(nv, dev, stream, w_bits, args, step_bytes, paths):
     region."""
     import torch
     N, K = N_DEC, K_DEC
+    # this step quantises the weight and then runs the GEMMs on it: the GEMMs
+    # must not read it before the quantiser has finished
+    nv.nvfp4_set_weight_prefetch(False)
     hW = torch.from_numpy(w_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
     hX = {M: torch.from_numpy(synth.decode_act(M).view(np.int16)).view(torch.bfloat16).pin_memory()
           for M in DECODE_M}

@@ -38,7 +38,9 @@
  *     reported by nvfp4_get_device_status().
  *   - Pointers to tensors must be 16-byte aligned (NVFP4_ERR_ALIGN).
  *   - The library keeps no state between calls except the crossover table
- *     (nvfp4_set_crossover) and the device status word.
+ *     (nvfp4_set_crossover), the W4A16 kernel knob
+ *     (nvfp4_set_w4a16_rf_max_m), the weight-prefetch flag
+ *     (nvfp4_set_weight_prefetch) and the device status word.
  */
 #ifndef NVFP4_H_
 #define NVFP4_H_
