@@ -71,12 +71,13 @@ amax_partial_kernel(const uint4* __restrict__ x, int64_t n_vec, uint32_t* __rest
   const uint64_t pol = l2_policy_evict_last();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (; i + 3 * stride < n_vec; i += 4 * stride) {
-    uint4 v[4];
+  // eight 16-byte loads in flight per thread
+  for (; i + 7 * stride < n_vec; i += 8 * stride) {
+    uint4 v[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = ld_u4_policy(x + i + u * stride, pol);
+    for (int u = 0; u < 8; ++u) v[u] = ld_u4_policy(x + i + u * stride, pol);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
       m2 = __vmaxu2(m2, v[u].x & 0x7FFF7FFFu);
       m2 = __vmaxu2(m2, v[u].y & 0x7FFF7FFFu);
       m2 = __vmaxu2(m2, v[u].z & 0x7FFF7FFFu);
@@ -174,18 +175,26 @@ __device__ __forceinline__ float cand(const f2 (&x2)[8], float bmax, float eff, 
       const float rlo = __fmul_rn(r, 0.99999904632568359375f);  // 1 - 2^-20
       const float rhi = __fmul_rn(r, 1.00000095367431640625f);  // 1 + 2^-20
       const f2 rl2 = pk(rlo, rlo), rh2 = pk(rhi, rhi);
+      uint32_t differ = 0;  // OR of (low end code ^ high end code) over the pairs
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         float l0, l1, h0, h1;
         upk(mul2(x2[j], rl2), l0, l1);
         upk(mul2(x2[j], rh2), h0, h1);
-        uint32_t cl = cvt_e2m1x2(l1, l0);
-        if (__builtin_expect(cl != cvt_e2m1x2(h1, h0), 0)) {
-          float x0, x1;
-          upk(x2[j], x0, x1);
-          cl = exact_pair(x0, x1, eff);
+        bl[j] = cvt_e2m1x2(l1, l0);
+        differ |= bl[j] ^ cvt_e2m1x2(h1, h0);
+      }
+      if (__builtin_expect(differ != 0, 0)) {  // rare: redo the ambiguous pairs by division
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float l0, l1, h0, h1, x0, x1;
+          upk(mul2(x2[j], rl2), l0, l1);
+          upk(mul2(x2[j], rh2), h0, h1);
+          if (cvt_e2m1x2(l1, l0) != cvt_e2m1x2(h1, h0)) {
+            upk(x2[j], x0, x1);
+            bl[j] = exact_pair(x0, x1, eff);
+          }
         }
-        bl[j] = cl;
       }
     } else {
 #pragma unroll
@@ -212,7 +221,7 @@ __device__ __forceinline__ float cand(const f2 (&x2)[8], float bmax, float eff, 
 }
 
 template <bool kFos>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
 quant_kernel(const uint4* __restrict__ x, int64_t rows, int64_t K, const uint32_t* __restrict__ partial,
              int n_partial, float divisor, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
              uint8_t* __restrict__ scales_mma, float* __restrict__ ts_out, uint8_t* __restrict__ choice,
@@ -233,113 +242,114 @@ quant_kernel(const uint4* __restrict__ x, int64_t rows, int64_t K, const uint32_
   const bool fast6 = __fmul_rn(6.0f, ts) >= 0x1p-126f;
   const float inv6ts = fast6 ? __frcp_rn(__fmul_rn(6.0f, ts)) : 0.0f;
 
-  const int64_t kb = K >> 4;
-  const int64_t ct = (kb + 3) >> 2;
-  const int64_t nblk = rows * kb;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  // (row, block column) of this thread's block, advanced by the grid stride
-  // without a division inside the loop
-  const int64_t stride_r = stride / kb, stride_c = stride - stride_r * kb;
-  int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  int64_t r = blk / kb, c = blk - r * kb;
+  // Work unit: one tile of the MMA scale layout, 128 rows x 4 blocks of 16
+  // (64 K positions); thread i of the CTA takes blocks (i/4, i%4) and
+  // (i/4 + 64, i%4), so a warp reads 8 rows x 128 contiguous bytes and the
+  // tile's 512 scale bytes are staged in shared memory and written as one
+  // coalesced 512-byte store (padding rows and columns become 0 there).
+  const int kb = (int)(K >> 4);
+  const int ct = (kb + 3) >> 2;
+  const int64_t tiles_r = (rows + 127) >> 7;
+  const int64_t ntiles = tiles_r * ct;
+  const int ri = threadIdx.x >> 2, ci = threadIdx.x & 3;
+  __shared__ __align__(16) uint8_t stage[2][kScaleTileBytes];
   uint32_t n_m4 = 0;
   const uint64_t pol = l2_policy_evict_first();
-  // the next block's 32 bytes are loaded while this one is processed
-  uint4 n0 = make_uint4(0, 0, 0, 0), n1 = n0;
-  if (blk < nblk) {
-    n0 = ld_u4_policy(x + 2 * blk, pol);
-    n1 = ld_u4_policy(x + 2 * blk + 1, pol);
-  }
-  for (; blk < nblk; blk += stride) {
-    const uint4 v0 = n0, v1 = n1;
-    if (blk + stride < nblk) {
-      n0 = ld_u4_policy(x + 2 * (blk + stride), pol);
-      n1 = ld_u4_policy(x + 2 * (blk + stride) + 1, pol);
-    }
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    f2 x2[8];  // magnitudes, elements (2j, 2j+1)
-    uint32_t m2 = 0;
+  int buf = 0;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, buf ^= 1) {
+    const int64_t tr = t / ct;
+    const int tc = (int)(t - tr * ct);
+    const int c = tc * 4 + ci;
+    int64_t rr[2];
+    bool ok[2];
+    uint4 v[2][2];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t a = w[j] & 0x7FFF7FFFu;
-      x2[j] = pk(__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u));
-      m2 = __vmaxu2(m2, a);
+    for (int h = 0; h < 2; ++h) {  // both blocks' loads go out first
+      rr[h] = tr * 128 + ri + 64 * h;
+      ok[h] = rr[h] < rows && c < kb;
+      if (ok[h]) {
+        const uint4* p = x + rr[h] * (K >> 3) + 2 * c;
+        v[h][0] = ld_u4_policy(p, pol);
+        v[h][1] = ld_u4_policy(p + 1, pol);
+      }
     }
-    // sign bits of the 16 codes: byte j of sgn[h] gets the signs of elements
-    // 8h+2j (bit 3) and 8h+2j+1 (bit 7), i.e. bit 15 and bit 31 of word 4h+j
-    uint32_t sgn[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const uint32_t g1 = __byte_perm(__byte_perm(w[4 * h], w[4 * h + 1], 0x0051u),
-                                      __byte_perm(w[4 * h + 2], w[4 * h + 3], 0x0051u), 0x5410u);
-      const uint32_t g3 = __byte_perm(__byte_perm(w[4 * h], w[4 * h + 1], 0x0073u),
-                                      __byte_perm(w[4 * h + 2], w[4 * h + 3], 0x0073u), 0x5410u);
-      sgn[h] = ((g1 >> 4) & 0x08080808u) | (g3 & 0x80808080u);
-    }
-    const float bmax = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
-    // s6 = E4M3((amax_block / 6) / ts).  bmax * inv6ts is within 2^-21 of the
-    // twice-rounded quotient (relative; tiny quotients are far below the
-    // smallest E4M3 step either way), so the two ends of a 2^-20 bracket
-    // convert to the same E4M3 code unless the quotient is within ~2^-20 of
-    // a rounding midpoint -- then the quotient is formed as written.
-    uint32_t s6;
-    {
-      const float q = __fmul_rn(bmax, inv6ts);
-      const uint32_t c2 = cvt_e4m3x2(__fmul_rn(q, 1.00000095367431640625f), __fmul_rn(q, 0.99999904632568359375f));
-      s6 = c2 & 0xFFu;
-      if (__builtin_expect(!fast6 || s6 != (c2 >> 8), 0)) s6 = cvt_e4m3x2(0.0f, __fdiv_rn(__fdiv_rn(bmax, 6.0f), ts)) & 0xFFu;
-    }
-    const float s6v = e4m3_to_f32(s6);
-    uint32_t cw[2];
-    const float sse6 = cand(x2, bmax, __fmul_rn(s6v, ts), cw);
-    uint32_t s = s6;
-    if (kFos) {
-      const uint32_t s4 = cvt_e4m3x2(0.0f, __fmul_rn(s6v, 1.5f)) & 0xFFu;
-      bool m4 = false;
-      if (s4 != s6) {  // equal scales tie, and a tie keeps M=6
-        uint32_t cw4[2];
-        const float sse4 = cand(x2, bmax, __fmul_rn(e4m3_to_f32(s4), ts), cw4);
-        m4 = sse4 < sse6;
-        if (m4) {
-          cw[0] = cw4[0];
-          cw[1] = cw4[1];
-          s = s4;
-          ++n_m4;
+      uint32_t s = 0;
+      if (ok[h]) {
+        const uint32_t w[8] = {v[h][0].x, v[h][0].y, v[h][0].z, v[h][0].w,
+                               v[h][1].x, v[h][1].y, v[h][1].z, v[h][1].w};
+        f2 x2[8];  // magnitudes, elements (2j, 2j+1)
+        uint32_t m2 = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t a = w[j] & 0x7FFF7FFFu;
+          x2[j] = pk(__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u));
+          m2 = __vmaxu2(m2, a);
         }
+        // sign bits of the 16 codes: byte j of sgn[q] gets the signs of elements
+        // 8q+2j (bit 3) and 8q+2j+1 (bit 7), i.e. bit 15 and bit 31 of word 4q+j
+        uint32_t sgn[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint32_t g1 = __byte_perm(__byte_perm(w[4 * q], w[4 * q + 1], 0x0051u),
+                                          __byte_perm(w[4 * q + 2], w[4 * q + 3], 0x0051u), 0x5410u);
+          const uint32_t g3 = __byte_perm(__byte_perm(w[4 * q], w[4 * q + 1], 0x0073u),
+                                          __byte_perm(w[4 * q + 2], w[4 * q + 3], 0x0073u), 0x5410u);
+          sgn[q] = ((g1 >> 4) & 0x08080808u) | (g3 & 0x80808080u);
+        }
+        const float bmax = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
+        // s6 = E4M3((amax_block / 6) / ts).  bmax * inv6ts is within 2^-21 of
+        // the twice-rounded quotient (relative; tiny quotients are far below
+        // the smallest E4M3 step either way), so the two ends of a 2^-20
+        // bracket convert to the same E4M3 code unless the quotient is within
+        // ~2^-20 of a rounding midpoint -- then it is formed as written.
+        uint32_t s6;
+        {
+          const float q = __fmul_rn(bmax, inv6ts);
+          const uint32_t c2 =
+              cvt_e4m3x2(__fmul_rn(q, 1.00000095367431640625f), __fmul_rn(q, 0.99999904632568359375f));
+          s6 = c2 & 0xFFu;
+          if (__builtin_expect(!fast6 || s6 != (c2 >> 8), 0))
+            s6 = cvt_e4m3x2(0.0f, __fdiv_rn(__fdiv_rn(bmax, 6.0f), ts)) & 0xFFu;
+        }
+        const float s6v = e4m3_to_f32(s6);
+        uint32_t cw[2];
+        const float sse6 = cand(x2, bmax, __fmul_rn(s6v, ts), cw);
+        s = s6;
+        const int64_t blk = rr[h] * kb + c;
+        if (kFos) {
+          const uint32_t s4 = cvt_e4m3x2(0.0f, __fmul_rn(s6v, 1.5f)) & 0xFFu;
+          bool m4 = false;
+          if (s4 != s6) {  // equal scales tie, and a tie keeps M=6
+            uint32_t cw4[2];
+            const float sse4 = cand(x2, bmax, __fmul_rn(e4m3_to_f32(s4), ts), cw4);
+            m4 = sse4 < sse6;
+            if (m4) {
+              cw[0] = cw4[0];
+              cw[1] = cw4[1];
+              s = s4;
+              ++n_m4;
+            }
+          }
+          if (choice != nullptr) choice[blk] = m4 ? 1 : 0;
+        }
+        *reinterpret_cast<uint2*>(codes + 8 * blk) = make_uint2(cw[0] | sgn[0], cw[1] | sgn[1]);
+        if (scales != nullptr) scales[blk] = (uint8_t)s;
       }
-      if (choice != nullptr) choice[blk] = m4 ? 1 : 0;
+      if (scales_mma != nullptr) {
+        const int r = ri + 64 * h;  // row inside the tile
+        stage[buf][(r & 31) * 16 + (r >> 5) * 4 + ci] = (uint8_t)s;
+      }
     }
-    *reinterpret_cast<uint2*>(codes + 8 * blk) = make_uint2(cw[0] | sgn[0], cw[1] | sgn[1]);
-    if (scales != nullptr) scales[blk] = (uint8_t)s;
-    if (scales_mma != nullptr) scales_mma[scale_mma_offset(r, c, ct)] = (uint8_t)s;
-    r += stride_r;
-    c += stride_c;
-    if (c >= kb) {
-      c -= kb;
-      ++r;
+    if (scales_mma != nullptr) {
+      __syncthreads();
+      if (threadIdx.x < kScaleTileBytes / 16)
+        reinterpret_cast<uint4*>(scales_mma + t * kScaleTileBytes)[threadIdx.x] =
+            reinterpret_cast<const uint4*>(stage[buf])[threadIdx.x];
     }
   }
   griddep_launch_dependents();
-  // zero the padding of the MMA scale tiling (rows up to a multiple of 128,
-  // scale columns up to a multiple of 4)
-  if (scales_mma != nullptr) {
-    const int64_t rows_p = (rows + 127) & ~int64_t(127), cols_p = ct * 4;
-    const int64_t pad_cols = cols_p - kb;
-    const int64_t n_pad_a = rows * pad_cols;              // real rows, padded columns
-    const int64_t n_pad_b = (rows_p - rows) * cols_p;     // padded rows, all columns
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_pad_a + n_pad_b; i += stride) {
-      int64_t r, c;
-      if (i < n_pad_a) {
-        r = i / pad_cols;
-        c = kb + (i - r * pad_cols);
-      } else {
-        const int64_t j = i - n_pad_a;
-        r = rows + j / cols_p;
-        c = j % cols_p;
-      }
-      scales_mma[scale_mma_offset(r, c, ct)] = 0;
-    }
-  }
   if (kFos && m4_count != nullptr) {
     n_m4 = __reduce_add_sync(0xffffffffu, n_m4);
     if ((threadIdx.x & 31) == 0 && n_m4) atomicAdd(m4_count, (unsigned long long)n_m4);
@@ -370,8 +380,8 @@ cudaError_t launch_quantize(const void* x, int64_t rows, int64_t K, float diviso
   cudaError_t err = cudaLaunchKernelEx(&cfg, amax_partial_kernel, static_cast<const uint4*>(x), n_vec, partial,
                                        fos ? m4_count : (unsigned long long*)nullptr);
   if (err != cudaSuccess) return err;
-  const int64_t nblk = rows * (K / 16);
-  int g2 = (int)std::min<int64_t>((nblk + kThreads - 1) / kThreads, (int64_t)num_sms * 8);
+  const int64_t ntiles = ((rows + 127) / 128) * ((K / 16 + 3) / 4);
+  int g2 = (int)std::min<int64_t>(ntiles, (int64_t)num_sms * 8);
   cfg.gridDim = dim3(std::max(g2, 1));
   if (fos)
     return cudaLaunchKernelEx(&cfg, quant_kernel<true>, static_cast<const uint4*>(x), rows, K,

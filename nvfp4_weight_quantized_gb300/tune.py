@@ -17,31 +17,51 @@ from . import (OUT_BF16, NVFP4Weight, lib, nvfp4_gemm_w4a16, nvfp4_gemm_w4a4, nv
 DEFAULT_SWEEP = (1, 2, 4, 8, 16, 24, 32, 48, 64, 96, 128, 192, 256)
 
 
-def _time_graph(fn, reps: int, stream) -> float:
+def _time_graphs(fn, reps: int, nsets: int, stream) -> float:
+    """Seconds per call of fn(i): nsets graphs of `reps` calls each (call i of
+    set k gets index k * reps + i), replayed once to warm up, then timed as
+    one pass over all sets, so that no call reuses what the previous replay
+    left in L2 when the indexed data is larger than L2."""
     with torch.cuda.stream(stream):
-        for _ in range(2):
-            fn(0)
-    stream.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for i in range(reps):
+        for i in range(2):
             fn(i)
+    stream.synchronize()
+    graphs = []
+    for k in range(nsets):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(reps):
+                fn(k * reps + i)
+        graphs.append(g)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        g.replay()
+        for g in graphs:
+            g.replay()
         e0.record(stream)
-        g.replay()
+        for g in graphs:
+            g.replay()
         e1.record(stream)
     e1.synchronize()
-    return e0.elapsed_time(e1) * 1e-3 / reps
+    return e0.elapsed_time(e1) * 1e-3 / (reps * nsets)
 
 
-def measure(N: int, K: int, sweep=DEFAULT_SWEEP, copies: int = 16, reps: int = 16, seed: int = 0):
-    """Per-M seconds per call of both paths: {M: (t_w4a16, t_w4a4)}."""
+def _time_graph(fn, reps: int, stream) -> float:
+    return _time_graphs(fn, reps, 1, stream)
+
+
+def measure(N: int, K: int, sweep=DEFAULT_SWEEP, copies: int = 0, reps: int = 16, seed: int = 0):
+    """Per-M seconds per call of both paths: {M: (t_w4a16, t_w4a4)}.  The
+    weight is copied `copies` times (default: enough for twice the L2) and
+    every timed call reads a different copy."""
     dev = torch.device("cuda")
     gen = torch.Generator(device=dev).manual_seed(seed)
     w = (torch.randn(N, K, device=dev, generator=gen) * 0.02).to(torch.bfloat16)
     q = nvfp4_quantize_fos(w, logical_scales=False, choice=False)
+    wbytes = N * K // 2 + N * K // 16
+    if copies <= 0:
+        copies = max(2 * reps, -(-2 * 126 * 2**20 // wbytes))
+    nsets = max(1, -(-copies // reps))
+    copies = nsets * reps
     Ws = [NVFP4Weight(q.codes.clone(), q.scales_mma.clone(), q.tensor_scale.clone(), N, K)
           for _ in range(copies)]
     stream = torch.cuda.Stream(device=dev)
@@ -62,7 +82,7 @@ def measure(N: int, K: int, sweep=DEFAULT_SWEEP, copies: int = 16, reps: int = 1
             assert st == 0
             nvfp4_gemm_w4a4(a, Ws[i % copies], OUT_BF16, out=y, stream=stream)
 
-        out[M] = (_time_graph(f16, reps, stream), _time_graph(f4, reps, stream))
+        out[M] = (_time_graphs(f16, reps, nsets, stream), _time_graphs(f4, reps, nsets, stream))
     return out
 
 
