@@ -25,6 +25,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -39,7 +40,6 @@ using namespace sm100;
 
 constexpr int BM = 128;             // tokens per tile (MMA M = TMEM lanes)
 constexpr int BK = 256;             // FP4 elements per stage (128 bytes per row)
-constexpr int kStages = 4;
 constexpr int kEpiWarps = 4, kSfWarps = 4;
 constexpr int kProducerWarp = kEpiWarps + kSfWarps, kMmaWarp = kProducerWarp + 1;
 constexpr int kThreads = 32 * (kMmaWarp + 1);
@@ -49,6 +49,10 @@ constexpr int kSfaBytes = (BK / 64) * kScaleTileBytes;    // 2 KB: 4 atoms (one 
 
 template <int BN>
 struct Cfg {
+  // operand stages: 3 for the wide tile, whose epilogue also stages half an
+  // output tile (32 KB) in shared memory for TMA stores; 4 for the narrow one
+  static constexpr int kStages = BN == 256 ? 3 : 4;
+  static constexpr int kYStageBytes = BN == 256 ? 2 * BM * 128 : 1024;  // two 128 x 64 bf16 boxes (unused at BN = 64)
   static constexpr int kBBytes = BN * BK / 2;
   static constexpr int kSfbTiles = (BN + 127) / 128;                        // 128-row scale tiles
   static constexpr int kSfbBytes = kSfbTiles * (BK / 64) * kScaleTileBytes;
@@ -67,6 +71,8 @@ struct Cfg {
 
 template <int BN>
 struct __align__(1024) Smem {
+  static constexpr int kStages = Cfg<BN>::kStages;
+  uint8_t ystage[Cfg<BN>::kYStageBytes];  // first: 1024-aligned for the 128-byte swizzle
   uint8_t a[kStages][kABytes];
   uint8_t b[kStages][Cfg<BN>::kBBytes];
   uint8_t sfa[kStages][kSfaBytes];
@@ -89,6 +95,13 @@ __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[
       ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
+}
+
+// Two floats -> bf16 pair (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -135,10 +148,11 @@ __device__ __forceinline__ void store_row32(void* y, int64_t row_off, int64_t n,
 template <int BN, bool kF32>
 __global__ void __launch_bounds__(kThreads, 1)
 w4a4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-            const uint8_t* __restrict__ a_smma, const uint8_t* __restrict__ b_smma,
+            const __grid_constant__ CUtensorMap tmap_y, int tma_store, const uint8_t* __restrict__ a_smma, const uint8_t* __restrict__ b_smma,
             const float* __restrict__ a_ts, const float* __restrict__ b_ts, int64_t M, int64_t N, int64_t K,
             void* __restrict__ y, unsigned int* __restrict__ status) {
   using C = Cfg<BN>;
+  constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   Smem<BN>& sm = *reinterpret_cast<Smem<BN>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -318,6 +332,53 @@ w4a4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
           for (int c = 0; c < BN / 32; ++c)
             if (n0 + 32 * c < N) store_row32<kF32>(y, row * N, n0 + 32 * c, N, v[c], alpha, vec_ok);
         }
+      } else if (!kF32 && BN == 256 && tma_store) {
+        // wide tile, bf16: each half (128 columns) is converted into two
+        // 128 x 64 bf16 boxes in shared memory (128-byte swizzle) and written
+        // by TMA stores; the accumulator goes back to the MMA warp as soon as
+        // its last columns are in registers, so the stores overlap the next
+        // tile's MMAs.  The TMA clips rows and columns outside Y.
+        const int r = warp * 32 + lane;  // tile row = TMEM lane
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+          asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");  // staging buffer free
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            const int c = 4 * half + cc;
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tmem + lane_base + C::kAccCol + 32 * c, v);
+            tmem_wait_ld();
+            if (c == BN / 32 - 1) {
+              fence_before_sync();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&sm.acc_free);
+            }
+            uint8_t* box = sm.ystage + (cc >> 1) * (BM * 128) + r * 128;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {  // 16-byte unit (cc & 1) * 4 + u of the row, swizzled
+              const uint4 p = make_uint4(
+                  bf16x2_rn(__uint_as_float(v[8 * u]) * alpha, __uint_as_float(v[8 * u + 1]) * alpha),
+                  bf16x2_rn(__uint_as_float(v[8 * u + 2]) * alpha, __uint_as_float(v[8 * u + 3]) * alpha),
+                  bf16x2_rn(__uint_as_float(v[8 * u + 4]) * alpha, __uint_as_float(v[8 * u + 5]) * alpha),
+                  bf16x2_rn(__uint_as_float(v[8 * u + 6]) * alpha, __uint_as_float(v[8 * u + 7]) * alpha));
+              const int unit = ((cc & 1) * 4 + u) ^ (r & 7);
+              *reinterpret_cast<uint4*>(box + unit * 16) = p;
+            }
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+          if (threadIdx.x == 0) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              asm volatile(
+                  "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(&tmap_y),
+                  "r"((int)(n0 + 128 * half + 64 * j)), "r"((int)(m_tile * BM)),
+                  "r"(smem_addr(sm.ystage + j * (BM * 128)))
+                  : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          }
+        }
       } else {
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
@@ -332,6 +393,8 @@ w4a4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       }
     }
     if (failed && lane == 0) atomicOr(status, kStatusTimeout);
+    // the output stores must be complete before the grid ends
+    if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
   fence_before_sync();
   __syncthreads();
@@ -373,14 +436,32 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_by
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Y as bf16 [M, N] for TMA stores: boxes of 128 rows x 64 columns (128
+// bytes), 128-byte swizzle.
+bool make_y_map(CUtensorMap* map, void* y, uint64_t M, uint64_t N) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {N, M};
+  cuuint64_t strides[1] = {N * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)BM};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int BN>
 cudaError_t launch_bn(const uint8_t* a_codes, const uint8_t* a_smma, const float* a_ts, int64_t M,
                       const uint8_t* w_codes, const uint8_t* w_smma, const float* w_ts, int64_t N, int64_t K,
                       void* y, bool out_f32, unsigned int* status, int num_sms, cudaStream_t stream) {
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, my;
   if (!make_map(&ma, a_codes, (uint64_t)M, (uint64_t)K / 2, BM) ||
       !make_map(&mb, w_codes, (uint64_t)N, (uint64_t)K / 2, BN))
     return cudaErrorInvalidValue;
+  // TMA stores of the output: bf16, wide tiles, rows of Y 16-byte aligned
+  int tma_store = (!out_f32 && BN == 256 && N % 8 == 0) ? 1 : 0;
+  memset(&my, 0, sizeof my);
+  if (tma_store && !make_y_map(&my, y, (uint64_t)M, (uint64_t)N)) tma_store = 0;
   // one CTA per SM: each allocates all 512 TMEM columns, which the block
   // scheduler does not count, so ask for enough shared memory that a second
   // CTA never lands on the same SM (228 KB per SM)
@@ -399,7 +480,7 @@ cudaError_t launch_bn(const uint8_t* a_codes, const uint8_t* a_smma, const float
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, ma, mb, a_smma, w_smma, a_ts, w_ts, M, N, K, y, status);
+  return cudaLaunchKernelEx(&cfg, kern, ma, mb, my, tma_store, a_smma, w_smma, a_ts, w_ts, M, N, K, y, status);
 }
 
 }  // namespace
