@@ -162,9 +162,9 @@ nvfp4_status nvfp4_gemm_w4a16(const void* X, int64_t M, const nvfp4_weight* W, v
                               cudaStream_t stream);
 
 /*
- * W4A4 GEMM (same section: the path above the crossover, "natively invoking
- * NVFP4 MMA instructions"): block-scaled FP4 x FP4 tensor-core MMA with fp32
- * accumulation,
+ * W4A4 GEMM (same section: above the crossover the GEMM runs on the native
+ * NVFP4 tensor-core instruction): block-scaled FP4 x FP4 tensor-core MMA with
+ * fp32 accumulation,
  *   Y[m, n] = ts_a * ts_w * sum_k value(qa[m,k]) value(sa[m,k/16]) value(qw[n,k]) value(sw[n,k/16]).
  *   a_codes      in: device [M, K/2] (from nvfp4_quantize_act)
  *   a_scales_mma in: device, nvfp4_scales_mma_bytes(M, K) bytes
@@ -178,9 +178,10 @@ nvfp4_status nvfp4_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma
                              cudaStream_t stream);
 
 /*
- * NVFP4 linear layer with M-based dispatch (same section: "M <= 48 uses W4A16,
- * M > 48 switches to W4A4; the runtime selects the lower-latency
- * implementation").  M <= crossover(N, K) runs nvfp4_gemm_w4a16; otherwise
+ * NVFP4 linear layer with M-based dispatch (same section: small token counts
+ * take W4A16, larger ones W4A4, the two latency curves crossing near M = 48
+ * on the pages' GPU, and the faster path is chosen per call).  M <=
+ * crossover(N, K) runs nvfp4_gemm_w4a16; otherwise
  * nvfp4_quantize_act (into the workspace) then nvfp4_gemm_w4a4.
  *   workspace  nvfp4_workspace_bytes(NVFP4_OP_LINEAR, M, N, K) bytes
  */

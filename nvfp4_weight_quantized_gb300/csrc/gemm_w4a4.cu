@@ -1,8 +1,8 @@
 // gemm_w4a4.cu -- NVFP4 x NVFP4 GEMM on the 5th-generation tensor cores.
 //
 // The large-M path of "SOAR 2026 Recap ...", section "1. Quantization and GEMM
-// dispatch": activations quantised online to NVFP4, then a GEMM that natively
-// issues the block-scaled FP4 MMA.  On sm_103a that instruction is
+// dispatch": activations quantised online to NVFP4, then a GEMM built on the
+// block-scaled FP4 tensor-core MMA itself.  On sm_103a that instruction is
 // tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X: E2M1 operands packed
 // two per byte, one UE4M3 scale per 16 elements along K, fp32 accumulation in
 // tensor memory (TMEM).

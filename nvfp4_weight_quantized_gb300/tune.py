@@ -1,7 +1,7 @@
 """Measure the W4A16 / W4A4 crossover of nvfp4_linear on the current GPU.
 
 The dispatch rule ("SOAR 2026 Recap ...", section "1. Quantization and GEMM
-dispatch") picks, per token count M, the lower-latency of the two GEMM paths;
+dispatch") picks, per token count M, whichever of the two GEMM paths is faster;
 the pages found the curves crossing near M = 48 on their GPU.  This module
 times both paths for one weight shape with CUDA graphs (many launches per
 replay, weights rotated so reads are cold) and returns the largest M for which
