@@ -73,9 +73,13 @@ def oracle_w4a4(a_codes, a_scales, a_ts, w_codes, w_scales, w_ts, m_rows=None, n
 
 
 def bf16_half_ulp(ref: np.ndarray) -> np.ndarray:
+    """Half a bf16 ulp at each reference value: 2^(e-8) for binary exponent
+    e, and 2^-134 in the subnormal range (below 2^-126 the spacing is fixed at
+    2^-133), also at zero."""
     a = np.abs(ref)
     e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
-    return np.where(a > 0, 2.0 ** (e - 8), 0.0)
+    e = np.where(a > 0, np.maximum(e, -126.0), -126.0)
+    return 2.0 ** (e - 8)
 
 
 def gemm_errors(y: np.ndarray, ref: np.ndarray, bf16: bool):

@@ -101,21 +101,70 @@ def test_w4a16_ragged(shape, M):
     run_w4a16(x, wref, K, nv.OUT_BF16)
 
 
-@pytest.mark.parametrize("M", [1, 8, 9, 17, 24, 31, 40, 48, 56, 64])
-def test_w4a16_both_kernels(M):
-    """The register-file kernel (every token-tile width it is built for) and
-    the tensor-memory kernel, forced in turn, both match the oracle."""
-    N, K = 328, 1344
-    wref = oracle_weight(synth.weight_normal(N, K, seed=77, outlier_frac=0.01))
-    x = synth.act_normal(M, K, seed=500 + M)
+def each_w4a16_kernel(fn):
+    """Runs fn() with each W4A16 kernel forced in turn: the register-file
+    decode kernel and the tensor-memory kernel."""
     saved = nv.nvfp4_get_w4a16_rf_max_m()
     try:
         for rf in (64, 0):
             nv.nvfp4_set_w4a16_rf_max_m(rf)
-            run_w4a16(x, wref, K, nv.OUT_F32)
-            run_w4a16(x, wref, K, nv.OUT_BF16)
+            fn()
     finally:
         nv.nvfp4_set_w4a16_rf_max_m(saved)
+
+
+@pytest.mark.parametrize("M", [1, 8, 9, 17, 24, 31, 40, 48, 56, 64])
+def test_w4a16_both_kernels(M):
+    """Every W4A16 kernel (the decode ones at every token-tile width they are
+    built for), forced in turn, matches the oracle."""
+    N, K = 328, 1344
+    wref = oracle_weight(synth.weight_normal(N, K, seed=77, outlier_frac=0.01))
+    x = synth.act_normal(M, K, seed=500 + M)
+
+    def check():
+        run_w4a16(x, wref, K, nv.OUT_F32)
+        run_w4a16(x, wref, K, nv.OUT_BF16)
+    each_w4a16_kernel(check)
+
+
+@pytest.mark.parametrize("shape", [(128, 256), (128, 64), (256, 4096), (1280, 2048), (200, 11008), (3000, 320)])
+@pytest.mark.parametrize("M", [1, 3, 16, 33])
+def test_w4a16_split_shapes(shape, M):
+    """K splits of every kind: one tile with one stage, one tile split over a
+    whole cluster, uneven splits, a ragged last stage, a ragged last tile,
+    many tiles."""
+    N, K = shape
+    wref = oracle_weight(synth.weight_normal(N, K, seed=N + 3 * K, outlier_frac=0.01))
+    x = synth.act_normal(M, K, seed=40 + M)
+    run_w4a16(x, wref, K, nv.OUT_F32)
+    assert nv.nvfp4_get_device_status() == 0
+
+
+@pytest.mark.parametrize("M", [8, 20])
+def test_w4a16_activation_range(M):
+    """Tokens spanning the whole bf16 range (tiny, subnormal, huge, zero, a
+    token whose magnitude jumps by 2^23 in a later K stage, one that shrinks)
+    match the oracle row by row: no kernel loses them to overflow, underflow
+    or a per-token power-of-two scaling of the activations."""
+    N, K = 328, 1344
+    wref = oracle_weight(synth.weight_normal(N, K, seed=78, outlier_frac=0.01))
+    rng = np.random.default_rng(600 + M)
+    x = rng.standard_normal((M, K))
+    x[0] *= 2.0 ** -120                       # tiny (bf16 normal range)
+    x[1] *= 2.0 ** 100                        # huge
+    x[2, :700] *= 1e-3                        # grows by ~2^23 after the first stages
+    x[2, 700:] *= 1e4
+    x[3] = 0.0                                # zero token
+    x[4, :300] *= 1e6                         # shrinks: later elements far below the maximum
+    x[4, 300:] *= 1e-2
+    x[5] *= 2.0 ** -130                       # bf16 subnormals only
+    x[6, 1000] = 1e36                         # one huge element in an ordinary token
+    bits = synth.f32_to_bf16_bits(x.astype(np.float32))
+
+    def check():
+        run_w4a16(bits, wref, K, nv.OUT_F32)
+        run_w4a16(bits, wref, K, nv.OUT_BF16)
+    each_w4a16_kernel(check)
 
 
 def test_w4a16_weight_prefetch_chain():
