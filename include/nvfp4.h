@@ -39,7 +39,7 @@
  *   - Pointers to tensors must be 16-byte aligned (NVFP4_ERR_ALIGN).
  *   - The library keeps no state between calls except the crossover table
  *     (nvfp4_set_crossover), the W4A16 kernel knob
- *     (nvfp4_set_w4a16_rf_max_m), the weight-prefetch flag
+ *     (nvfp4_set_w4a16_rf_max_m, nvfp4_set_w4a16_sk_max_m), the weight-prefetch flag
  *     (nvfp4_set_weight_prefetch) and the device status word.
  */
 #ifndef NVFP4_H_
@@ -152,10 +152,16 @@ nvfp4_status nvfp4_quantize_act(const void* X, int64_t M, int64_t K, float divis
  *   X      in:  device bf16 [M, K];  M >= 0 (M == 0 launches nothing)
  *   W      in:  quantised weight; K % 64 == 0
  *   Y      out: device [M, N] of out_dtype
- * Two kernels implement it: for M <= nvfp4_get_w4a16_rf_max_m() the weights
- * are dequantised in registers and multiplied with warp-level MMAs (decode
- * sizes), above that they are dequantised into tensor memory for tcgen05
- * MMAs.  Both give the same result up to fp32 summation order.
+ * Three kernels implement it.  For M <= nvfp4_get_w4a16_sk_max_m(): a
+ * persistent split-K kernel (one CTA per SM; clusters of up to 8 CTAs each
+ * own a run of 128-row weight tiles, CTA r of a cluster a K slice of every
+ * one, the slices of a tile summed through distributed shared memory) that
+ * keeps its K slice of X in shared memory as f16 scaled per token by a power
+ * of two and multiplies exactly dequantised f16 weights with warp-level MMAs.
+ * For M <= nvfp4_get_w4a16_rf_max_m(): one CTA per tile and K slice, bf16
+ * warp-level MMAs, the slices summed across a cluster.  Above that, weights
+ * dequantised into tensor memory for tcgen05 MMAs.  All give the same result
+ * up to fp32 summation order.  The workspace arguments are unused (NULL, 0).
  */
 nvfp4_status nvfp4_gemm_w4a16(const void* X, int64_t M, const nvfp4_weight* W, void* Y,
                               int out_dtype, void* workspace, size_t workspace_bytes,
@@ -230,6 +236,12 @@ int64_t nvfp4_get_crossover(int64_t N, int64_t K);
  * product.  Thread-safe; returns NVFP4_ERR_INVALID_ARG outside the range. */
 nvfp4_status nvfp4_set_w4a16_rf_max_m(int64_t M);
 int64_t nvfp4_get_w4a16_rf_max_m(void);
+
+/* Largest M that nvfp4_gemm_w4a16 sends to its persistent split-K kernel
+ * (0 ..= 64; default 8).  A tuning knob: every kernel computes the same
+ * product.  Thread-safe; returns NVFP4_ERR_INVALID_ARG outside the range. */
+nvfp4_status nvfp4_set_w4a16_sk_max_m(int64_t M);
+int64_t nvfp4_get_w4a16_sk_max_m(void);
 
 /* Weight prefetch (default off).  When on, the W4A16 kernels start reading
  * the weight codes and scales before the previous kernel in the stream has

@@ -23,7 +23,8 @@ __all__ = [
     "NVFP4Error", "NVFP4Weight", "NVFP4Act", "lib", "library_path", "declared_functions",
     "nvfp4_scales_mma_bytes", "nvfp4_workspace_bytes", "nvfp4_quantize_fos", "nvfp4_quantize_act",
     "nvfp4_gemm_w4a16", "nvfp4_gemm_w4a4", "nvfp4_linear", "nvfp4_linear_noalloc", "nvfp4_set_crossover",
-    "nvfp4_get_crossover", "nvfp4_set_w4a16_rf_max_m", "nvfp4_get_w4a16_rf_max_m", "nvfp4_set_weight_prefetch",
+    "nvfp4_get_crossover", "nvfp4_set_w4a16_rf_max_m", "nvfp4_get_w4a16_rf_max_m",
+    "nvfp4_set_w4a16_sk_max_m", "nvfp4_get_w4a16_sk_max_m", "nvfp4_set_weight_prefetch",
     "nvfp4_get_weight_prefetch", "nvfp4_get_device_status",
     "nvfp4_status_string",
 ]
@@ -78,6 +79,8 @@ def lib() -> ctypes.CDLL:
             "nvfp4_get_crossover": (i64, [i64, i64]),
             "nvfp4_set_w4a16_rf_max_m": (st, [i64]),
             "nvfp4_get_w4a16_rf_max_m": (i64, []),
+            "nvfp4_set_w4a16_sk_max_m": (st, [i64]),
+            "nvfp4_get_w4a16_sk_max_m": (i64, []),
             "nvfp4_set_weight_prefetch": (st, [ctypes.c_int]),
             "nvfp4_get_weight_prefetch": (ctypes.c_int, []),
             "nvfp4_get_device_status": (st, [vp]),
@@ -147,6 +150,15 @@ def nvfp4_set_w4a16_rf_max_m(m: int) -> None:
 
 def nvfp4_get_w4a16_rf_max_m() -> int:
     return lib().nvfp4_get_w4a16_rf_max_m()
+
+
+def nvfp4_set_w4a16_sk_max_m(m: int) -> None:
+    """Largest M that nvfp4_gemm_w4a16 sends to its persistent split-K kernel."""
+    _check(lib().nvfp4_set_w4a16_sk_max_m(m), "nvfp4_set_w4a16_sk_max_m")
+
+
+def nvfp4_get_w4a16_sk_max_m() -> int:
+    return lib().nvfp4_get_w4a16_sk_max_m()
 
 
 def nvfp4_set_weight_prefetch(enable: bool) -> None:

@@ -31,6 +31,8 @@ std::map<std::pair<int64_t, int64_t>, int64_t> g_crossover = {
 int64_t g_default_crossover = 48;
 // Largest M that nvfp4_gemm_w4a16 sends to the register-file kernel.
 std::atomic<int64_t> g_w4a16_rf_max_m{64};
+// Largest M that nvfp4_gemm_w4a16 sends to the persistent split-K kernel.
+std::atomic<int64_t> g_w4a16_sk_max_m{8};
 // Whether GEMM kernels may read the weights before the previous kernel in the
 // stream has finished (nvfp4_set_weight_prefetch).
 std::atomic<bool> g_weight_prefetch{false};
@@ -200,13 +202,23 @@ nvfp4_status nvfp4_gemm_w4a16(const void* X, int64_t M, const nvfp4_weight* W, v
   if (!aligned(X, 16) || !aligned(Y, 16)) return fail(NVFP4_ERR_ALIGN, "X and Y must be 16-byte aligned");
   const DeviceInfo* d = nullptr;
   if ((st = device_info(&d)) != NVFP4_OK) return st;
-  const bool rf = M <= g_w4a16_rf_max_m.load(std::memory_order_relaxed);
-  cudaError_t err =
-      rf ? nvfp4::launch_gemm_w4a16_rf(X, M, W->codes, W->scales_mma, W->tensor_scale, W->N, W->K, Y,
-                                       out_dtype == NVFP4_OUT_F32, g_weight_prefetch.load(std::memory_order_relaxed),
-                                       d->status, d->num_sms, stream)
-         : nvfp4::launch_gemm_w4a16(X, M, W->codes, W->scales_mma, W->tensor_scale, W->N, W->K, Y,
-                                    out_dtype == NVFP4_OUT_F32, d->status, d->num_sms, stream);
+  const bool f32 = out_dtype == NVFP4_OUT_F32, pf = g_weight_prefetch.load(std::memory_order_relaxed);
+  const int64_t sk_max = g_w4a16_sk_max_m.load(std::memory_order_relaxed);
+  const int64_t rf_max = g_w4a16_rf_max_m.load(std::memory_order_relaxed);
+  cudaError_t err = cudaErrorNotSupported;
+  if (M <= sk_max)
+    err = nvfp4::launch_gemm_w4a16_sk(X, M, W->codes, W->scales_mma, W->tensor_scale, W->N, W->K, Y, f32, pf,
+                                      d->status, d->num_sms, stream);
+  if (err == cudaErrorNotSupported) {
+    // the split-K kernel declines shapes whose activation slice does not fit
+    // in shared memory: the cluster split kernel takes those
+    if (M <= rf_max || M <= sk_max)
+      err = nvfp4::launch_gemm_w4a16_rf(X, M, W->codes, W->scales_mma, W->tensor_scale, W->N, W->K, Y, f32, pf,
+                                        d->status, d->num_sms, stream);
+    else
+      err = nvfp4::launch_gemm_w4a16(X, M, W->codes, W->scales_mma, W->tensor_scale, W->N, W->K, Y, f32,
+                                     d->status, d->num_sms, stream);
+  }
   if (err == cudaErrorNotSupported) return fail(NVFP4_ERR_UNSUPPORTED, "gemm_w4a16: unsupported size");
   if (err != cudaSuccess) return fail_cuda(err, "gemm_w4a16 launch");
   return NVFP4_OK;
@@ -273,6 +285,14 @@ nvfp4_status nvfp4_set_w4a16_rf_max_m(int64_t M) {
 }
 
 int64_t nvfp4_get_w4a16_rf_max_m(void) { return g_w4a16_rf_max_m.load(std::memory_order_relaxed); }
+
+nvfp4_status nvfp4_set_w4a16_sk_max_m(int64_t M) {
+  if (M < 0 || M > nvfp4::w4a16_sk_max_tokens()) return fail(NVFP4_ERR_INVALID_ARG, "w4a16 sk max M out of range");
+  g_w4a16_sk_max_m.store(M, std::memory_order_relaxed);
+  return NVFP4_OK;
+}
+
+int64_t nvfp4_get_w4a16_sk_max_m(void) { return g_w4a16_sk_max_m.load(std::memory_order_relaxed); }
 
 nvfp4_status nvfp4_set_weight_prefetch(int enable) {
   g_weight_prefetch.store(enable != 0, std::memory_order_relaxed);

@@ -36,6 +36,14 @@ cudaError_t launch_gemm_w4a16_rf(const void* x, int64_t M, const uint8_t* codes,
                                  void* y, bool out_f32, bool prefetch_w, unsigned int* status,
                                  int num_sms, cudaStream_t stream);
 
+// The same for M <= w4a16_sk_max_tokens() as a persistent split-K kernel
+// with the activations resident in shared memory (f16 MMAs).
+int w4a16_sk_max_tokens();
+cudaError_t launch_gemm_w4a16_sk(const void* x, int64_t M, const uint8_t* codes,
+                                 const uint8_t* scales_mma, const float* ts, int64_t N, int64_t K,
+                                 void* y, bool out_f32, bool prefetch_w, unsigned int* status,
+                                 int num_sms, cudaStream_t stream);
+
 // W4A4: block-scaled FP4 tensor-core GEMM.
 cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma, const float* a_ts,
                              int64_t M, const uint8_t* w_codes, const uint8_t* w_scales_mma,

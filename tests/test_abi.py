@@ -65,6 +65,18 @@ def test_w4a16_kernel_knob(L):
     assert nv.nvfp4_get_w4a16_rf_max_m() == saved
 
 
+def test_w4a16_sk_knob(L):
+    saved = nv.nvfp4_get_w4a16_sk_max_m()
+    assert 0 <= saved <= 64
+    nv.nvfp4_set_w4a16_sk_max_m(0)
+    assert nv.nvfp4_get_w4a16_sk_max_m() == 0
+    for bad in (-1, 65):
+        with pytest.raises(nv.NVFP4Error):
+            nv.nvfp4_set_w4a16_sk_max_m(bad)
+    nv.nvfp4_set_w4a16_sk_max_m(saved)
+    assert nv.nvfp4_get_w4a16_sk_max_m() == saved
+
+
 def test_status_strings(L):
     for s in range(9):
         assert nv.nvfp4_status_string(s)

@@ -102,15 +102,17 @@ def test_w4a16_ragged(shape, M):
 
 
 def each_w4a16_kernel(fn):
-    """Runs fn() with each W4A16 kernel forced in turn: the register-file
-    decode kernel and the tensor-memory kernel."""
-    saved = nv.nvfp4_get_w4a16_rf_max_m()
+    """Runs fn() with each W4A16 kernel forced in turn: the persistent
+    split-K kernel, the cluster split kernel and the tensor-memory kernel."""
+    saved = (nv.nvfp4_get_w4a16_sk_max_m(), nv.nvfp4_get_w4a16_rf_max_m())
     try:
-        for rf in (64, 0):
+        for sk, rf in ((64, 64), (0, 64), (0, 0)):
+            nv.nvfp4_set_w4a16_sk_max_m(sk)
             nv.nvfp4_set_w4a16_rf_max_m(rf)
             fn()
     finally:
-        nv.nvfp4_set_w4a16_rf_max_m(saved)
+        nv.nvfp4_set_w4a16_sk_max_m(saved[0])
+        nv.nvfp4_set_w4a16_rf_max_m(saved[1])
 
 
 @pytest.mark.parametrize("M", [1, 8, 9, 17, 24, 31, 40, 48, 56, 64])
@@ -136,7 +138,7 @@ def test_w4a16_split_shapes(shape, M):
     N, K = shape
     wref = oracle_weight(synth.weight_normal(N, K, seed=N + 3 * K, outlier_frac=0.01))
     x = synth.act_normal(M, K, seed=40 + M)
-    run_w4a16(x, wref, K, nv.OUT_F32)
+    each_w4a16_kernel(lambda: run_w4a16(x, wref, K, nv.OUT_F32))
     assert nv.nvfp4_get_device_status() == 0
 
 
