@@ -201,7 +201,7 @@ template <int NT, bool kF32, int SPLIT = split_for(NT), typename Wp = Warps<SPLI
 __global__ void __launch_bounds__(Wp::kThreads, 1)
 w4a16_sk_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __nv_bfloat16* __restrict__ x,
                 const uint8_t* __restrict__ smma, const float* __restrict__ ts_ptr, int64_t M, int64_t N,
-                int64_t K, int stages, int sps, int tiles_n, int clusters, int max_tiles, int prefetch_w,
+                int64_t K, int stages, int sps, int tiles_n, int clusters, int log2_ks, int max_tiles, int prefetch_w,
                 void* __restrict__ y, unsigned int* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -214,8 +214,8 @@ w4a16_sk_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __nv_bfloa
   const uint32_t sbase = smem_addr(base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int ks = (int)(gridDim.x / (unsigned)clusters);
-  const int cid = (int)blockIdx.x / ks;
+  const int ks = 1 << log2_ks;
+  const int cid = (int)(blockIdx.x >> log2_ks);
   const int rank = (int)cluster_ctarank();
   const int nchunk = (int)(K / kChunkK);
   const int nstage = (nchunk + kChunksPerStage - 1) / kChunksPerStage;
@@ -234,8 +234,7 @@ w4a16_sk_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __nv_bfloa
     fence_mbar_init();
   }
   if (threadIdx.x < n_tok) tmax[threadIdx.x] = 0u;
-  __syncwarp();
-  cluster_sync_all();  // every CTA's barriers are initialised before peers arrive on them
+  __syncthreads();
 
   auto chunks_at = [&](int st) { return min(kChunksPerStage, nchunk - kChunksPerStage * st); };
   // unit i = (tile cid + (i / nst) * clusters, stage st_begin + i % nst), tracked
@@ -277,18 +276,35 @@ w4a16_sk_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __nv_bfloa
   for (int i = threadIdx.x; i < n_tok * 8; i += kThreads) tslot[i] = 0u;
   __syncthreads();
   const int my_tok = threadIdx.x / kTpt, my_sub = threadIdx.x - my_tok * kTpt;
-  const bool has_tok = my_tok < n_tok;
-  const uint4* my_row = reinterpret_cast<const uint4*>(x + (int64_t)(my_tok < m_valid ? my_tok : 0) * K + k0);
-  if (has_tok && my_tok < m_valid) {
+  const bool has_tok = my_tok < n_tok, loads = my_tok < m_valid;
+  const uint4* my_row = reinterpret_cast<const uint4*>(x + (int64_t)(loads ? my_tok : 0) * K + k0);
+  // up to kHold pieces per thread are read once and kept in registers; a
+  // longer slice is read twice
+  constexpr int kHold = 8;
+  const bool hold = upt <= kHold * kTpt;
+  uint4 hv[kHold];
+  if (has_tok && loads) {
     uint32_t mx = 0;
-    for (int u = my_sub; u < upt; u += 4 * kTpt) {
-      uint4 v[4];
+    if (hold) {
 #pragma unroll
-      for (int r = 0; r < 4; ++r) v[r] = u + r * kTpt < upt ? __ldg(my_row + u + r * kTpt) : make_uint4(0, 0, 0, 0);
+      for (int j = 0; j < kHold; ++j) {
+        const int u = my_sub + j * kTpt;
+        hv[j] = u < upt ? __ldg(my_row + u) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
-        mx = max_u16x2(mx, max_u16x2(max_u16x2(v[r].x & 0x7FFF7FFFu, v[r].y & 0x7FFF7FFFu),
-                                     max_u16x2(v[r].z & 0x7FFF7FFFu, v[r].w & 0x7FFF7FFFu)));
+      for (int j = 0; j < kHold; ++j)
+        mx = max_u16x2(mx, max_u16x2(max_u16x2(hv[j].x & 0x7FFF7FFFu, hv[j].y & 0x7FFF7FFFu),
+                                     max_u16x2(hv[j].z & 0x7FFF7FFFu, hv[j].w & 0x7FFF7FFFu)));
+    } else {
+      for (int u = my_sub; u < upt; u += 4 * kTpt) {
+        uint4 v[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) v[r] = u + r * kTpt < upt ? __ldg(my_row + u + r * kTpt) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          mx = max_u16x2(mx, max_u16x2(max_u16x2(v[r].x & 0x7FFF7FFFu, v[r].y & 0x7FFF7FFFu),
+                                       max_u16x2(v[r].z & 0x7FFF7FFFu, v[r].w & 0x7FFF7FFFu)));
+      }
     }
     mx = max(mx & 0xFFFFu, mx >> 16);
     if (mx != 0u) atomicMax(&tslot[my_tok * 8 + (my_sub & 7)], mx);
@@ -305,18 +321,26 @@ w4a16_sk_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __nv_bfloa
   if (has_tok) {
     const float c = exp2i(142 - (int)tmax[my_tok]);
     const uint32_t xrow = sbase + L.x_off + my_tok * 128;
-    for (int u = my_sub; u < upt; u += 4 * kTpt) {
-      uint4 v[4];
+    auto put = [&](int u, uint4 v) {
+      sts128(xrow + (u >> 3) * L.x_tile + (((u & 7) ^ (my_tok & 7)) << 4),
+             make_uint4(bf16x2_to_f16x2(v.x, c), bf16x2_to_f16x2(v.y, c), bf16x2_to_f16x2(v.z, c),
+                        bf16x2_to_f16x2(v.w, c)));
+    };
+    if (hold) {
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
-        v[r] = (my_tok < m_valid && u + r * kTpt < upt) ? __ldg(my_row + u + r * kTpt) : make_uint4(0, 0, 0, 0);
+      for (int j = 0; j < kHold; ++j) {
+        const int u = my_sub + j * kTpt;
+        if (u < upt) put(u, loads ? hv[j] : make_uint4(0, 0, 0, 0));
+      }
+    } else {
+      for (int u = my_sub; u < upt; u += 4 * kTpt) {
+        uint4 v[4];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int uu = u + r * kTpt;
-        if (uu < upt)
-          sts128(xrow + (uu >> 3) * L.x_tile + (((uu & 7) ^ (my_tok & 7)) << 4),
-                 make_uint4(bf16x2_to_f16x2(v[r].x, c), bf16x2_to_f16x2(v[r].y, c), bf16x2_to_f16x2(v[r].z, c),
-                            bf16x2_to_f16x2(v[r].w, c)));
+        for (int r = 0; r < 4; ++r)
+          v[r] = (loads && u + r * kTpt < upt) ? __ldg(my_row + u + r * kTpt) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          if (u + r * kTpt < upt) put(u + r * kTpt, v[r]);
       }
     }
   }
@@ -459,7 +483,7 @@ w4a16_sk_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __nv_bfloa
   // The next kernel in the stream may start its prologue now (it waits for
   // this grid to finish before it touches data).
   griddep_launch_dependents();
-  cluster_sync_all();  // every partial tile of the cluster is in
+  cluster_sync_all();  // every partial tile of the cluster is in (and every peer is running)
   // ---- rows [rank * 128 / ks, (rank + 1) * 128 / ks) of every tile: the ks
   // slices summed in rank order, stored ----
   {
@@ -652,9 +676,11 @@ cudaError_t launch_gemm_w4a16_sk(const void* x, int64_t M, const uint8_t* codes,
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   int pf = prefetch_w ? 1 : 0, tn = (int)tiles_n, sps = best_sps, cl = best_cl, mt = max_tiles;
-  void* args[] = {(void*)&mc, (void*)&x,  (void*)&scales_mma, (void*)&ts, (void*)&M,  (void*)&N,
-                  (void*)&K,  (void*)&stages, (void*)&sps,    (void*)&tn, (void*)&cl, (void*)&mt,
-                  (void*)&pf, (void*)&y,  (void*)&status};
+  int lks = 0;
+  while ((1 << lks) < best_ks) ++lks;
+  void* args[] = {(void*)&mc, (void*)&x,      (void*)&scales_mma, (void*)&ts, (void*)&M,   (void*)&N,
+                  (void*)&K,  (void*)&stages, (void*)&sps,        (void*)&tn, (void*)&cl,  (void*)&lks,
+                  (void*)&mt, (void*)&pf,     (void*)&y,          (void*)&status};
   return cudaLaunchKernelExC(&cfg, kern, args);
 }
 
