@@ -125,9 +125,10 @@ class ClockSampler:
 
 # --------------------------------------------------------------- our arm ---
 
-def traffic_from_profiles(kernel_key: str, src_file: str):
+def traffic_from_profiles(kernel_key: str, src_files: dict):
     """DRAM bytes per launch of `kernel_key` from the committed ncu summary, or
-    None when the summary is missing or was taken on a different source."""
+    None when the summary is missing or was taken on a different source: the
+    summary holds source_sha_<tag> for every {tag: source file} given."""
     path = os.path.join(ROOT, "profiles", f"{kernel_key}.traffic.txt")
     try:
         kv = {}
@@ -136,10 +137,11 @@ def traffic_from_profiles(kernel_key: str, src_file: str):
                 if "=" in line and not line.startswith("#"):
                     k, v = line.strip().split("=", 1)
                     kv[k.strip()] = v.strip()
-        with open(src_file, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
-        if kv.get("source_sha") != sha:
-            return None
+        for tag, src_file in src_files.items():
+            with open(src_file, "rb") as f:
+                sha = hashlib.sha256(f.read()).hexdigest()[:16]
+            if kv.get(f"source_sha_{tag}") != sha:
+                return None
         return float(kv["dram_bytes_per_launch"])
     except Exception:
         return None
@@ -282,18 +284,19 @@ def run_ours(args):
     w16_time = sum(lin_avg[M] for M in DECODE_M if paths[M] == "w4a16")
     w16_bytes = sum(w4a16_bytes(M, N, K) for M in DECODE_M if paths[M] == "w4a16")
     if w16_time >= q_avg and w16_time > 0:
-        dom = "gemm_w4a16 (w4a16_rf_kernel)"
+        dom = "gemm_w4a16 (w4a16_sk_kernel for M <= 8, w4a16_rf_kernel above)"
         achieved = w16_bytes / w16_time / 1e9
-        traffic = traffic_from_profiles("w4a16_decode", os.path.join(ROOT, "nvfp4_weight_quantized_gb300",
-                                                                     "csrc", "gemm_w4a16_rf.cu"))
+        csrc = os.path.join(ROOT, "nvfp4_weight_quantized_gb300", "csrc")
+        traffic = traffic_from_profiles("w4a16_decode", {"sk": os.path.join(csrc, "gemm_w4a16_sk.cu"),
+                                                         "rf": os.path.join(csrc, "gemm_w4a16_rf.cu")})
         launches = sum(1 for M in DECODE_M if paths[M] == "w4a16")
         if traffic is not None:
             traffic = traffic  # bytes per launch averaged over the M sweep
     else:
         dom = "quantize_fos"
         achieved = q_bytes(N, K) / q_avg / 1e9
-        traffic = traffic_from_profiles("quantize_fos_decode", os.path.join(
-            ROOT, "nvfp4_weight_quantized_gb300", "csrc", "quant.cu"))
+        traffic = traffic_from_profiles("quantize_fos_decode", {"quant": os.path.join(
+            ROOT, "nvfp4_weight_quantized_gb300", "csrc", "quant.cu")})
         launches = 2
 
     detail = {
