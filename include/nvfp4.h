@@ -152,7 +152,7 @@ nvfp4_status nvfp4_quantize_act(const void* X, int64_t M, int64_t K, float divis
  *   X      in:  device bf16 [M, K];  M >= 0 (M == 0 launches nothing)
  *   W      in:  quantised weight; K % 64 == 0
  *   Y      out: device [M, N] of out_dtype
- * Three kernels implement it.  For M <= nvfp4_get_w4a16_sk_max_m(): a
+ * Three kernels implement it.  For small M (see nvfp4_set_w4a16_sk_max_m): a
  * persistent split-K kernel (one CTA per SM; clusters of up to 8 CTAs each
  * own a run of 128-row weight tiles, CTA r of a cluster a K slice of every
  * one, the slices of a tile summed through distributed shared memory) that
@@ -237,9 +237,11 @@ int64_t nvfp4_get_crossover(int64_t N, int64_t K);
 nvfp4_status nvfp4_set_w4a16_rf_max_m(int64_t M);
 int64_t nvfp4_get_w4a16_rf_max_m(void);
 
-/* Largest M that nvfp4_gemm_w4a16 sends to its persistent split-K kernel
- * (0 ..= 64; default 8).  A tuning knob: every kernel computes the same
- * product.  Thread-safe; returns NVFP4_ERR_INVALID_ARG outside the range. */
+/* Which M nvfp4_gemm_w4a16 sends to its persistent split-K kernel: M <= the
+ * value (0 ..= 64), or, for -1 (the default), by the rule measured on GB300:
+ * M <= 8, and M <= 16 / M <= 32 on weights of at least 64 / 128 row tiles of
+ * 128.  A tuning knob: every kernel computes the same product.  Thread-safe;
+ * returns NVFP4_ERR_INVALID_ARG outside -1 ..= 64. */
 nvfp4_status nvfp4_set_w4a16_sk_max_m(int64_t M);
 int64_t nvfp4_get_w4a16_sk_max_m(void);
 

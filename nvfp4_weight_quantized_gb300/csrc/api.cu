@@ -31,8 +31,9 @@ std::map<std::pair<int64_t, int64_t>, int64_t> g_crossover = {
 int64_t g_default_crossover = 48;
 // Largest M that nvfp4_gemm_w4a16 sends to the register-file kernel.
 std::atomic<int64_t> g_w4a16_rf_max_m{64};
-// Largest M that nvfp4_gemm_w4a16 sends to the persistent split-K kernel.
-std::atomic<int64_t> g_w4a16_sk_max_m{8};
+// Largest M that nvfp4_gemm_w4a16 sends to the persistent split-K kernel, or
+// -1: by the measured rule in nvfp4_gemm_w4a16.
+std::atomic<int64_t> g_w4a16_sk_max_m{-1};
 // Whether GEMM kernels may read the weights before the previous kernel in the
 // stream has finished (nvfp4_set_weight_prefetch).
 std::atomic<bool> g_weight_prefetch{false};
@@ -206,13 +207,18 @@ nvfp4_status nvfp4_gemm_w4a16(const void* X, int64_t M, const nvfp4_weight* W, v
   const int64_t sk_max = g_w4a16_sk_max_m.load(std::memory_order_relaxed);
   const int64_t rf_max = g_w4a16_rf_max_m.load(std::memory_order_relaxed);
   cudaError_t err = cudaErrorNotSupported;
-  if (M <= sk_max)
+  // by default split-K up to 8 tokens, and up to 16 / 32 on weights of at
+  // least 64 / 128 row tiles, where it measured faster than the cluster split
+  // kernel on GB300
+  const int64_t tiles = (W->N + 127) / 128;
+  const bool sk = sk_max < 0 ? (M <= 8 || (M <= 16 && tiles >= 64) || (M <= 32 && tiles >= 128)) : M <= sk_max;
+  if (sk)
     err = nvfp4::launch_gemm_w4a16_sk(X, M, W->codes, W->scales_mma, W->tensor_scale, W->N, W->K, Y, f32, pf,
                                       d->status, d->num_sms, stream);
   if (err == cudaErrorNotSupported) {
     // the split-K kernel declines shapes whose activation slice does not fit
     // in shared memory: the cluster split kernel takes those
-    if (M <= rf_max || M <= sk_max)
+    if (M <= rf_max || sk)
       err = nvfp4::launch_gemm_w4a16_rf(X, M, W->codes, W->scales_mma, W->tensor_scale, W->N, W->K, Y, f32, pf,
                                         d->status, d->num_sms, stream);
     else
@@ -287,7 +293,7 @@ nvfp4_status nvfp4_set_w4a16_rf_max_m(int64_t M) {
 int64_t nvfp4_get_w4a16_rf_max_m(void) { return g_w4a16_rf_max_m.load(std::memory_order_relaxed); }
 
 nvfp4_status nvfp4_set_w4a16_sk_max_m(int64_t M) {
-  if (M < 0 || M > nvfp4::w4a16_sk_max_tokens()) return fail(NVFP4_ERR_INVALID_ARG, "w4a16 sk max M out of range");
+  if (M < -1 || M > nvfp4::w4a16_sk_max_tokens()) return fail(NVFP4_ERR_INVALID_ARG, "w4a16 sk max M out of range");
   g_w4a16_sk_max_m.store(M, std::memory_order_relaxed);
   return NVFP4_OK;
 }

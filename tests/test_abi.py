@@ -67,10 +67,11 @@ def test_w4a16_kernel_knob(L):
 
 def test_w4a16_sk_knob(L):
     saved = nv.nvfp4_get_w4a16_sk_max_m()
-    assert 0 <= saved <= 64
-    nv.nvfp4_set_w4a16_sk_max_m(0)
-    assert nv.nvfp4_get_w4a16_sk_max_m() == 0
-    for bad in (-1, 65):
+    assert -1 <= saved <= 64
+    for v in (0, 64, -1):
+        nv.nvfp4_set_w4a16_sk_max_m(v)
+        assert nv.nvfp4_get_w4a16_sk_max_m() == v
+    for bad in (-2, 65):
         with pytest.raises(nv.NVFP4Error):
             nv.nvfp4_set_w4a16_sk_max_m(bad)
     nv.nvfp4_set_w4a16_sk_max_m(saved)
