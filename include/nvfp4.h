@@ -39,7 +39,8 @@
  *   - Pointers to tensors must be 16-byte aligned (NVFP4_ERR_ALIGN).
  *   - The library keeps no state between calls except the crossover table
  *     (nvfp4_set_crossover), the W4A16 kernel knob
- *     (nvfp4_set_w4a16_rf_max_m, nvfp4_set_w4a16_sk_max_m), the weight-prefetch flag
+ *     (nvfp4_set_w4a16_rf_max_m, nvfp4_set_w4a16_sk_max_m), the W4A4 kernel
+ *     knob (nvfp4_set_w4a4_pair), the weight-prefetch flag
  *     (nvfp4_set_weight_prefetch) and the device status word.
  */
 #ifndef NVFP4_H_
@@ -254,6 +255,14 @@ int64_t nvfp4_get_w4a16_sk_max_m(void);
  * quantised once and then only read, as in inference.  Thread-safe. */
 nvfp4_status nvfp4_set_weight_prefetch(int enable);
 int nvfp4_get_weight_prefetch(void);
+
+/* W4A4 kernel for M > 128 (default on).  On: pairs of CTAs in a cluster share
+ * each 256 x 256 output tile through cta_group::2 MMAs (each CTA stages half
+ * of the A rows and half of the B rows of every K stage); off: one CTA per
+ * 128 x 256 tile.  Both compute the same product with the same fp32
+ * accumulation order per output.  A tuning knob; thread-safe. */
+nvfp4_status nvfp4_set_w4a4_pair(int enable);
+int nvfp4_get_w4a4_pair(void);
 
 /* Synchronises `stream`, then returns and clears the device status word of the
  * current device: NVFP4_OK, NVFP4_ERR_NONFINITE or NVFP4_ERR_TIMEOUT. */

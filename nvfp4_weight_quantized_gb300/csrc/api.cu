@@ -300,6 +300,13 @@ nvfp4_status nvfp4_set_w4a16_sk_max_m(int64_t M) {
 
 int64_t nvfp4_get_w4a16_sk_max_m(void) { return g_w4a16_sk_max_m.load(std::memory_order_relaxed); }
 
+nvfp4_status nvfp4_set_w4a4_pair(int enable) {
+  nvfp4::w4a4_set_pair(enable != 0);
+  return NVFP4_OK;
+}
+
+int nvfp4_get_w4a4_pair(void) { return nvfp4::w4a4_get_pair() ? 1 : 0; }
+
 nvfp4_status nvfp4_set_weight_prefetch(int enable) {
   g_weight_prefetch.store(enable != 0, std::memory_order_relaxed);
   return NVFP4_OK;

@@ -25,6 +25,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -102,6 +103,15 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
   uint32_t d;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
   return d;
+}
+
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -304,6 +314,7 @@ w4a4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     }
   } else {
     // ---------------- epilogue (warps 0-3; TMEM lanes 32w..32w+31 = tile rows) ----------------
+    griddep_wait();  // the tensor scales may come from the previous kernel in the stream
     const float alpha = __fmul_rn(*a_ts, *b_ts);
     const bool vec_ok = kF32 ? (N % 4 == 0) : (N % 8 == 0);
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
@@ -404,6 +415,310 @@ w4a4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   }
 }
 
+// ---------------------------------------------------------------------------
+// Pair kernel: the same GEMM with 256 x 256 output tiles, each computed by the
+// two CTAs of a cluster with cta_group::2 MMAs (M = 256, N = 256, K = 64).
+// CTA r of the pair stages A rows [m0 + 128 r, +128) and B rows
+// [n0 + 128 r, +128) of every K stage in its own shared memory, so a CTA
+// streams half the operand bytes of the single-CTA 128 x 256 tile for the same
+// MMA work, and the MMA reads each operand byte from shared memory once.  Each
+// CTA holds the A scales of its rows and the B scales of all 256 tile rows in
+// its own TMEM (same columns in both), and its 128 x 256 fp32 accumulator.
+//
+//   producer (warp 8, each CTA): TMA of its A and B halves and the scale
+//     tiles into its shared memory, signalled on its own full[s];
+//   scale loaders (warps 4-7, each CTA): full[s] -> TMEM -> arrive on the
+//     even CTA's sf_full[s] (8 arrivals: the stage is ready in both CTAs);
+//   MMA issuer (warp 9 of the even CTA): four pair MMAs per stage, then one
+//     commit that arrives on empty[s] of both CTAs; acc_full likewise;
+//   epilogue (warps 0-3, each CTA): drains its accumulator lanes, then
+//     arrives on the even CTA's acc_free (8 arrivals).
+constexpr int kPairStages = 5;
+
+struct __align__(1024) PairSmem {
+  uint8_t ystage[2 * BM * 128];          // two 128 x 64 bf16 output boxes
+  uint8_t a[kPairStages][kABytes];       // this CTA's 128 A rows x 256 K
+  uint8_t b[kPairStages][kABytes];       // this CTA's 128 B rows x 256 K
+  uint8_t sfa[kPairStages][kSfaBytes];   // A scales of this CTA's rows
+  uint8_t sfb[kPairStages][2 * kSfaBytes];  // B scales of both 128-row halves
+  uint64_t full[kPairStages];     // this CTA's loads landed
+  uint64_t sf_full[kPairStages];  // even CTA: scales in TMEM in both CTAs
+  uint64_t empty[kPairStages];    // MMAs of the stage done (from the even CTA)
+  uint64_t acc_full;              // tile accumulated (from the even CTA)
+  uint64_t acc_free;              // even CTA: both accumulators drained
+  uint32_t tmem_base;
+};
+
+constexpr uint32_t kPairSfCol = 256;                  // after the 256 accumulator columns
+constexpr uint32_t kPairSfStageCols = 16 + 32;        // A: 4 MMAs x 4; B: 4 MMAs x 2 halves x 4
+static_assert(kPairSfCol + kPairStages * kPairSfStageCols <= kTmemCols, "TMEM budget");
+// kind::mxf4nvf4, E2M1 x E2M1, K-major, N = 256, UE4M3 scales, M = 256
+constexpr uint32_t kPairIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(256 >> 3) << 17) | (2u << 27);
+
+template <bool kF32>
+__global__ void __launch_bounds__(kThreads, 1)
+w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                 const __grid_constant__ CUtensorMap tmap_y, int tma_store, const uint8_t* __restrict__ a_smma,
+                 const uint8_t* __restrict__ b_smma, const float* __restrict__ a_ts,
+                 const float* __restrict__ b_ts, int64_t M, int64_t N, int64_t K, void* __restrict__ y,
+                 unsigned int* __restrict__ status) {
+  constexpr int S = kPairStages;
+  extern __shared__ uint8_t smem_raw[];
+  PairSmem& sm = *reinterpret_cast<PairSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int kb64 = (int)(K / 64);
+  const int kt = (kb64 + 3) / 4;
+  const int64_t b_row_tiles = (N + 127) / 128;
+  const int64_t n_tiles = (N + 255) / 256;
+  const int64_t n_work = ((M + 255) / 256) * n_tiles;
+
+  if (warp == kProducerWarp && lane == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.sf_full[s], 2 * kSfWarps);
+      mbar_init(&sm.empty[s], 1);
+    }
+    mbar_init(&sm.acc_full, 1);
+    mbar_init(&sm.acc_free, 2 * kEpiWarps);
+    fence_mbar_init();
+    prefetch_tmap(&tmap_a);
+    prefetch_tmap(&tmap_b);
+  }
+  if (warp == 0) tmem_alloc_pair(&sm.tmem_base, kTmemCols);
+  fence_before_sync();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any cross-CTA arrive
+  fence_after_sync();
+  const uint32_t tmem = sm.tmem_base;
+  bool failed = false;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      // ---------------- producer (each CTA) ----------------
+      griddep_wait();
+      int g = 0;
+      for (int64_t w = pair; w < n_work && !failed; w += npairs) {
+        const int64_t m_tile = w / n_tiles, n_tile = w - m_tile * n_tiles;
+        const int64_t arow = m_tile * 256 + 128 * rank;
+        const int64_t n0 = n_tile * 256;
+        const int64_t brow = n0 + 128 * rank;
+        // a CTA whose A (or B) rows all lie past M (N) loads nothing for them:
+        // its accumulator rows (or the tile's columns from that half) are never stored
+        const bool has_a = arow < M, has_b = brow < N;
+        const int64_t sfb_left = b_row_tiles - n0 / 128;
+        const int nsfb = sfb_left < 2 ? (int)sfb_left : 2;
+        for (int ks = 0; ks < kt; ++ks, ++g) {
+          const int s = g % S;
+          if (g >= S && !mbar_wait(&sm.empty[s], (uint32_t)(g / S - 1) & 1u)) {
+            failed = true;
+            break;
+          }
+          const int kk_n = min(4, kb64 - 4 * ks);
+          const uint32_t sf_bytes = (uint32_t)kk_n * kScaleTileBytes;
+          mbar_arrive_expect_tx(&sm.full[s], (has_a ? kABytes + sf_bytes : 0) + (has_b ? kABytes : 0) +
+                                                 sf_bytes * nsfb);
+          if (has_a) tma_load_2d(sm.a[s], &tmap_a, ks * (BK / 2), (int)arow, &sm.full[s]);
+          if (has_b) tma_load_2d(sm.b[s], &tmap_b, ks * (BK / 2), (int)brow, &sm.full[s]);
+          if (has_a)
+            bulk_load(sm.sfa[s], a_smma + ((arow / 128) * kb64 + 4 * ks) * kScaleTileBytes, sf_bytes, &sm.full[s]);
+          for (int rt = 0; rt < nsfb; ++rt)
+            bulk_load(sm.sfb[s] + rt * kSfaBytes, b_smma + ((n0 / 128 + rt) * kb64 + 4 * ks) * kScaleTileBytes,
+                      sf_bytes, &sm.full[s]);
+        }
+      }
+      griddep_launch_dependents();
+      // before the CTA may exit: this CTA's loads have landed and the pair's
+      // MMAs that read them have completed
+      for (int i = max(0, g - S); i < g && !failed; ++i)
+        if (!mbar_wait(&sm.full[i % S], (uint32_t)(i / S) & 1u) ||
+            !mbar_wait(&sm.empty[i % S], (uint32_t)(i / S) & 1u))
+          failed = true;
+      if (failed) atomicOr(status, kStatusTimeout);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (even CTA) ----------------
+      int g = 0, t = 0;
+      for (int64_t w = pair; w < n_work && !failed; w += npairs, ++t) {
+        if (t > 0 && !mbar_wait(&sm.acc_free, (uint32_t)(t - 1) & 1u)) {
+          failed = true;
+          break;
+        }
+        fence_after_sync();
+        for (int ks = 0; ks < kt; ++ks, ++g) {
+          const int s = g % S;
+          if (!mbar_wait(&sm.sf_full[s], (uint32_t)(g / S) & 1u)) {
+            failed = true;
+            break;
+          }
+          fence_after_sync();
+          const int kk_n = min(4, kb64 - 4 * ks);
+          const uint32_t sfa_t = tmem + kPairSfCol + kPairSfStageCols * s;
+          const uint32_t sfb_t = sfa_t + 16;
+          const uint64_t adesc = smem_desc(smem_addr(sm.a[s]), 0, 1024, 2);
+          const uint64_t bdesc = smem_desc(smem_addr(sm.b[s]), 0, 1024, 2);
+          for (int kk = 0; kk < kk_n; ++kk)
+            mma_mxf4nvf4_pair(tmem, adesc + 2ull * kk, bdesc + 2ull * kk, kPairIdesc, sfa_t + 4 * kk,
+                              sfb_t + 8 * kk, (ks | kk) != 0);
+          commit_pair(&sm.empty[s]);
+        }
+        if (!failed) commit_pair(&sm.acc_full);
+      }
+      if (failed) atomicOr(status, kStatusTimeout);
+    }
+  } else if (warp >= kEpiWarps) {
+    // ---------------- scale loaders (each CTA): shared memory -> TMEM ----------------
+    // atom kk of A at column 4 kk; atom (kk, half rt) of B at 16 + 4 (2 kk + rt)
+    const uint32_t lane_base = (uint32_t)((warp - kEpiWarps) * 32) << 16;
+    int g = 0;
+    for (int64_t w = pair; w < n_work && !failed; w += npairs) {
+      for (int ks = 0; ks < kt; ++ks, ++g) {
+        const int s = g % S;
+        if (!mbar_wait(&sm.full[s], (uint32_t)(g / S) & 1u) ||
+            (g >= S && !mbar_wait(&sm.empty[s], (uint32_t)(g / S - 1) & 1u))) {
+          failed = true;
+          break;
+        }
+        const uint32_t col = tmem + lane_base + kPairSfCol + kPairSfStageCols * s;
+        uint32_t r[16];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint4 v = *reinterpret_cast<const uint4*>(sm.sfa[s] + kk * kScaleTileBytes + lane * 16);
+          r[4 * kk] = v.x;
+          r[4 * kk + 1] = v.y;
+          r[4 * kk + 2] = v.z;
+          r[4 * kk + 3] = v.w;
+        }
+        tmem_st_x16(col, r);
+#pragma unroll
+        for (int h = 0; h < 8; h += 4) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int idx = h + q;  // = 2 kk + rt
+            const int kk = idx >> 1, rt = idx & 1;
+            const uint4 v =
+                *reinterpret_cast<const uint4*>(sm.sfb[s] + rt * kSfaBytes + kk * kScaleTileBytes + lane * 16);
+            r[4 * q] = v.x;
+            r[4 * q + 1] = v.y;
+            r[4 * q + 2] = v.z;
+            r[4 * q + 3] = v.w;
+          }
+          tmem_st_x16(col + 16 + 4 * h, r);
+        }
+        tmem_wait_st();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(&sm.sf_full[s], 0);
+      }
+    }
+    if (failed && lane == 0) atomicOr(status, kStatusTimeout);
+  } else {
+    // ---------------- epilogue (each CTA; TMEM lane = tile row) ----------------
+    griddep_wait();  // the tensor scales may come from the previous kernel in the stream
+    const float alpha = __fmul_rn(*a_ts, *b_ts);
+    const bool vec_ok = kF32 ? (N % 4 == 0) : (N % 8 == 0);
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int r = warp * 32 + lane;
+    int t = 0;
+    for (int64_t w = pair; w < n_work; w += npairs, ++t) {
+      const int64_t m_tile = w / n_tiles, n_tile = w - m_tile * n_tiles;
+      const int64_t m0 = m_tile * 256 + 128 * rank, n0 = n_tile * 256;
+      const int64_t row = m0 + r;
+      const bool ok = __all_sync(0xffffffffu, !failed && mbar_wait(&sm.acc_full, (uint32_t)t & 1u));
+      if (!ok) {
+        failed = true;
+        break;
+      }
+      fence_after_sync();
+      if (!kF32 && tma_store) {
+        // Columns 0-127 go straight to the staging buffer (two 128 x 64 bf16
+        // boxes, 128-byte swizzle), columns 128-255 into registers as scaled
+        // bf16 pairs; then the accumulator goes back to the MMA warp and the
+        // TMA stores (which clip rows past M) overlap the next tile's MMAs.
+        if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");  // staging buffer free
+        uint32_t hi[8][8];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {  // 16 columns per load
+          uint32_t v[16], p[8];
+          tmem_ld_32x32b_x16(tmem + lane_base + 16 * c, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            p[i] = bf16x2_rn(__uint_as_float(v[2 * i]) * alpha, __uint_as_float(v[2 * i + 1]) * alpha);
+          if (c < 8) {
+            uint8_t* box = sm.ystage + (c >> 2) * (BM * 128) + r * 128;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int unit = ((c & 3) * 2 + u) ^ (r & 7);
+              *reinterpret_cast<uint4*>(box + unit * 16) = make_uint4(p[4 * u], p[4 * u + 1], p[4 * u + 2], p[4 * u + 3]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) hi[c - 8][i] = p[i];
+          }
+        }
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(&sm.acc_free, 0);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          if (half == 1) {
+            if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              uint8_t* box = sm.ystage + (c >> 2) * (BM * 128) + r * 128;
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                const int unit = ((c & 3) * 2 + u) ^ (r & 7);
+                *reinterpret_cast<uint4*>(box + unit * 16) =
+                    make_uint4(hi[c][4 * u], hi[c][4 * u + 1], hi[c][4 * u + 2], hi[c][4 * u + 3]);
+              }
+            }
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+          if (threadIdx.x == 0 && m0 < M) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              if (n0 + 128 * half + 64 * j < N)
+                asm volatile(
+                    "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(&tmap_y),
+                    "r"((int)(n0 + 128 * half + 64 * j)), "r"((int)m0), "r"(smem_addr(sm.ystage + j * (BM * 128)))
+                    : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + lane_base + 32 * c, v);
+          tmem_wait_ld();
+          if (row < M && n0 + 32 * c < N) store_row32<kF32>(y, row * N, n0 + 32 * c, N, v, alpha, vec_ok);
+        }
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(&sm.acc_free, 0);
+      }
+    }
+    if (failed && lane == 0) atomicOr(status, kStatusTimeout);
+    if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  }
+  // neither CTA leaves (or frees TMEM) while the other may still touch its
+  // shared memory or TMEM
+  fence_before_sync();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 0) {
+    fence_after_sync();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -483,7 +798,62 @@ cudaError_t launch_bn(const uint8_t* a_codes, const uint8_t* a_smma, const float
   return cudaLaunchKernelEx(&cfg, kern, ma, mb, my, tma_store, a_smma, w_smma, a_ts, w_ts, M, N, K, y, status);
 }
 
+std::atomic<int> g_use_pair{1};
+
+// Pair kernel launch: clusters of two CTAs, one CTA per SM (the shared-memory
+// request is above half an SM's), as many pairs as fit at once or as there
+// are tiles.  cudaErrorNotSupported when no pair can be resident.
+cudaError_t launch_pair(const uint8_t* a_codes, const uint8_t* a_smma, const float* a_ts, int64_t M,
+                        const uint8_t* w_codes, const uint8_t* w_smma, const float* w_ts, int64_t N, int64_t K,
+                        void* y, bool out_f32, unsigned int* status, cudaStream_t stream) {
+  CUtensorMap ma, mb, my;
+  if (!make_map(&ma, a_codes, (uint64_t)M, (uint64_t)K / 2, BM) ||
+      !make_map(&mb, w_codes, (uint64_t)N, (uint64_t)K / 2, 128))
+    return cudaErrorInvalidValue;
+  int tma_store = (!out_f32 && N % 8 == 0) ? 1 : 0;
+  memset(&my, 0, sizeof my);
+  if (tma_store && !make_y_map(&my, y, (uint64_t)M, (uint64_t)N)) tma_store = 0;
+  const size_t smem = sizeof(PairSmem) + 1024;
+  auto kern = out_f32 ? w4a4_pair_kernel<true> : w4a4_pair_kernel<false>;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  // resident pairs per GPU, once per output type (the device is fixed for the process)
+  static int max_pairs[2] = {0, 0};
+  static std::once_flag once[2];
+  cudaError_t err = cudaSuccess;
+  std::call_once(once[out_f32 ? 1 : 0], [&] {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return;
+    cudaLaunchConfig_t q = cfg;
+    q.gridDim = dim3(2);
+    q.numAttrs = 1;  // the cluster shape only
+    int n = 0;
+    err = cudaOccupancyMaxActiveClusters(&n, kern, &q);
+    max_pairs[out_f32 ? 1 : 0] = err == cudaSuccess ? n : 0;
+  });
+  if (err != cudaSuccess) return err;
+  const int mp = max_pairs[out_f32 ? 1 : 0];
+  if (mp < 1) return cudaErrorNotSupported;
+  const int64_t work = ((M + 255) / 256) * ((N + 255) / 256);
+  cfg.gridDim = dim3((unsigned)(2 * std::min<int64_t>(work, mp)));
+  return cudaLaunchKernelEx(&cfg, kern, ma, mb, my, tma_store, a_smma, w_smma, a_ts, w_ts, M, N, K, y, status);
+}
+
 }  // namespace
+
+void w4a4_set_pair(bool on) { g_use_pair.store(on ? 1 : 0, std::memory_order_relaxed); }
+bool w4a4_get_pair() { return g_use_pair.load(std::memory_order_relaxed) != 0; }
 
 cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma, const float* a_ts, int64_t M,
                              const uint8_t* w_codes, const uint8_t* w_scales_mma, const float* w_ts, int64_t N,
@@ -494,6 +864,11 @@ cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma
   if (M <= BM)
     return launch_bn<64>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, out_f32, status,
                          num_sms, stream);
+  if (w4a4_get_pair()) {
+    const cudaError_t err =
+        launch_pair(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, out_f32, status, stream);
+    if (err != cudaErrorNotSupported) return err;
+  }
   return launch_bn<256>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, out_f32, status,
                         num_sms, stream);
 }

@@ -78,6 +78,15 @@ def test_w4a16_sk_knob(L):
     assert nv.nvfp4_get_w4a16_sk_max_m() == saved
 
 
+def test_w4a4_pair_knob(L):
+    saved = nv.nvfp4_get_w4a4_pair()
+    assert saved in (True, False)
+    for v in (False, True):
+        nv.nvfp4_set_w4a4_pair(v)
+        assert nv.nvfp4_get_w4a4_pair() == v
+    nv.nvfp4_set_w4a4_pair(saved)
+
+
 def test_status_strings(L):
     for s in range(9):
         assert nv.nvfp4_status_string(s)

@@ -233,6 +233,35 @@ def test_w4a4_small(shape, M):
     run_w4a4(x, wref, K, nv.OUT_BF16)
 
 
+def each_w4a4_kernel(fn):
+    """Runs fn() with the CTA-pair kernel and then the single-CTA kernel for
+    M > 128 (M <= 128 has one kernel)."""
+    saved = nv.nvfp4_get_w4a4_pair()
+    try:
+        for pair in (True, False):
+            nv.nvfp4_set_w4a4_pair(pair)
+            fn()
+    finally:
+        nv.nvfp4_set_w4a4_pair(saved)
+
+
+@pytest.mark.parametrize("shape", [(256, 256), (200, 320), (300, 512), (520, 1024), (1000, 4160)])
+@pytest.mark.parametrize("M", [129, 200, 256, 300, 513])
+def test_w4a4_both_kernels(shape, M):
+    """Both W4A4 kernels for M > 128 match the oracle: ragged M (a CTA pair
+    whose second CTA has no rows), ragged N (a tile whose second weight half is
+    empty or partial), K with a partial last stage."""
+    N, K = shape
+    wref = oracle_weight(synth.weight_normal(N, K, seed=N * 5 + K, outlier_frac=0.01))
+    x = synth.act_student_t(M, K, seed=M + 2000)
+
+    def check():
+        run_w4a4(x, wref, K, nv.OUT_F32)
+        run_w4a4(x, wref, K, nv.OUT_BF16)
+    each_w4a4_kernel(check)
+    assert nv.nvfp4_get_device_status() == 0
+
+
 def test_w4a4_prefill_shapes():
     wref = oracle_weight(synth.prefill_weight())
     cols = sample_rows(11008, 256, 2)
