@@ -40,7 +40,7 @@
  *   - The library keeps no state between calls except the crossover table
  *     (nvfp4_set_crossover), the W4A16 kernel knob
  *     (nvfp4_set_w4a16_rf_max_m, nvfp4_set_w4a16_sk_max_m), the W4A4 kernel
- *     knob (nvfp4_set_w4a4_pair), the weight-prefetch flag
+ *     knob (nvfp4_set_w4a4_cluster), the weight-prefetch flag
  *     (nvfp4_set_weight_prefetch) and the device status word.
  */
 #ifndef NVFP4_H_
@@ -256,13 +256,20 @@ int64_t nvfp4_get_w4a16_sk_max_m(void);
 nvfp4_status nvfp4_set_weight_prefetch(int enable);
 int nvfp4_get_weight_prefetch(void);
 
-/* W4A4 kernel for M > 128 (default on).  On: pairs of CTAs in a cluster share
- * each 256 x 256 output tile through cta_group::2 MMAs (each CTA stages half
- * of the A rows and half of the B rows of every K stage); off: one CTA per
- * 128 x 256 tile.  Both compute the same product with the same fp32
- * accumulation order per output.  A tuning knob; thread-safe. */
-nvfp4_status nvfp4_set_w4a4_pair(int enable);
-int nvfp4_get_w4a4_pair(void);
+/* W4A4 kernel for M > 128: CTAs per thread-block cluster (default 2).
+ *   2: a pair of CTAs shares each 256 x 256 output tile through cta_group::2
+ *      MMAs (each CTA stages half of the A rows and half of the B rows of
+ *      every K stage);
+ *   4: two such pairs compute adjacent tiles of the same 256 rows and share
+ *      those A rows by TMA multicast (each CTA fetches a quarter of them);
+ *   1: one CTA per 128 x 256 tile.
+ * On GB300, 4 measured no faster than 2 (fewer SMs hold clusters of four).
+ * Where a cluster of the requested size cannot be resident the next smaller
+ * one is used.  All compute the same product with the same fp32 accumulation
+ * order per output.  A tuning knob; thread-safe; NVFP4_ERR_INVALID_ARG for
+ * any other value. */
+nvfp4_status nvfp4_set_w4a4_cluster(int ctas);
+int nvfp4_get_w4a4_cluster(void);
 
 /* Synchronises `stream`, then returns and clears the device status word of the
  * current device: NVFP4_OK, NVFP4_ERR_NONFINITE or NVFP4_ERR_TIMEOUT. */

@@ -25,7 +25,7 @@ __all__ = [
     "nvfp4_gemm_w4a16", "nvfp4_gemm_w4a4", "nvfp4_linear", "nvfp4_linear_noalloc", "nvfp4_set_crossover",
     "nvfp4_get_crossover", "nvfp4_set_w4a16_rf_max_m", "nvfp4_get_w4a16_rf_max_m",
     "nvfp4_set_w4a16_sk_max_m", "nvfp4_get_w4a16_sk_max_m", "nvfp4_set_weight_prefetch",
-    "nvfp4_get_weight_prefetch", "nvfp4_set_w4a4_pair", "nvfp4_get_w4a4_pair", "nvfp4_get_device_status",
+    "nvfp4_get_weight_prefetch", "nvfp4_set_w4a4_cluster", "nvfp4_get_w4a4_cluster", "nvfp4_get_device_status",
     "nvfp4_status_string",
 ]
 
@@ -83,8 +83,8 @@ def lib() -> ctypes.CDLL:
             "nvfp4_get_w4a16_sk_max_m": (i64, []),
             "nvfp4_set_weight_prefetch": (st, [ctypes.c_int]),
             "nvfp4_get_weight_prefetch": (ctypes.c_int, []),
-            "nvfp4_set_w4a4_pair": (st, [ctypes.c_int]),
-            "nvfp4_get_w4a4_pair": (ctypes.c_int, []),
+            "nvfp4_set_w4a4_cluster": (st, [ctypes.c_int]),
+            "nvfp4_get_w4a4_cluster": (ctypes.c_int, []),
             "nvfp4_get_device_status": (st, [vp]),
             "nvfp4_status_string": (ctypes.c_char_p, [st]),
             "nvfp4_last_error": (ctypes.c_char_p, []),
@@ -172,13 +172,13 @@ def nvfp4_get_weight_prefetch() -> bool:
     return bool(lib().nvfp4_get_weight_prefetch())
 
 
-def nvfp4_set_w4a4_pair(enable: bool) -> None:
-    """W4A4 above 128 tokens on CTA pairs (256 x 256 tiles) or single CTAs."""
-    _check(lib().nvfp4_set_w4a4_pair(1 if enable else 0), "nvfp4_set_w4a4_pair")
+def nvfp4_set_w4a4_cluster(ctas: int) -> None:
+    """CTAs per cluster of the W4A4 kernel above 128 tokens: 4, 2 or 1."""
+    _check(lib().nvfp4_set_w4a4_cluster(ctas), "nvfp4_set_w4a4_cluster")
 
 
-def nvfp4_get_w4a4_pair() -> bool:
-    return bool(lib().nvfp4_get_w4a4_pair())
+def nvfp4_get_w4a4_cluster() -> int:
+    return lib().nvfp4_get_w4a4_cluster()
 
 
 def nvfp4_get_device_status(stream=None) -> int:

@@ -300,12 +300,12 @@ nvfp4_status nvfp4_set_w4a16_sk_max_m(int64_t M) {
 
 int64_t nvfp4_get_w4a16_sk_max_m(void) { return g_w4a16_sk_max_m.load(std::memory_order_relaxed); }
 
-nvfp4_status nvfp4_set_w4a4_pair(int enable) {
-  nvfp4::w4a4_set_pair(enable != 0);
+nvfp4_status nvfp4_set_w4a4_cluster(int ctas) {
+  if (!nvfp4::w4a4_set_cluster_ctas(ctas)) return fail(NVFP4_ERR_INVALID_ARG, "w4a4 cluster size must be 1, 2 or 4");
   return NVFP4_OK;
 }
 
-int nvfp4_get_w4a4_pair(void) { return nvfp4::w4a4_get_pair() ? 1 : 0; }
+int nvfp4_get_w4a4_cluster(void) { return nvfp4::w4a4_get_cluster_ctas(); }
 
 nvfp4_status nvfp4_set_weight_prefetch(int enable) {
   g_weight_prefetch.store(enable != 0, std::memory_order_relaxed);

@@ -433,7 +433,19 @@ w4a4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 //     commit that arrives on empty[s] of both CTAs; acc_full likewise;
 //   epilogue (warps 0-3, each CTA): drains its accumulator lanes, then
 //     arrives on the even CTA's acc_free (8 arrivals).
+// With kPairs = 2 a cluster holds two pairs that compute horizontally
+// adjacent tiles (same A rows, weight tiles 2j and 2j + 1): CTA r of pair p
+// loads 64 of its 128 A rows per stage and multicasts them to CTA r of both
+// pairs, so each CTA fetches 8 KB of A per stage instead of 16 KB.  A stage
+// buffer is then written by both pairs, so each pair's leader commits the
+// stage's completion to all four CTAs (empty[s] counts kPairs arrivals).
 constexpr int kPairStages = 5;
+// The pair kernel's loads are issued by three producer warps (A rows and
+// their scales; B rows; B scales): one thread waits ~130-170 cycles per
+// TMA or bulk-copy issue (measured), and the MMAs of a stage take ~560.
+constexpr int kProdB = kMmaWarp + 1, kProdSfb = kMmaWarp + 2;
+constexpr int kPairProducers = 3;
+constexpr int kPairThreads = 32 * (kProdSfb + 1);
 
 struct __align__(1024) PairSmem {
   uint8_t ystage[2 * BM * 128];          // two 128 x 64 bf16 output boxes
@@ -455,8 +467,8 @@ static_assert(kPairSfCol + kPairStages * kPairSfStageCols <= kTmemCols, "TMEM bu
 // kind::mxf4nvf4, E2M1 x E2M1, K-major, N = 256, UE4M3 scales, M = 256
 constexpr uint32_t kPairIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(256 >> 3) << 17) | (2u << 27);
 
-template <bool kF32>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int kPairs, bool kF32>
+__global__ void __launch_bounds__(kPairThreads, 1)
 w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                  const __grid_constant__ CUtensorMap tmap_y, int tma_store, const uint8_t* __restrict__ a_smma,
                  const uint8_t* __restrict__ b_smma, const float* __restrict__ a_ts,
@@ -466,19 +478,23 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
   extern __shared__ uint8_t smem_raw[];
   PairSmem& sm = *reinterpret_cast<PairSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_rank();
-  const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  constexpr int kCtas = 2 * kPairs;
+  const uint32_t crank = cluster_rank();
+  const uint32_t rank = crank & 1u, pidx = crank >> 1, lead = crank & ~1u;  // CTA in pair, pair, its even CTA
+  const uint16_t pair_mask = (uint16_t)(3u << lead), all_mask = (uint16_t)((1u << kCtas) - 1u);
+  const int64_t cl = blockIdx.x / kCtas, ncl = gridDim.x / kCtas;
   const int kb64 = (int)(K / 64);
   const int kt = (kb64 + 3) / 4;
   const int64_t b_row_tiles = (N + 127) / 128;
   const int64_t n_tiles = (N + 255) / 256;
-  const int64_t n_work = ((M + 255) / 256) * n_tiles;
+  const int64_t n_groups = (n_tiles + kPairs - 1) / kPairs;  // a cluster's unit: kPairs adjacent tiles
+  const int64_t n_work = ((M + 255) / 256) * n_groups;
 
   if (warp == kProducerWarp && lane == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.full[s], kPairProducers);
       mbar_init(&sm.sf_full[s], 2 * kSfWarps);
-      mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.empty[s], kPairs);
     }
     mbar_init(&sm.acc_full, 1);
     mbar_init(&sm.acc_free, 2 * kEpiWarps);
@@ -494,21 +510,25 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
   const uint32_t tmem = sm.tmem_base;
   bool failed = false;
 
-  if (warp == kProducerWarp) {
+  if (warp == kProducerWarp || warp == kProdB || warp == kProdSfb) {
     if (lane == 0) {
-      // ---------------- producer (each CTA) ----------------
+      // ---------------- producers (each CTA): A + A scales / B / B scales ----------------
       griddep_wait();
       int g = 0;
-      for (int64_t w = pair; w < n_work && !failed; w += npairs) {
-        const int64_t m_tile = w / n_tiles, n_tile = w - m_tile * n_tiles;
+      for (int64_t w = cl; w < n_work && !failed; w += ncl) {
+        const int64_t m_tile = w / n_groups, n_tile = (w - m_tile * n_groups) * kPairs + pidx;
         const int64_t arow = m_tile * 256 + 128 * rank;
-        const int64_t n0 = n_tile * 256;
+        const int64_t n0 = n_tile * 256;  // past N for the idle pair of a ragged last unit
         const int64_t brow = n0 + 128 * rank;
         // a CTA whose A (or B) rows all lie past M (N) loads nothing for them:
         // its accumulator rows (or the tile's columns from that half) are never stored
         const bool has_a = arow < M, has_b = brow < N;
+        // with kPairs = 2 the two 64-row halves of the A rows come from the two
+        // pairs; a half that lies wholly past M is not loaded by either side
+        const uint32_t a_bytes = kPairs == 1 ? (has_a ? kABytes : 0)
+                                             : (has_a ? kABytes / 2 : 0) + (arow + 64 < M ? kABytes / 2 : 0);
         const int64_t sfb_left = b_row_tiles - n0 / 128;
-        const int nsfb = sfb_left < 2 ? (int)sfb_left : 2;
+        const int nsfb = sfb_left <= 0 ? 0 : sfb_left < 2 ? (int)sfb_left : 2;
         for (int ks = 0; ks < kt; ++ks, ++g) {
           const int s = g % S;
           if (g >= S && !mbar_wait(&sm.empty[s], (uint32_t)(g / S - 1) & 1u)) {
@@ -517,18 +537,31 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
           }
           const int kk_n = min(4, kb64 - 4 * ks);
           const uint32_t sf_bytes = (uint32_t)kk_n * kScaleTileBytes;
-          mbar_arrive_expect_tx(&sm.full[s], (has_a ? kABytes + sf_bytes : 0) + (has_b ? kABytes : 0) +
-                                                 sf_bytes * nsfb);
-          if (has_a) tma_load_2d(sm.a[s], &tmap_a, ks * (BK / 2), (int)arow, &sm.full[s]);
-          if (has_b) tma_load_2d(sm.b[s], &tmap_b, ks * (BK / 2), (int)brow, &sm.full[s]);
-          if (has_a)
-            bulk_load(sm.sfa[s], a_smma + ((arow / 128) * kb64 + 4 * ks) * kScaleTileBytes, sf_bytes, &sm.full[s]);
-          for (int rt = 0; rt < nsfb; ++rt)
-            bulk_load(sm.sfb[s] + rt * kSfaBytes, b_smma + ((n0 / 128 + rt) * kb64 + 4 * ks) * kScaleTileBytes,
-                      sf_bytes, &sm.full[s]);
+          if (warp == kProducerWarp) {
+            mbar_arrive_expect_tx(&sm.full[s], a_bytes + (has_a ? sf_bytes : 0));
+            if (kPairs == 1) {
+              if (has_a) tma_load_2d(sm.a[s], &tmap_a, ks * (BK / 2), (int)arow, &sm.full[s]);
+            } else if (arow + 64 * pidx < M) {
+              // rows [64 pidx, +64) of this CTA's 128, to this CTA and its
+              // counterpart in the other pair
+              tma_load_2d_mc(sm.a[s] + pidx * (kABytes / 2), &tmap_a, ks * (BK / 2), (int)(arow + 64 * pidx),
+                             &sm.full[s], (uint16_t)((1u << rank) | (1u << (rank + 2))));
+            }
+            if (has_a)
+              bulk_load(sm.sfa[s], a_smma + ((arow / 128) * kb64 + 4 * ks) * kScaleTileBytes, sf_bytes,
+                        &sm.full[s]);
+          } else if (warp == kProdB) {
+            mbar_arrive_expect_tx(&sm.full[s], has_b ? kABytes : 0);
+            if (has_b) tma_load_2d(sm.b[s], &tmap_b, ks * (BK / 2), (int)brow, &sm.full[s]);
+          } else {
+            mbar_arrive_expect_tx(&sm.full[s], sf_bytes * nsfb);
+            for (int rt = 0; rt < nsfb; ++rt)
+              bulk_load(sm.sfb[s] + rt * kSfaBytes, b_smma + ((n0 / 128 + rt) * kb64 + 4 * ks) * kScaleTileBytes,
+                        sf_bytes, &sm.full[s]);
+          }
         }
       }
-      griddep_launch_dependents();
+      if (warp == kProducerWarp) griddep_launch_dependents();
       // before the CTA may exit: this CTA's loads have landed and the pair's
       // MMAs that read them have completed
       for (int i = max(0, g - S); i < g && !failed; ++i)
@@ -539,9 +572,9 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0 && rank == 0) {
-      // ---------------- MMA issuer (even CTA) ----------------
+      // ---------------- MMA issuer (even CTA of each pair) ----------------
       int g = 0, t = 0;
-      for (int64_t w = pair; w < n_work && !failed; w += npairs, ++t) {
+      for (int64_t w = cl; w < n_work && !failed; w += ncl, ++t) {
         if (t > 0 && !mbar_wait(&sm.acc_free, (uint32_t)(t - 1) & 1u)) {
           failed = true;
           break;
@@ -562,9 +595,9 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
           for (int kk = 0; kk < kk_n; ++kk)
             mma_mxf4nvf4_pair(tmem, adesc + 2ull * kk, bdesc + 2ull * kk, kPairIdesc, sfa_t + 4 * kk,
                               sfb_t + 8 * kk, (ks | kk) != 0);
-          commit_pair(&sm.empty[s]);
+          commit_pair(&sm.empty[s], all_mask);
         }
-        if (!failed) commit_pair(&sm.acc_full);
+        if (!failed) commit_pair(&sm.acc_full, pair_mask);
       }
       if (failed) atomicOr(status, kStatusTimeout);
     }
@@ -573,7 +606,7 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
     // atom kk of A at column 4 kk; atom (kk, half rt) of B at 16 + 4 (2 kk + rt)
     const uint32_t lane_base = (uint32_t)((warp - kEpiWarps) * 32) << 16;
     int g = 0;
-    for (int64_t w = pair; w < n_work && !failed; w += npairs) {
+    for (int64_t w = cl; w < n_work && !failed; w += ncl) {
       for (int ks = 0; ks < kt; ++ks, ++g) {
         const int s = g % S;
         if (!mbar_wait(&sm.full[s], (uint32_t)(g / S) & 1u) ||
@@ -610,7 +643,7 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         tmem_wait_st();
         fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(&sm.sf_full[s], 0);
+        if (lane == 0) mbar_arrive_cluster(&sm.sf_full[s], lead);
       }
     }
     if (failed && lane == 0) atomicOr(status, kStatusTimeout);
@@ -622,8 +655,8 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const int r = warp * 32 + lane;
     int t = 0;
-    for (int64_t w = pair; w < n_work; w += npairs, ++t) {
-      const int64_t m_tile = w / n_tiles, n_tile = w - m_tile * n_tiles;
+    for (int64_t w = cl; w < n_work; w += ncl, ++t) {
+      const int64_t m_tile = w / n_groups, n_tile = (w - m_tile * n_groups) * kPairs + pidx;
       const int64_t m0 = m_tile * 256 + 128 * rank, n0 = n_tile * 256;
       const int64_t row = m0 + r;
       const bool ok = __all_sync(0xffffffffu, !failed && mbar_wait(&sm.acc_full, (uint32_t)t & 1u));
@@ -662,7 +695,7 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         }
         fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(&sm.acc_free, 0);
+        if (lane == 0) mbar_arrive_cluster(&sm.acc_free, lead);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           if (half == 1) {
@@ -702,7 +735,7 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         }
         fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(&sm.acc_free, 0);
+        if (lane == 0) mbar_arrive_cluster(&sm.acc_free, lead);
       }
     }
     if (failed && lane == 0) atomicOr(status, kStatusTimeout);
@@ -798,62 +831,68 @@ cudaError_t launch_bn(const uint8_t* a_codes, const uint8_t* a_smma, const float
   return cudaLaunchKernelEx(&cfg, kern, ma, mb, my, tma_store, a_smma, w_smma, a_ts, w_ts, M, N, K, y, status);
 }
 
-std::atomic<int> g_use_pair{1};
+std::atomic<int> g_cluster_ctas{2};
 
-// Pair kernel launch: clusters of two CTAs, one CTA per SM (the shared-memory
-// request is above half an SM's), as many pairs as fit at once or as there
-// are tiles.  cudaErrorNotSupported when no pair can be resident.
-cudaError_t launch_pair(const uint8_t* a_codes, const uint8_t* a_smma, const float* a_ts, int64_t M,
-                        const uint8_t* w_codes, const uint8_t* w_smma, const float* w_ts, int64_t N, int64_t K,
-                        void* y, bool out_f32, unsigned int* status, cudaStream_t stream) {
+// Pair-kernel launch: clusters of 2 * kPairs CTAs, one CTA per SM (the
+// shared-memory request is above half an SM's), as many clusters as fit at
+// once or as there are work units.  cudaErrorNotSupported when no cluster of
+// that shape can be resident.
+template <int kPairs>
+cudaError_t launch_pairs(const uint8_t* a_codes, const uint8_t* a_smma, const float* a_ts, int64_t M,
+                         const uint8_t* w_codes, const uint8_t* w_smma, const float* w_ts, int64_t N, int64_t K,
+                         void* y, bool out_f32, unsigned int* status, cudaStream_t stream) {
   CUtensorMap ma, mb, my;
-  if (!make_map(&ma, a_codes, (uint64_t)M, (uint64_t)K / 2, BM) ||
+  if (!make_map(&ma, a_codes, (uint64_t)M, (uint64_t)K / 2, 128 / kPairs) ||
       !make_map(&mb, w_codes, (uint64_t)N, (uint64_t)K / 2, 128))
     return cudaErrorInvalidValue;
   int tma_store = (!out_f32 && N % 8 == 0) ? 1 : 0;
   memset(&my, 0, sizeof my);
   if (tma_store && !make_y_map(&my, y, (uint64_t)M, (uint64_t)N)) tma_store = 0;
   const size_t smem = sizeof(PairSmem) + 1024;
-  auto kern = out_f32 ? w4a4_pair_kernel<true> : w4a4_pair_kernel<false>;
+  auto kern = out_f32 ? w4a4_pair_kernel<kPairs, true> : w4a4_pair_kernel<kPairs, false>;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = 2 * kPairs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kPairThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  // resident pairs per GPU, once per output type (the device is fixed for the process)
-  static int max_pairs[2] = {0, 0};
+  // resident clusters per GPU, once per output type (the device is fixed for the process)
+  static int max_clusters[2] = {0, 0};
   static std::once_flag once[2];
   cudaError_t err = cudaSuccess;
   std::call_once(once[out_f32 ? 1 : 0], [&] {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return;
     cudaLaunchConfig_t q = cfg;
-    q.gridDim = dim3(2);
+    q.gridDim = dim3(2 * kPairs);
     q.numAttrs = 1;  // the cluster shape only
     int n = 0;
     err = cudaOccupancyMaxActiveClusters(&n, kern, &q);
-    max_pairs[out_f32 ? 1 : 0] = err == cudaSuccess ? n : 0;
+    max_clusters[out_f32 ? 1 : 0] = err == cudaSuccess ? n : 0;
   });
   if (err != cudaSuccess) return err;
-  const int mp = max_pairs[out_f32 ? 1 : 0];
-  if (mp < 1) return cudaErrorNotSupported;
-  const int64_t work = ((M + 255) / 256) * ((N + 255) / 256);
-  cfg.gridDim = dim3((unsigned)(2 * std::min<int64_t>(work, mp)));
+  const int mc = max_clusters[out_f32 ? 1 : 0];
+  if (mc < 1) return cudaErrorNotSupported;
+  const int64_t work = ((M + 255) / 256) * (((N + 255) / 256 + kPairs - 1) / kPairs);
+  cfg.gridDim = dim3((unsigned)(2 * kPairs * std::min<int64_t>(work, mc)));
   return cudaLaunchKernelEx(&cfg, kern, ma, mb, my, tma_store, a_smma, w_smma, a_ts, w_ts, M, N, K, y, status);
 }
 
 }  // namespace
 
-void w4a4_set_pair(bool on) { g_use_pair.store(on ? 1 : 0, std::memory_order_relaxed); }
-bool w4a4_get_pair() { return g_use_pair.load(std::memory_order_relaxed) != 0; }
+bool w4a4_set_cluster_ctas(int ctas) {
+  if (ctas != 1 && ctas != 2 && ctas != 4) return false;
+  g_cluster_ctas.store(ctas, std::memory_order_relaxed);
+  return true;
+}
+int w4a4_get_cluster_ctas() { return g_cluster_ctas.load(std::memory_order_relaxed); }
 
 cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma, const float* a_ts, int64_t M,
                              const uint8_t* w_codes, const uint8_t* w_scales_mma, const float* w_ts, int64_t N,
@@ -864,11 +903,15 @@ cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma
   if (M <= BM)
     return launch_bn<64>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, out_f32, status,
                          num_sms, stream);
-  if (w4a4_get_pair()) {
-    const cudaError_t err =
-        launch_pair(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, out_f32, status, stream);
-    if (err != cudaErrorNotSupported) return err;
-  }
+  const int ctas = w4a4_get_cluster_ctas();
+  cudaError_t err = cudaErrorNotSupported;
+  if (ctas == 4)
+    err = launch_pairs<2>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, out_f32, status,
+                          stream);
+  if (ctas >= 2 && err == cudaErrorNotSupported)
+    err = launch_pairs<1>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, out_f32, status,
+                          stream);
+  if (err != cudaErrorNotSupported) return err;
   return launch_bn<256>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, out_f32, status,
                         num_sms, stream);
 }

@@ -49,9 +49,10 @@ cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma
                              int64_t M, const uint8_t* w_codes, const uint8_t* w_scales_mma,
                              const float* w_ts, int64_t N, int64_t K, void* y, bool out_f32,
                              unsigned int* status, int num_sms, cudaStream_t stream);
-// Whether M > 128 runs on CTA pairs (cta_group::2, 256 x 256 tiles) or on
-// single CTAs (128 x 256 tiles).
-void w4a4_set_pair(bool on);
-bool w4a4_get_pair();
+// CTAs per cluster for M > 128: 4 (two CTA pairs sharing A rows by TMA
+// multicast), 2 (one pair, cta_group::2 MMAs on 256 x 256 tiles) or 1 (single
+// CTAs on 128 x 256 tiles).  The setter rejects anything else.
+bool w4a4_set_cluster_ctas(int ctas);
+int w4a4_get_cluster_ctas();
 
 }  // namespace nvfp4

@@ -153,13 +153,25 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
   asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
-// Arrive on `bar` in both CTAs of the pair once every tcgen05 operation this
-// thread issued so far has completed.
-__device__ __forceinline__ void commit_pair(uint64_t* bar) {
+// Arrive on `bar` in every CTA of `cta_mask` (cluster ranks) once every
+// tcgen05 operation this thread issued so far has completed.
+__device__ __forceinline__ void commit_pair(uint64_t* bar, uint16_t cta_mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
           smem_addr(bar)),
-      "h"((uint16_t)3)
+      "h"(cta_mask)
+      : "memory");
+}
+
+// 2-D tiled TMA load of one box into the same shared-memory offset of every
+// CTA in `cta_mask`, each CTA's mbarrier at `bar`'s offset receiving the bytes
+// that land in it.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                               uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(cta_mask)
       : "memory");
 }
 

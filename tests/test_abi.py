@@ -78,13 +78,16 @@ def test_w4a16_sk_knob(L):
     assert nv.nvfp4_get_w4a16_sk_max_m() == saved
 
 
-def test_w4a4_pair_knob(L):
-    saved = nv.nvfp4_get_w4a4_pair()
-    assert saved in (True, False)
-    for v in (False, True):
-        nv.nvfp4_set_w4a4_pair(v)
-        assert nv.nvfp4_get_w4a4_pair() == v
-    nv.nvfp4_set_w4a4_pair(saved)
+def test_w4a4_cluster_knob(L):
+    saved = nv.nvfp4_get_w4a4_cluster()
+    assert saved in (1, 2, 4)
+    for v in (1, 2, 4):
+        nv.nvfp4_set_w4a4_cluster(v)
+        assert nv.nvfp4_get_w4a4_cluster() == v
+    for bad in (0, 3, 8):
+        with pytest.raises(nv.NVFP4Error):
+            nv.nvfp4_set_w4a4_cluster(bad)
+    nv.nvfp4_set_w4a4_cluster(saved)
 
 
 def test_status_strings(L):
