@@ -54,6 +54,21 @@ def peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+FP4_PER_BF16 = 13.5 / 2.25   # nominal dense FP4 : bf16 tensor rate
+
+
+def fp4_peaks():
+    """(burst, sustained) dense FP4 TFLOP/s: the measured bf16 peaks times the
+    nominal FP4/bf16 ratio (the file holds no FP4 figure), and their source."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return (float(p["bf16_tflops"]) * FP4_PER_BF16, float(p["bf16_tflops_sustained"]) * FP4_PER_BF16,
+                "measured bf16 (MEASURED_PEAKS.json bf16_tflops, bf16_tflops_sustained) x 6")
+    except Exception:
+        return 1900.0 * FP4_PER_BF16, 1700.0 * FP4_PER_BF16, "fallback bf16 1.9 / 1.7 PFLOP/s x 6"
+
+
 def q_bytes(N, K):   # quantiser: bf16 read once + codes + MMA scales written
     return N * K * 2 + N * K // 2 + N * K // 16
 
@@ -314,6 +329,7 @@ def run_ours(args):
     }
     if not args.no_prefill and rank == 0:
         detail["w4a4_prefill"] = prefill_sweep(nv, dev, stream)
+        detail["model_quantizer"] = model_quantizer(nv, dev, stream)
 
     e2e = measure_e2e(nv, dev, stream, w_bits, args, step_bytes, paths) if rank == 0 else None
 
@@ -376,8 +392,83 @@ def prefill_sweep(nv, dev, stream):
             e1.record(stream)
         e1.synchronize()
         t = e0.elapsed_time(e1) * 1e-3 / reps
-        res[str(M)] = {"gemm_us": round(t * 1e6, 1), "tflops": round(2 * M * N * K / t / 1e12, 1)}
+        tf = 2 * M * N * K / t / 1e12
+        burst, sustained, _ = fp4_peaks()
+        res[str(M)] = {"gemm_us": round(t * 1e6, 1), "tflops": round(tf, 1),
+                       "frac_fp4_burst": round(tf / burst, 3), "frac_fp4_sustained": round(tf / sustained, 3)}
+    res["fp4_peak_tflops"] = {"burst": round(fp4_peaks()[0], 1), "sustained": round(fp4_peaks()[1], 1),
+                              "source": fp4_peaks()[2]}
     return res
+
+
+def model_quantizer(nv, dev, stream, layers=32, distinct=2):
+    """Whole-model quantiser throughput: a 32-layer stack (qkv 6144x4096, o
+    4096x4096, gate/up 22016x4096, down 4096x11008; N(0, 0.02^2), 0.5 %
+    outliers x8) quantised one matrix at a time, inputs resident.  `distinct`
+    layers are generated on the device from seeded generators (each larger
+    than L2) and reused in turn; the timed region is one CUDA graph of all
+    4 * layers FourOverSix quantisations.  Reports GB/s of bf16 read, the
+    fraction of HBM on the quantiser's algorithmic bytes, and the fraction of
+    blocks that chose M=4."""
+    import torch
+    shapes = [(N, K) for _, N, K in synth.MODEL_LAYER_SHAPES]
+    gen = torch.Generator(device=dev)
+    ws = []
+    for li in range(distinct):
+        mats = []
+        for wi, (N, K) in enumerate(shapes):
+            gen.manual_seed(500 + 4 * li + wi)
+            w = torch.randn(N, K, device=dev, generator=gen) * 0.02
+            w = torch.where(torch.rand(N, K, device=dev, generator=gen) < 0.005, w * 8, w)
+            mats.append(w.to(torch.bfloat16))
+            del w
+        ws.append(mats)
+    outs = []
+    for N, K in shapes:
+        outs.append((torch.empty(N * K // 2, dtype=torch.uint8, device=dev),
+                     torch.empty(nv.nvfp4_scales_mma_bytes(N, K), dtype=torch.uint8, device=dev),
+                     torch.empty(1, dtype=torch.float32, device=dev)))
+    wsb = max(nv.nvfp4_workspace_bytes(nv.OP_QUANTIZE_FOS, 0, N, K) for N, K in shapes)
+    qws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    m4 = torch.zeros(1, dtype=torch.int64, device=dev)
+
+    def quant(w, o, N, K, count):
+        st = nv.lib().nvfp4_quantize_fos(w.data_ptr(), N, K, 0.0, o[0].data_ptr(), None, o[1].data_ptr(),
+                                         o[2].data_ptr(), None, m4.data_ptr() if count else None, qws.data_ptr(),
+                                         qws.numel(), stream.cuda_stream)
+        assert st == 0, nv.nvfp4_status_string(st)
+
+    # fraction of M=4 blocks over the distinct layers (outside the timed region)
+    n4, nblk = 0, 0
+    with torch.cuda.stream(stream):
+        for mats in ws:
+            for w, o, (N, K) in zip(mats, outs, shapes):
+                quant(w, o, N, K, True)
+                stream.synchronize()
+                n4 += int(m4.item())
+                nblk += N * K // 16
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for li in range(layers):
+            for w, o, (N, K) in zip(ws[li % distinct], outs, shapes):
+                quant(w, o, N, K, False)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    t = e0.elapsed_time(e1) * 1e-3
+    elems = layers * sum(N * K for N, K in shapes)
+    qb = layers * sum(q_bytes(N, K) for N, K in shapes)
+    hbm_peak = peaks()[0]
+    del ws, g
+    torch.cuda.empty_cache()
+    return {"layers": layers, "params": elems, "ms": round(t * 1e3, 3),
+            "gbs_bf16_read": round(2 * elems / t / 1e9, 1), "frac_hbm": round(qb / t / 1e9 / hbm_peak, 3),
+            "m4_block_fraction": round(n4 / nblk, 4),
+            "inputs": f"{distinct} distinct layers generated on the device (torch, seeded), reused in turn"}
 
 
 def measure_e2e(nv, dev, stream, w_bits, args, step_bytes, paths):
