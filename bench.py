@@ -330,6 +330,7 @@ def run_ours(args):
     if not args.no_prefill and rank == 0:
         detail["w4a4_prefill"] = prefill_sweep(nv, dev, stream)
         detail["model_quantizer"] = model_quantizer(nv, dev, stream)
+        detail["act_fos"] = act_fos_compare(nv, dev, stream)
 
     e2e = measure_e2e(nv, dev, stream, w_bits, args, step_bytes, paths) if rank == 0 else None
 
@@ -399,6 +400,53 @@ def prefill_sweep(nv, dev, stream):
     res["fp4_peak_tflops"] = {"burst": round(fp4_peaks()[0], 1), "sustained": round(fp4_peaks()[1], 1),
                               "source": fp4_peaks()[2]}
     return res
+
+
+def act_fos_compare(nv, dev, stream, M=1024):
+    """FourOverSix for activations against the M=6-only rule on the prefill
+    workload (W [11008, 4096], X [M, 4096] 0.5 * Student-t(4)): normwise error
+    of the W4A4 output against W4A16 on the unquantised activations (same
+    quantised weight, so the difference is the activation quantisation), the
+    M=4 block fraction, and the quantiser's cost (graph of 10 calls each)."""
+    import torch
+    bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
+    qp = nv.nvfp4_quantize_fos(bf(synth.prefill_weight()), logical_scales=False, choice=False)
+    X = bf(synth.prefill_act(M))
+    with torch.cuda.stream(stream):
+        y16 = nv.nvfp4_gemm_w4a16(X, qp, nv.OUT_F32, stream=stream).double()
+        a6 = nv.nvfp4_quantize_act(X, stream=stream)
+        y6 = nv.nvfp4_gemm_w4a4(a6, qp, nv.OUT_F32, stream=stream).double()
+        q4 = nv.nvfp4_quantize_fos(X, logical_scales=False, choice=True, stream=stream)
+        a4 = nv.NVFP4Act(codes=q4.codes, scales_mma=q4.scales_mma, tensor_scale=q4.tensor_scale, M=M, K=X.shape[1])
+        y4 = nv.nvfp4_gemm_w4a4(a4, qp, nv.OUT_F32, stream=stream).double()
+    stream.synchronize()
+    ref = torch.linalg.norm(y16)
+    err6 = float(torch.linalg.norm(y6 - y16) / ref)
+    err4 = float(torch.linalg.norm(y4 - y16) / ref)
+    m4 = float(q4.choice.float().mean())
+
+    def timed(fn, reps=10):
+        with torch.cuda.stream(stream):
+            fn()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) * 1e-3 / reps
+
+    t6 = timed(lambda: nv.nvfp4_quantize_act(X, stream=stream))
+    t4 = timed(lambda: nv.nvfp4_quantize_fos(X, logical_scales=False, choice=False, stream=stream))
+    return {"M": M, "rel_err_m6": round(err6, 5), "rel_err_fos": round(err4, 5), "m4_block_fraction": round(m4, 4),
+            "quant_us_m6": round(t6 * 1e6, 2), "quant_us_fos": round(t4 * 1e6, 2),
+            "error": "||Y_w4a4 - Y_w4a16||_F / ||Y_w4a16||_F, same quantised weight"}
 
 
 def model_quantizer(nv, dev, stream, layers=32, distinct=2):

@@ -40,7 +40,8 @@
  *   - The library keeps no state between calls except the crossover table
  *     (nvfp4_set_crossover), the W4A16 kernel knob
  *     (nvfp4_set_w4a16_rf_max_m, nvfp4_set_w4a16_sk_max_m), the W4A4 kernel
- *     knob (nvfp4_set_w4a4_cluster), the weight-prefetch flag
+ *     knob (nvfp4_set_w4a4_cluster), the activation FourOverSix flag
+ *     (nvfp4_set_act_fos), the weight-prefetch flag
  *     (nvfp4_set_weight_prefetch) and the device status word.
  */
 #ifndef NVFP4_H_
@@ -189,7 +190,8 @@ nvfp4_status nvfp4_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma
  * take W4A16, larger ones W4A4, the two latency curves crossing near M = 48
  * on the pages' GPU, and the faster path is chosen per call).  M <=
  * crossover(N, K) runs nvfp4_gemm_w4a16; otherwise
- * nvfp4_quantize_act (into the workspace) then nvfp4_gemm_w4a4.
+ * nvfp4_quantize_act (into the workspace) then nvfp4_gemm_w4a4 -- or, with
+ * nvfp4_set_act_fos(1), the FourOverSix quantiser on the activations.
  *   workspace  nvfp4_workspace_bytes(NVFP4_OP_LINEAR, M, N, K) bytes
  */
 nvfp4_status nvfp4_linear(const void* X, int64_t M, const nvfp4_weight* W, void* Y,
@@ -255,6 +257,18 @@ int64_t nvfp4_get_w4a16_sk_max_m(void);
  * quantised once and then only read, as in inference.  Thread-safe. */
 nvfp4_status nvfp4_set_weight_prefetch(int enable);
 int nvfp4_get_weight_prefetch(void);
+
+/* FourOverSix for activations (default off).  The pages apply the M=4 / M=6
+ * choice to weights and say nothing of activations; when on, nvfp4_linear's
+ * W4A4 branch quantises X with the same FourOverSix rule and kernel as
+ * nvfp4_quantize_fos (per 16-block: scale 6 or its 1.5x rounding, whichever
+ * gives the smaller block squared error; tensor scale amax / 2688) instead of
+ * the scale-6-only rule of nvfp4_quantize_act.  nvfp4_quantize_fos itself
+ * accepts any bf16 [rows, K] tensor, activations included, and its codes,
+ * MMA scales and tensor scale feed nvfp4_gemm_w4a4 as the A operand.
+ * Thread-safe. */
+nvfp4_status nvfp4_set_act_fos(int enable);
+int nvfp4_get_act_fos(void);
 
 /* W4A4 kernel for M > 128: CTAs per thread-block cluster (default 2).
  *   2: a pair of CTAs shares each 256 x 256 output tile through cta_group::2

@@ -25,7 +25,7 @@ __all__ = [
     "nvfp4_gemm_w4a16", "nvfp4_gemm_w4a4", "nvfp4_linear", "nvfp4_linear_noalloc", "nvfp4_set_crossover",
     "nvfp4_get_crossover", "nvfp4_set_w4a16_rf_max_m", "nvfp4_get_w4a16_rf_max_m",
     "nvfp4_set_w4a16_sk_max_m", "nvfp4_get_w4a16_sk_max_m", "nvfp4_set_weight_prefetch",
-    "nvfp4_get_weight_prefetch", "nvfp4_set_w4a4_cluster", "nvfp4_get_w4a4_cluster", "nvfp4_get_device_status",
+    "nvfp4_get_weight_prefetch", "nvfp4_set_w4a4_cluster", "nvfp4_get_w4a4_cluster", "nvfp4_set_act_fos", "nvfp4_get_act_fos", "nvfp4_get_device_status",
     "nvfp4_status_string",
 ]
 
@@ -84,6 +84,8 @@ def lib() -> ctypes.CDLL:
             "nvfp4_set_weight_prefetch": (st, [ctypes.c_int]),
             "nvfp4_get_weight_prefetch": (ctypes.c_int, []),
             "nvfp4_set_w4a4_cluster": (st, [ctypes.c_int]),
+            "nvfp4_set_act_fos": (st, [ctypes.c_int]),
+            "nvfp4_get_act_fos": (ctypes.c_int, []),
             "nvfp4_get_w4a4_cluster": (ctypes.c_int, []),
             "nvfp4_get_device_status": (st, [vp]),
             "nvfp4_status_string": (ctypes.c_char_p, [st]),
@@ -179,6 +181,15 @@ def nvfp4_set_w4a4_cluster(ctas: int) -> None:
 
 def nvfp4_get_w4a4_cluster() -> int:
     return lib().nvfp4_get_w4a4_cluster()
+
+
+def nvfp4_set_act_fos(enable: bool) -> None:
+    """nvfp4_linear's W4A4 branch: FourOverSix (True) or M=6-only (False) activations."""
+    _check(lib().nvfp4_set_act_fos(1 if enable else 0), "nvfp4_set_act_fos")
+
+
+def nvfp4_get_act_fos() -> bool:
+    return bool(lib().nvfp4_get_act_fos())
 
 
 def nvfp4_get_device_status(stream=None) -> int:

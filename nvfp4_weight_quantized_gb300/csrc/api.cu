@@ -37,6 +37,9 @@ std::atomic<int64_t> g_w4a16_sk_max_m{-1};
 // Whether GEMM kernels may read the weights before the previous kernel in the
 // stream has finished (nvfp4_set_weight_prefetch).
 std::atomic<bool> g_weight_prefetch{false};
+// Whether nvfp4_linear's W4A4 branch quantises activations with FourOverSix
+// (nvfp4_set_act_fos) instead of the M=6 scale only.
+std::atomic<bool> g_act_fos{false};
 
 struct DeviceInfo {
   bool ready = false;
@@ -270,8 +273,9 @@ nvfp4_status nvfp4_linear(const void* X, int64_t M, const nvfp4_weight* W, void*
   uint8_t* a_codes = ws + l.codes_off;
   uint8_t* a_smma = ws + l.scales_off;
   float* a_ts = reinterpret_cast<float*>(ws + l.ts_off);
-  st = nvfp4_quantize_act(X, M, W->K, NVFP4_DEFAULT_DIVISOR, a_codes, nullptr, a_smma, a_ts, ws + l.quant_off,
-                          workspace_bytes - l.quant_off, stream);
+  st = quantize_common(X, M, W->K, NVFP4_DEFAULT_DIVISOR, g_act_fos.load(std::memory_order_relaxed), a_codes,
+                       nullptr, a_smma, a_ts, nullptr, nullptr, ws + l.quant_off, workspace_bytes - l.quant_off,
+                       stream);
   if (st != NVFP4_OK) return st;
   return nvfp4_gemm_w4a4(a_codes, a_smma, a_ts, M, W, Y, out_dtype, nullptr, 0, stream);
 }
@@ -313,6 +317,13 @@ nvfp4_status nvfp4_set_weight_prefetch(int enable) {
 }
 
 int nvfp4_get_weight_prefetch(void) { return g_weight_prefetch.load(std::memory_order_relaxed) ? 1 : 0; }
+
+nvfp4_status nvfp4_set_act_fos(int enable) {
+  g_act_fos.store(enable != 0, std::memory_order_relaxed);
+  return NVFP4_OK;
+}
+
+int nvfp4_get_act_fos(void) { return g_act_fos.load(std::memory_order_relaxed) ? 1 : 0; }
 
 int64_t nvfp4_get_crossover(int64_t N, int64_t K) {
   std::lock_guard<std::mutex> lk(g_mu);

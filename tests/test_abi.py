@@ -90,6 +90,14 @@ def test_w4a4_cluster_knob(L):
     nv.nvfp4_set_w4a4_cluster(saved)
 
 
+def test_act_fos_knob(L):
+    saved = nv.nvfp4_get_act_fos()
+    for v in (True, False):
+        nv.nvfp4_set_act_fos(v)
+        assert nv.nvfp4_get_act_fos() == v
+    nv.nvfp4_set_act_fos(saved)
+
+
 def test_status_strings(L):
     for s in range(9):
         assert nv.nvfp4_status_string(s)

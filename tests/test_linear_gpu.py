@@ -52,6 +52,41 @@ def test_dispatch_follows_crossover():
         nv.nvfp4_set_crossover(N, K, old)
 
 
+def test_linear_with_fos_activations():
+    """With the activation FourOverSix option the W4A4 branch equals W4A4 on
+    nvfp4_quantize_fos(X) and matches the oracle with FourOverSix-quantised
+    activations; the W4A16 branch is unaffected."""
+    N, K = 384, 1024
+    w = synth.weight_normal(N, K, seed=93, outlier_frac=0.01)
+    W = nv.nvfp4_quantize_fos(to_dev(w))
+    wts = oracle.tensor_scale(w)
+    wref = oracle.quantize_rows(w, wts, True, THREADS)
+    old = nv.nvfp4_get_crossover(N, K)
+    nv.nvfp4_set_crossover(N, K, 40)
+    nv.nvfp4_set_act_fos(True)
+    try:
+        for M in (1, 41, 130, 300):
+            x = synth.act_student_t(M, K, seed=700 + M)
+            X = to_dev(x)
+            y = nv.nvfp4_linear(X, W, nv.OUT_F32)
+            if M <= 40:
+                direct = nv.nvfp4_gemm_w4a16(X, W, nv.OUT_F32)
+            else:
+                q = nv.nvfp4_quantize_fos(X, logical_scales=False, choice=False)
+                A = nv.NVFP4Act(codes=q.codes, scales_mma=q.scales_mma, tensor_scale=q.tensor_scale, M=M, K=K)
+                direct = nv.nvfp4_gemm_w4a4(A, W, nv.OUT_F32)
+            torch.cuda.synchronize()
+            assert torch.equal(y, direct), M
+            if M > 40:
+                aref = oracle.quantize_rows(x, oracle.tensor_scale(x), True, THREADS)
+                ref = oracle_w4a4(aref["codes"], aref["scales"], aref["ts"], wref["codes"], wref["scales"],
+                                  wref["ts"])
+                assert_gemm_close(y_to_np(y), ref, bf16=False, what=f"linear act-FOS M={M}")
+    finally:
+        nv.nvfp4_set_act_fos(False)
+        nv.nvfp4_set_crossover(N, K, old)
+
+
 def test_linear_small_k_always_takes_w4a16():
     N, K = 64, 128  # below one 256-wide K stage of the tensor-core kernel
     w = synth.weight_normal(N, K, seed=5)

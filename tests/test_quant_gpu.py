@@ -88,6 +88,14 @@ def test_ragged_shapes(shape):
     check_act(synth.act_student_t(N, K, seed=N * 11 + K))
 
 
+def test_fos_on_activations():
+    """FourOverSix applied to activation-shaped tensors (Student-t tokens, the
+    prefill distribution), the activation option of nvfp4_linear: codes,
+    scales, choices and tensor scale bit-exact against the oracle."""
+    for M, K, seed in ((130, 1024, 3), (257, 4096, 4)):
+        check_fos(synth.act_student_t(M, K, seed=seed))
+
+
 def test_custom_divisor():
     w = synth.weight_normal(64, 512, seed=77, outlier_frac=0.02)
     check_fos(w, divisor=4 * 448.0)
