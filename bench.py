@@ -331,6 +331,7 @@ def run_ours(args):
         detail["w4a4_prefill"] = prefill_sweep(nv, dev, stream)
         detail["model_quantizer"] = model_quantizer(nv, dev, stream)
         detail["act_fos"] = act_fos_compare(nv, dev, stream)
+        detail["gate_up_silu_mul"] = gate_up_bench(nv, dev, stream)
 
     e2e = measure_e2e(nv, dev, stream, w_bits, args, step_bytes, paths) if rank == 0 else None
 
@@ -447,6 +448,65 @@ def act_fos_compare(nv, dev, stream, M=1024):
     return {"M": M, "rel_err_m6": round(err6, 5), "rel_err_fos": round(err4, 5), "m4_block_fraction": round(m4, 4),
             "quant_us_m6": round(t6 * 1e6, 2), "quant_us_fos": round(t4 * 1e6, 2),
             "error": "||Y_w4a4 - Y_w4a16||_F / ||Y_w4a16||_F, same quantised weight"}
+
+
+def gate_up_bench(nv, dev, stream):
+    """Gated MLP projection silu(X W_gate^T) * (X W_up^T) on the config-3
+    gate/up weight [2 x 11008, 4096] (N(0, 0.02^2) x per-row lognormal(0, 0.5)):
+    nvfp4_linear_silu_mul against nvfp4_linear on the same weight (Y [M, 2F]),
+    at decode M (W4A16 + the separate silu kernel; 4 weight copies rotate so
+    reads are cold) and prefill M (W4A4 with silu(G) * U fused into the
+    CTA-pair kernel's epilogue)."""
+    import torch
+    bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
+    gate_up, _ = synth.mlp_weights()
+    q = nv.nvfp4_quantize_fos(bf(gate_up), logical_scales=False, choice=False)
+    N, K = q.N, q.K
+    copies = [q] + [nv.NVFP4Weight(q.codes.clone(), q.scales_mma.clone(), q.tensor_scale.clone(), N, K)
+                     for _ in range(3)]
+
+    def timed(fn, reps):
+        with torch.cuda.stream(stream):
+            fn(0)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(reps):
+                fn(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) * 1e-3 / reps
+
+    res = {}
+    for M in (1, 8, 32, 48, 4096, 16384):
+        X = bf(synth.prefill_act(M) if M > 64 else synth.decode_act(M))
+        Y1 = torch.empty((M, N // 2), dtype=torch.bfloat16, device=dev)
+        Y2 = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        ws1 = torch.empty(nv.nvfp4_workspace_bytes(nv.OP_LINEAR_SILU_MUL, M, N, K), dtype=torch.uint8, device=dev)
+        ws2 = torch.empty(max(nv.nvfp4_workspace_bytes(nv.OP_LINEAR, M, N, K), 256), dtype=torch.uint8, device=dev)
+        reps = 8 if M <= 64 else 3
+        t1 = timed(lambda i: nv.nvfp4_linear_silu_mul(X, copies[i % 4], out=Y1, workspace=ws1, stream=stream), reps)
+        t2 = timed(lambda i: nv.nvfp4_linear(X, copies[i % 4], out=Y2, workspace=ws2, stream=stream), reps)
+        res[str(M)] = {"silu_mul_us": round(t1 * 1e6, 2), "linear_us": round(t2 * 1e6, 2)}
+        if M > 64:
+            # the separate form (GEMM to fp32 in 1024-row chunks, then the silu
+            # kernel), which single-CTA W4A4 tiles force
+            saved = nv.nvfp4_get_w4a4_cluster()
+            nv.nvfp4_set_w4a4_cluster(1)
+            try:
+                t3 = timed(lambda i: nv.nvfp4_linear_silu_mul(X, copies[i % 4], out=Y1, workspace=ws1,
+                                                              stream=stream), reps)
+            finally:
+                nv.nvfp4_set_w4a4_cluster(saved)
+            res[str(M)]["silu_mul_separate_us"] = round(t3 * 1e6, 2)
+            res[str(M)]["silu_mul_tflops"] = round(2 * M * N * K / t1 / 1e12, 1)
+        del ws1, ws2, Y1, Y2, X
+    return res
 
 
 def model_quantizer(nv, dev, stream, layers=32, distinct=2):

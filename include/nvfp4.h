@@ -76,7 +76,8 @@ typedef enum nvfp4_op {
   NVFP4_OP_QUANTIZE_ACT = 1,
   NVFP4_OP_GEMM_W4A16 = 2,
   NVFP4_OP_GEMM_W4A4 = 3,
-  NVFP4_OP_LINEAR = 4
+  NVFP4_OP_LINEAR = 4,
+  NVFP4_OP_LINEAR_SILU_MUL = 5
 } nvfp4_op;
 
 #define NVFP4_DEFAULT_DIVISOR 2688.0f /* 6 (E2M1 max) * 448 (E4M3 max) */
@@ -197,6 +198,28 @@ nvfp4_status nvfp4_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma
 nvfp4_status nvfp4_linear(const void* X, int64_t M, const nvfp4_weight* W, void* Y,
                           int out_dtype, void* workspace, size_t workspace_bytes,
                           cudaStream_t stream);
+
+/*
+ * Gated MLP input projection (the survey's next-2 fusion; the pages fuse
+ * elementwise epilogues of other layers the same way): W is the concatenated
+ * gate/up weight [2F, K] (rows [0, F) gate, [F, 2F) up), and
+ *   Y[m, f] = silu(G[m, f]) * U[m, f],  silu(g) = g / (1 + e^-g),
+ * with G = X W_gate^T and U = X W_up^T computed as nvfp4_linear would (same
+ * dispatch by M over the whole [2F, K] weight), in binary32.
+ *   X          in:  device bf16 [M, K]
+ *   W          in:  quantised [2F, K] weight (N = 2F even)
+ *   Y          out: device [M, F] of out_dtype
+ *   workspace  nvfp4_workspace_bytes(NVFP4_OP_LINEAR_SILU_MUL, M, 2F, K) bytes
+ * Above 128 tokens with bf16 output and F % 128 == 0 the CTA-pair W4A4
+ * kernel applies silu(G) * U in its epilogue (CTA 0 of a pair holds 128 gate
+ * rows, CTA 1 the matching up rows), so G and U never reach memory.
+ * Otherwise the GEMM writes fp32 [rows, 2F] into the workspace, 1024 rows at
+ * a time, and a separate kernel applies it; the fused and separate forms
+ * evaluate the same binary32 expression.
+ */
+nvfp4_status nvfp4_linear_silu_mul(const void* X, int64_t M, const nvfp4_weight* W, void* Y,
+                                   int out_dtype, void* workspace, size_t workspace_bytes,
+                                   cudaStream_t stream);
 
 /* Size of the scratch array built into the library for nvfp4_linear_noalloc
  * (32 MiB, held on every GPU that loads the library until the process exits). */

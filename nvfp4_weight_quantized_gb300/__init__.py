@@ -22,7 +22,7 @@ import torch
 __all__ = [
     "NVFP4Error", "NVFP4Weight", "NVFP4Act", "lib", "library_path", "declared_functions",
     "nvfp4_scales_mma_bytes", "nvfp4_workspace_bytes", "nvfp4_quantize_fos", "nvfp4_quantize_act",
-    "nvfp4_gemm_w4a16", "nvfp4_gemm_w4a4", "nvfp4_linear", "nvfp4_linear_noalloc", "nvfp4_set_crossover",
+    "nvfp4_gemm_w4a16", "nvfp4_gemm_w4a4", "nvfp4_linear", "nvfp4_linear_silu_mul", "nvfp4_linear_noalloc", "nvfp4_set_crossover",
     "nvfp4_get_crossover", "nvfp4_set_w4a16_rf_max_m", "nvfp4_get_w4a16_rf_max_m",
     "nvfp4_set_w4a16_sk_max_m", "nvfp4_get_w4a16_sk_max_m", "nvfp4_set_weight_prefetch",
     "nvfp4_get_weight_prefetch", "nvfp4_set_w4a4_cluster", "nvfp4_get_w4a4_cluster", "nvfp4_set_act_fos", "nvfp4_get_act_fos", "nvfp4_get_device_status",
@@ -38,7 +38,7 @@ OK = 0
 ERR_INVALID_ARG, ERR_SHAPE, ERR_ALIGN, ERR_WORKSPACE = 1, 2, 3, 4
 ERR_NONFINITE, ERR_TIMEOUT, ERR_CUDA, ERR_UNSUPPORTED = 5, 6, 7, 8
 OUT_BF16, OUT_F32 = 0, 1
-OP_QUANTIZE_FOS, OP_QUANTIZE_ACT, OP_GEMM_W4A16, OP_GEMM_W4A4, OP_LINEAR = 0, 1, 2, 3, 4
+OP_QUANTIZE_FOS, OP_QUANTIZE_ACT, OP_GEMM_W4A16, OP_GEMM_W4A4, OP_LINEAR, OP_LINEAR_SILU_MUL = 0, 1, 2, 3, 4, 5
 DEFAULT_DIVISOR = 2688.0
 
 
@@ -75,6 +75,7 @@ def lib() -> ctypes.CDLL:
             "nvfp4_gemm_w4a4": (st, [vp, vp, vp, i64, wp, vp, ctypes.c_int, vp, sz, vp]),
             "nvfp4_linear": (st, [vp, i64, wp, vp, ctypes.c_int, vp, sz, vp]),
             "nvfp4_linear_noalloc": (st, [vp, i64, wp, vp, ctypes.c_int, vp]),
+            "nvfp4_linear_silu_mul": (st, [vp, i64, wp, vp, ctypes.c_int, vp, sz, vp]),
             "nvfp4_set_crossover": (st, [i64, i64, i64]),
             "nvfp4_get_crossover": (i64, [i64, i64]),
             "nvfp4_set_w4a16_rf_max_m": (st, [i64]),
@@ -311,6 +312,21 @@ def nvfp4_linear(X: torch.Tensor, W: NVFP4Weight, out_dtype: int = OUT_BF16,
     d = W.descriptor()
     _check(lib().nvfp4_linear(X.data_ptr(), M, ctypes.byref(d), Y.data_ptr(), out_dtype, ws.data_ptr(),
                               ws.numel(), _stream(stream)), "nvfp4_linear")
+    return Y
+
+
+def nvfp4_linear_silu_mul(X: torch.Tensor, W: NVFP4Weight, out_dtype: int = OUT_BF16,
+                          out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                          stream=None) -> torch.Tensor:
+    """Y = silu(X W_gate^T) * (X W_up^T) for a gate/up weight [2F, K] (nvfp4_linear_silu_mul)."""
+    _require_cuda(X, out)
+    M = X.shape[0]
+    Y = _out(M, W.N // 2, out_dtype, X.device, out)
+    ws = workspace if workspace is not None else _workspace(
+        nvfp4_workspace_bytes(OP_LINEAR_SILU_MUL, M, W.N, W.K), X.device)
+    d = W.descriptor()
+    _check(lib().nvfp4_linear_silu_mul(X.data_ptr(), M, ctypes.byref(d), Y.data_ptr(), out_dtype, ws.data_ptr(),
+                                       ws.numel(), _stream(stream)), "nvfp4_linear_silu_mul")
     return Y
 
 

@@ -139,6 +139,11 @@ struct LinearWs {
   size_t codes_off, scales_off, ts_off, quant_off, total;
 };
 
+// Rows of the fp32 [rows, 2F] GEMM output that nvfp4_linear_silu_mul stages
+// in its workspace when silu(G) * U is not fused into the GEMM (a multiple of
+// the 128-row scale tiles, so a chunk's activation scales are contiguous).
+constexpr int64_t kSiluChunkRows = 1024;
+
 LinearWs linear_ws_layout(int64_t M, int64_t K) {
   LinearWs l;
   l.codes_off = 0;
@@ -174,6 +179,10 @@ size_t nvfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
       // sized for the W4A4 branch whatever the current crossover is
       if (M <= 0) return 0;
       return linear_ws_layout(M, K).total;
+    case NVFP4_OP_LINEAR_SILU_MUL:
+      // the linear workspace, then fp32 [min(M, chunk), N] for an unfused silu(G) * U
+      if (M <= 0 || N <= 0) return 0;
+      return linear_ws_layout(M, K).total + align256((size_t)std::min(M, kSiluChunkRows) * (size_t)N * 4);
     default: return 0;
   }
 }
@@ -278,6 +287,67 @@ nvfp4_status nvfp4_linear(const void* X, int64_t M, const nvfp4_weight* W, void*
                        stream);
   if (st != NVFP4_OK) return st;
   return nvfp4_gemm_w4a4(a_codes, a_smma, a_ts, M, W, Y, out_dtype, nullptr, 0, stream);
+}
+
+nvfp4_status nvfp4_linear_silu_mul(const void* X, int64_t M, const nvfp4_weight* W, void* Y, int out_dtype,
+                                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  nvfp4_status st = check_weight(W);
+  if (st != NVFP4_OK) return st;
+  if ((st = check_out_dtype(out_dtype)) != NVFP4_OK) return st;
+  if (W->N % 2 != 0) return fail(NVFP4_ERR_SHAPE, "linear_silu_mul: W needs an even number of rows (gate, up)");
+  if (M < 0 || M > kMaxElems / W->K || M > kMaxElems / W->N) return fail(NVFP4_ERR_SHAPE, "bad M");
+  if (M == 0) return NVFP4_OK;
+  if (X == nullptr || Y == nullptr) return fail(NVFP4_ERR_INVALID_ARG, "X and Y are required");
+  if (!aligned(X, 16) || !aligned(Y, 16)) return fail(NVFP4_ERR_ALIGN, "X and Y must be 16-byte aligned");
+  const int64_t N = W->N, F = N / 2, K = W->K;
+  const LinearWs l = linear_ws_layout(M, K);
+  const size_t need = nvfp4_workspace_bytes(NVFP4_OP_LINEAR_SILU_MUL, M, N, K);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
+    return fail(NVFP4_ERR_WORKSPACE, "linear_silu_mul: workspace missing, not 256-byte aligned or too small");
+  const DeviceInfo* d = nullptr;
+  if ((st = device_info(&d)) != NVFP4_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* y2 = reinterpret_cast<float*>(ws + l.total);  // fp32 [chunk, 2F]
+  const bool f32 = out_dtype == NVFP4_OUT_F32;
+  const size_t out_elt = f32 ? 4 : 2;
+  cudaError_t err;
+  if (M <= nvfp4_get_crossover(N, K) || K < 256) {
+    // W4A16 into fp32, then silu(G) * U
+    for (int64_t r0 = 0; r0 < M; r0 += kSiluChunkRows) {
+      const int64_t mc = std::min(kSiluChunkRows, M - r0);
+      st = nvfp4_gemm_w4a16(static_cast<const uint8_t*>(X) + (size_t)r0 * K * 2, mc, W, y2, NVFP4_OUT_F32,
+                            nullptr, 0, stream);
+      if (st != NVFP4_OK) return st;
+      if ((err = nvfp4::launch_silu_mul(y2, mc, F, static_cast<uint8_t*>(Y) + (size_t)r0 * F * out_elt, f32,
+                                        stream)) != cudaSuccess)
+        return fail_cuda(err, "silu_mul launch");
+    }
+    return NVFP4_OK;
+  }
+  uint8_t* a_codes = ws + l.codes_off;
+  uint8_t* a_smma = ws + l.scales_off;
+  float* a_ts = reinterpret_cast<float*>(ws + l.ts_off);
+  st = quantize_common(X, M, K, NVFP4_DEFAULT_DIVISOR, g_act_fos.load(std::memory_order_relaxed), a_codes, nullptr,
+                       a_smma, a_ts, nullptr, nullptr, ws + l.quant_off, l.total - l.quant_off, stream);
+  if (st != NVFP4_OK) return st;
+  if (!f32 && M > 128 && nvfp4::w4a4_get_cluster_ctas() >= 2) {
+    // silu(G) * U in the epilogue of the CTA-pair kernel
+    err = nvfp4::launch_gemm_w4a4_gate_up(a_codes, a_smma, a_ts, M, W->codes, W->scales_mma, W->tensor_scale, N, K,
+                                          Y, d->status, stream);
+    if (err == cudaSuccess) return NVFP4_OK;
+    if (err != cudaErrorNotSupported) return fail_cuda(err, "gemm_w4a4 gate/up launch");
+  }
+  const size_t ct = (size_t)((K / 16 + 3) / 4);  // scale column tiles per 128-row tile
+  for (int64_t r0 = 0; r0 < M; r0 += kSiluChunkRows) {
+    const int64_t mc = std::min(kSiluChunkRows, M - r0);
+    st = nvfp4_gemm_w4a4(a_codes + (size_t)r0 * (K / 2), a_smma + (size_t)(r0 / 128) * ct * 512, a_ts, mc, W, y2,
+                         NVFP4_OUT_F32, nullptr, 0, stream);
+    if (st != NVFP4_OK) return st;
+    if ((err = nvfp4::launch_silu_mul(y2, mc, F, static_cast<uint8_t*>(Y) + (size_t)r0 * F * out_elt, f32,
+                                      stream)) != cudaSuccess)
+      return fail_cuda(err, "silu_mul launch");
+  }
+  return NVFP4_OK;
 }
 
 nvfp4_status nvfp4_set_crossover(int64_t N, int64_t K, int64_t M_threshold) {

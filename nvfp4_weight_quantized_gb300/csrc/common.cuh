@@ -59,6 +59,15 @@ __device__ __forceinline__ float e2m1_mag_to_f32(uint32_t m) {
   return m < 2u ? (float)m * 0.5f : __uint_as_float((m << 22) + (126u << 23));
 }
 
+// silu(g) * u = g / (1 + e^-g) * u in binary32 with the fast exponential and
+// division intrinsics (relative error a few units in 2^-22 for |g| < 20; for
+// g < -87 the quotient's divisor exceeds 2^126 and the result is 0, the
+// limit).  Shared by the fused gate/up epilogue and the separate kernel, so
+// both give the same bits for the same G and U.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return __fmul_rn(__fdividef(g, __fadd_rn(1.0f, __expf(-g))), u);
+}
+
 // ------------------------------------------------------------ memory ops ---
 
 __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {

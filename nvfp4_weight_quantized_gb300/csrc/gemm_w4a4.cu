@@ -467,7 +467,12 @@ static_assert(kPairSfCol + kPairStages * kPairSfStageCols <= kTmemCols, "TMEM bu
 // kind::mxf4nvf4, E2M1 x E2M1, K-major, N = 256, UE4M3 scales, M = 256
 constexpr uint32_t kPairIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(256 >> 3) << 17) | (2u << 27);
 
-template <int kPairs, bool kF32>
+// kGateUp: W is a gated-MLP input projection [2F, K] (rows [0, F) gate,
+// [F, 2F) up, F % 128 == 0) and the kernel writes Y[m, f] = silu(G) * U for
+// F features: a tile covers 128 features, CTA 0 of the pair staging their
+// gate rows and CTA 1 their up rows, so accumulator column j (< 128) of every
+// row holds G[m, f0 + j] and column 128 + j holds U[m, f0 + j].
+template <int kPairs, bool kF32, bool kGateUp = false>
 __global__ void __launch_bounds__(kPairThreads, 1)
 w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                  const __grid_constant__ CUtensorMap tmap_y, int tma_store, const uint8_t* __restrict__ a_smma,
@@ -485,8 +490,10 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
   const int64_t cl = blockIdx.x / kCtas, ncl = gridDim.x / kCtas;
   const int kb64 = (int)(K / 64);
   const int kt = (kb64 + 3) / 4;
+  static_assert(!kGateUp || (kPairs == 1 && !kF32), "gate/up epilogue: one pair per cluster, bf16 output");
   const int64_t b_row_tiles = (N + 127) / 128;
-  const int64_t n_tiles = (N + 255) / 256;
+  const int64_t F = N / 2;  // features of a gate/up weight
+  const int64_t n_tiles = kGateUp ? F / 128 : (N + 255) / 256;
   const int64_t n_groups = (n_tiles + kPairs - 1) / kPairs;  // a cluster's unit: kPairs adjacent tiles
   const int64_t n_work = ((M + 255) / 256) * n_groups;
 
@@ -518,8 +525,8 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
       for (int64_t w = cl; w < n_work && !failed; w += ncl) {
         const int64_t m_tile = w / n_groups, n_tile = (w - m_tile * n_groups) * kPairs + pidx;
         const int64_t arow = m_tile * 256 + 128 * rank;
-        const int64_t n0 = n_tile * 256;  // past N for the idle pair of a ragged last unit
-        const int64_t brow = n0 + 128 * rank;
+        const int64_t n0 = n_tile * (kGateUp ? 128 : 256);  // past N for the idle pair of a ragged last unit
+        const int64_t brow = kGateUp ? n0 + F * rank : n0 + 128 * rank;
         // a CTA whose A (or B) rows all lie past M (N) loads nothing for them:
         // its accumulator rows (or the tile's columns from that half) are never stored
         const bool has_a = arow < M, has_b = brow < N;
@@ -528,7 +535,7 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         const uint32_t a_bytes = kPairs == 1 ? (has_a ? kABytes : 0)
                                              : (has_a ? kABytes / 2 : 0) + (arow + 64 < M ? kABytes / 2 : 0);
         const int64_t sfb_left = b_row_tiles - n0 / 128;
-        const int nsfb = sfb_left <= 0 ? 0 : sfb_left < 2 ? (int)sfb_left : 2;
+        const int nsfb = kGateUp ? 2 : sfb_left <= 0 ? 0 : sfb_left < 2 ? (int)sfb_left : 2;
         for (int ks = 0; ks < kt; ++ks, ++g) {
           const int s = g % S;
           if (g >= S && !mbar_wait(&sm.empty[s], (uint32_t)(g / S - 1) & 1u)) {
@@ -555,9 +562,13 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             if (has_b) tma_load_2d(sm.b[s], &tmap_b, ks * (BK / 2), (int)brow, &sm.full[s]);
           } else {
             mbar_arrive_expect_tx(&sm.full[s], sf_bytes * nsfb);
-            for (int rt = 0; rt < nsfb; ++rt)
-              bulk_load(sm.sfb[s] + rt * kSfaBytes, b_smma + ((n0 / 128 + rt) * kb64 + 4 * ks) * kScaleTileBytes,
-                        sf_bytes, &sm.full[s]);
+            for (int rt = 0; rt < nsfb; ++rt) {
+              // B rows 128 rt .. of the MMA: the next weight row tile, or for
+              // gate/up the up rows' tile F / 128 further on
+              const int64_t bt = kGateUp ? (n0 + F * rt) / 128 : n0 / 128 + rt;
+              bulk_load(sm.sfb[s] + rt * kSfaBytes, b_smma + (bt * kb64 + 4 * ks) * kScaleTileBytes, sf_bytes,
+                        &sm.full[s]);
+            }
           }
         }
       }
@@ -657,7 +668,7 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
     int t = 0;
     for (int64_t w = cl; w < n_work; w += ncl, ++t) {
       const int64_t m_tile = w / n_groups, n_tile = (w - m_tile * n_groups) * kPairs + pidx;
-      const int64_t m0 = m_tile * 256 + 128 * rank, n0 = n_tile * 256;
+      const int64_t m0 = m_tile * 256 + 128 * rank, n0 = n_tile * (kGateUp ? 128 : 256);
       const int64_t row = m0 + r;
       const bool ok = __all_sync(0xffffffffu, !failed && mbar_wait(&sm.acc_full, (uint32_t)t & 1u));
       if (!ok) {
@@ -665,7 +676,45 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         break;
       }
       fence_after_sync();
-      if (!kF32 && tma_store) {
+      if (kGateUp) {
+        // silu(G) * U for features n0 .. n0 + 127 straight into the staging
+        // buffer (two 128 x 64 bf16 boxes), then the accumulator goes back
+        // and one round of TMA stores writes the tile
+        if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t vg[16], vu[16], p[8];
+          tmem_ld_32x32b_x16(tmem + lane_base + 16 * c, vg);
+          tmem_ld_32x32b_x16(tmem + lane_base + 128 + 16 * c, vu);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            p[i] = bf16x2_rn(silu_mul(__uint_as_float(vg[2 * i]) * alpha, __uint_as_float(vu[2 * i]) * alpha),
+                             silu_mul(__uint_as_float(vg[2 * i + 1]) * alpha,
+                                      __uint_as_float(vu[2 * i + 1]) * alpha));
+          uint8_t* box = sm.ystage + (c >> 2) * (BM * 128) + r * 128;
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int unit = ((c & 3) * 2 + u) ^ (r & 7);
+            *reinterpret_cast<uint4*>(box + unit * 16) = make_uint4(p[4 * u], p[4 * u + 1], p[4 * u + 2], p[4 * u + 3]);
+          }
+        }
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(&sm.acc_free, lead);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+        if (threadIdx.x == 0 && m0 < M) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            asm volatile(
+                "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(&tmap_y),
+                "r"((int)(n0 + 64 * j)), "r"((int)m0), "r"(smem_addr(sm.ystage + j * (BM * 128)))
+                : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+      } else if (!kF32 && tma_store) {
         // Columns 0-127 go straight to the staging buffer (two 128 x 64 bf16
         // boxes, 128-byte swizzle), columns 128-255 into registers as scaled
         // bf16 pairs; then the accumulator goes back to the MMA warp and the
@@ -837,7 +886,7 @@ std::atomic<int> g_cluster_ctas{2};
 // shared-memory request is above half an SM's), as many clusters as fit at
 // once or as there are work units.  cudaErrorNotSupported when no cluster of
 // that shape can be resident.
-template <int kPairs>
+template <int kPairs, bool kGateUp = false>
 cudaError_t launch_pairs(const uint8_t* a_codes, const uint8_t* a_smma, const float* a_ts, int64_t M,
                          const uint8_t* w_codes, const uint8_t* w_smma, const float* w_ts, int64_t N, int64_t K,
                          void* y, bool out_f32, unsigned int* status, cudaStream_t stream) {
@@ -845,11 +894,14 @@ cudaError_t launch_pairs(const uint8_t* a_codes, const uint8_t* a_smma, const fl
   if (!make_map(&ma, a_codes, (uint64_t)M, (uint64_t)K / 2, 128 / kPairs) ||
       !make_map(&mb, w_codes, (uint64_t)N, (uint64_t)K / 2, 128))
     return cudaErrorInvalidValue;
-  int tma_store = (!out_f32 && N % 8 == 0) ? 1 : 0;
+  const int64_t n_out = kGateUp ? N / 2 : N;  // columns of Y
+  int tma_store = (!out_f32 && n_out % 8 == 0) ? 1 : 0;
   memset(&my, 0, sizeof my);
-  if (tma_store && !make_y_map(&my, y, (uint64_t)M, (uint64_t)N)) tma_store = 0;
+  if (tma_store && !make_y_map(&my, y, (uint64_t)M, (uint64_t)n_out)) tma_store = 0;
+  if (kGateUp && !tma_store) return cudaErrorNotSupported;
   const size_t smem = sizeof(PairSmem) + 1024;
   auto kern = out_f32 ? w4a4_pair_kernel<kPairs, true> : w4a4_pair_kernel<kPairs, false>;
+  if constexpr (kGateUp) kern = w4a4_pair_kernel<kPairs, false, true>;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2 * kPairs;
@@ -864,7 +916,7 @@ cudaError_t launch_pairs(const uint8_t* a_codes, const uint8_t* a_smma, const fl
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   // resident clusters per GPU, once per output type (the device is fixed for the process)
-  static int max_clusters[2] = {0, 0};
+  static int max_clusters[2] = {0, 0};  // per instantiation: [output f32]
   static std::once_flag once[2];
   cudaError_t err = cudaSuccess;
   std::call_once(once[out_f32 ? 1 : 0], [&] {
@@ -880,12 +932,23 @@ cudaError_t launch_pairs(const uint8_t* a_codes, const uint8_t* a_smma, const fl
   if (err != cudaSuccess) return err;
   const int mc = max_clusters[out_f32 ? 1 : 0];
   if (mc < 1) return cudaErrorNotSupported;
-  const int64_t work = ((M + 255) / 256) * (((N + 255) / 256 + kPairs - 1) / kPairs);
+  const int64_t tiles_n = kGateUp ? N / 2 / 128 : (N + 255) / 256;
+  const int64_t work = ((M + 255) / 256) * ((tiles_n + kPairs - 1) / kPairs);
   cfg.gridDim = dim3((unsigned)(2 * kPairs * std::min<int64_t>(work, mc)));
   return cudaLaunchKernelEx(&cfg, kern, ma, mb, my, tma_store, a_smma, w_smma, a_ts, w_ts, M, N, K, y, status);
 }
 
 }  // namespace
+
+cudaError_t launch_gemm_w4a4_gate_up(const uint8_t* a_codes, const uint8_t* a_scales_mma, const float* a_ts,
+                                     int64_t M, const uint8_t* w_codes, const uint8_t* w_scales_mma,
+                                     const float* w_ts, int64_t N, int64_t K, void* y, unsigned int* status,
+                                     cudaStream_t stream) {
+  if (M <= 0) return cudaSuccess;
+  if (N % 256 != 0 || K < BK || K % 64 != 0 || M > INT32_MAX || N > INT32_MAX) return cudaErrorNotSupported;
+  return launch_pairs<1, true>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, false, status,
+                               stream);
+}
 
 bool w4a4_set_cluster_ctas(int ctas) {
   if (ctas != 1 && ctas != 2 && ctas != 4) return false;

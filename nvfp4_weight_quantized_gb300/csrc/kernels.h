@@ -49,6 +49,16 @@ cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma
                              int64_t M, const uint8_t* w_codes, const uint8_t* w_scales_mma,
                              const float* w_ts, int64_t N, int64_t K, void* y, bool out_f32,
                              unsigned int* status, int num_sms, cudaStream_t stream);
+// W4A4 on a gate/up weight [2F, K] with silu(G) * U applied in the epilogue
+// of the CTA-pair kernel: Y bf16 [M, F].  cudaErrorNotSupported unless
+// F % 128 == 0 and a pair of CTAs can be resident.
+cudaError_t launch_gemm_w4a4_gate_up(const uint8_t* a_codes, const uint8_t* a_scales_mma, const float* a_ts,
+                                     int64_t M, const uint8_t* w_codes, const uint8_t* w_scales_mma,
+                                     const float* w_ts, int64_t N, int64_t K, void* y, unsigned int* status,
+                                     cudaStream_t stream);
+// Y[m, f] = silu(y2[m, f]) * y2[m, F + f] for y2 fp32 [M, 2F]; Y [M, F].
+cudaError_t launch_silu_mul(const float* y2, int64_t M, int64_t F, void* y, bool out_f32, cudaStream_t stream);
+
 // CTAs per cluster for M > 128: 4 (two CTA pairs sharing A rows by TMA
 // multicast), 2 (one pair, cta_group::2 MMAs on 256 x 256 tiles) or 1 (single
 // CTAs on 128 x 256 tiles).  The setter rejects anything else.

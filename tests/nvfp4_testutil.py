@@ -104,3 +104,36 @@ def assert_gemm_close(y: np.ndarray, ref: np.ndarray, bf16: bool, what: str = ""
         raise AssertionError(f"{what}: {int(bad.sum())} elements outside tolerance "
                              f"(worst normwise rel {worst:.3g}); e.g. {detail}")
     return worst
+
+
+# silu(G) * U: with |dG| <= GEMM_REL_TOL * max|G_row| and likewise for U (the
+# GEMM bound), |d(silu(g) u)| <= |silu'(g)| |dg| |u| + |silu(g)| |du| + ...
+# <= (1.1 + 1) * GEMM_REL_TOL * max|G_row| * max|U_row|, since
+# silu'(g) lies in [-0.1, 1.1] and |silu(g)| <= |g|; the binary32 silu adds a
+# few units of 2^-22 of |silu(g) u|.
+SILU_MUL_REL_TOL = 2.2 * GEMM_REL_TOL
+
+
+def silu_mul_ref(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """binary64 silu(g) * u = g / (1 + e^-g) * u."""
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g)) * u
+
+
+def assert_silu_mul_close(y: np.ndarray, g: np.ndarray, u: np.ndarray, bf16: bool, what: str = ""):
+    """y against silu(g) * u elementwise, g and u the binary64 GEMM references."""
+    ref = silu_mul_ref(g, u)
+    assert y.shape == ref.shape, (y.shape, ref.shape)
+    assert np.all(np.isfinite(y)), f"{what}: non-finite output"
+    scale = np.max(np.abs(g), axis=1, keepdims=True) * np.max(np.abs(u), axis=1, keepdims=True)
+    err = np.abs(y - ref)
+    allow = SILU_MUL_REL_TOL * scale + (bf16_half_ulp(ref) if bf16 else 0.0)
+    bad = err > allow
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        detail = ", ".join(f"[{i},{j}] y={y[i, j]!r} ref={ref[i, j]!r}" for i, j in idx)
+        raise AssertionError(f"{what}: {int(bad.sum())} elements outside tolerance; e.g. {detail}")
+    with np.errstate(divide="ignore", invalid="ignore"):
+        rel = np.where(scale > 0, np.max(np.maximum(err - (bf16_half_ulp(ref) if bf16 else 0.0), 0), axis=1,
+                                         keepdims=True) / scale, 0.0)
+    return float(np.max(rel)) if rel.size else 0.0

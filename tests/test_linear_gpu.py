@@ -6,7 +6,8 @@ import pytest
 
 import oracle
 import synth
-from nvfp4_testutil import THREADS, assert_gemm_close, oracle_w4a16, oracle_w4a4, to_dev, y_to_np
+from nvfp4_testutil import (THREADS, assert_gemm_close, assert_silu_mul_close, oracle_w4a16, oracle_w4a4,
+                            to_dev, y_to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -99,3 +100,70 @@ def test_linear_small_k_always_takes_w4a16():
 def test_default_crossover_is_sane():
     c = nv.nvfp4_get_crossover()
     assert 1 <= c <= 4096
+
+
+def _gate_up_refs(x, wref, path_w4a4, m_rows=None):
+    """binary64 G and U for a gate/up weight [2F, K] on the given path."""
+    if path_w4a4:
+        aref = oracle.quantize_rows(x, oracle.tensor_scale(x), False, THREADS)
+        y = oracle_w4a4(aref["codes"], aref["scales"], aref["ts"], wref["codes"], wref["scales"], wref["ts"],
+                        m_rows=m_rows)
+    else:
+        y = oracle_w4a16(x if m_rows is None else x[m_rows], wref["codes"], wref["scales"], wref["ts"])
+    F = y.shape[1] // 2
+    return y[:, :F], y[:, F:]
+
+
+@pytest.mark.parametrize("F", [256, 384, 200])
+def test_linear_silu_mul(F):
+    """Gated MLP projection against the oracle on both paths: W4A16 (M <= 40)
+    with the separate silu kernel, W4A4 with silu(G) * U fused into the
+    CTA-pair kernel's epilogue (bf16, M > 128, F % 128 == 0) or separate
+    (fp32 output, M <= 128, F = 200, single-CTA kernels)."""
+    K = 1024
+    N = 2 * F
+    w = synth.weight_normal(N, K, seed=F + 17, outlier_frac=0.01)
+    W = nv.nvfp4_quantize_fos(to_dev(w))
+    wref = oracle.quantize_rows(w, oracle.tensor_scale(w), True, THREADS)
+    old = nv.nvfp4_get_crossover(N, K)
+    saved_cl = nv.nvfp4_get_w4a4_cluster()
+    nv.nvfp4_set_crossover(N, K, 40)
+    try:
+        for M in (1, 40, 41, 130, 300):
+            x = synth.act_student_t(M, K, seed=900 + M)
+            X = to_dev(x)
+            g, u = _gate_up_refs(x, wref, M > 40)
+            for od in (nv.OUT_BF16, nv.OUT_F32):
+                for ctas in ((2, 1) if M > 128 else (2,)):
+                    nv.nvfp4_set_w4a4_cluster(ctas)
+                    y = y_to_np(nv.nvfp4_linear_silu_mul(X, W, od))
+                    torch.cuda.synchronize()
+                    assert_silu_mul_close(y, g, u, bf16=od == nv.OUT_BF16, what=f"F={F} M={M} od={od} ctas={ctas}")
+        assert nv.nvfp4_get_device_status() == 0
+    finally:
+        nv.nvfp4_set_w4a4_cluster(saved_cl)
+        nv.nvfp4_set_crossover(N, K, old)
+
+
+def test_linear_silu_mul_chunks_and_fused_match():
+    """More rows than one 1024-row workspace chunk on the separate path (fp32
+    output), sampled against the oracle; the fused bf16 result equals the
+    separate path's bf16 rounding of the same binary32 expression within one
+    bf16 step."""
+    F, K, M = 256, 512, 1100
+    N = 2 * F
+    w = synth.weight_normal(N, K, seed=4242, outlier_frac=0.01)
+    W = nv.nvfp4_quantize_fos(to_dev(w))
+    wref = oracle.quantize_rows(w, oracle.tensor_scale(w), True, THREADS)
+    x = synth.act_student_t(M, K, seed=4243)
+    X = to_dev(x)
+    rows = np.array(sorted(set(range(0, M, 37)) | {0, 1023, 1024, M - 1}))
+    g, u = _gate_up_refs(x, wref, True, m_rows=rows)
+    y32 = y_to_np(nv.nvfp4_linear_silu_mul(X, W, nv.OUT_F32))
+    assert_silu_mul_close(y32[rows], g, u, bf16=False, what="chunked fp32")
+    fused = nv.nvfp4_linear_silu_mul(X, W, nv.OUT_BF16).float()
+    sep = torch.from_numpy(y32).cuda().to(torch.bfloat16).float()
+    torch.cuda.synchronize()
+    diff = (fused - sep).abs()
+    step = sep.abs() * 2.0 ** -7 + 2.0 ** -133
+    assert bool((diff <= step).all()), float((diff / step).max())
