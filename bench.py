@@ -332,6 +332,7 @@ def run_ours(args):
         detail["model_quantizer"] = model_quantizer(nv, dev, stream)
         detail["act_fos"] = act_fos_compare(nv, dev, stream)
         detail["gate_up_silu_mul"] = gate_up_bench(nv, dev, stream)
+        detail["qat_step"] = qat_bench(nv, dev, stream)
 
     e2e = measure_e2e(nv, dev, stream, w_bits, args, step_bytes, paths) if rank == 0 else None
 
@@ -507,6 +508,46 @@ def gate_up_bench(nv, dev, stream):
             res[str(M)]["silu_mul_tflops"] = round(2 * M * N * K / t1 / 1e12, 1)
         del ws1, ws2, Y1, Y2, X
     return res
+
+
+def qat_bench(nv, dev, stream, M=4096):
+    """One quantisation-aware training step of the prefill linear (W [11008,
+    4096], X [M, 4096]): the FP4 forward (activation quantisation + W4A4,
+    weight quantised once) and the straight-through backward (bf16 dequantise
+    of W and X_hat, dX = dY W_hat and dW = dY^T X_hat on cuBLAS)."""
+    import torch
+    bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
+    qp = nv.nvfp4_quantize_fos(bf(synth.prefill_weight()), logical_scales=False, choice=False)
+    N, K = qp.N, qp.K
+    X = bf(synth.prefill_act(M))
+    dY = (torch.randn(M, N, device=dev, generator=torch.Generator(device=dev).manual_seed(7))).to(torch.bfloat16)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    A = nv.nvfp4_quantize_act(X)
+
+    def fwd():
+        nv.nvfp4_gemm_w4a4(nv.nvfp4_quantize_act(X, stream=stream), qp, out=Y, stream=stream)
+
+    def bwd():
+        nv.nvfp4_qat_backward(dY, qp, A, stream=stream)
+
+    def timed(fn, reps=5):
+        with torch.cuda.stream(stream):
+            fn()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) * 1e-3 / reps
+
+    tf, tb = timed(fwd), timed(bwd)
+    fl = 2.0 * M * N * K
+    return {"M": M, "N": N, "K": K, "forward_us": round(tf * 1e6, 1), "forward_tflops": round(fl / tf / 1e12, 1),
+            "backward_us": round(tb * 1e6, 1), "backward_tflops": round(2 * fl / tb / 1e12, 1),
+            "timing": "eager calls (the backward's cuBLAS handle is not captured), CUDA events"}
 
 
 def model_quantizer(nv, dev, stream, layers=32, distinct=2):

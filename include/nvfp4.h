@@ -77,7 +77,8 @@ typedef enum nvfp4_op {
   NVFP4_OP_GEMM_W4A16 = 2,
   NVFP4_OP_GEMM_W4A4 = 3,
   NVFP4_OP_LINEAR = 4,
-  NVFP4_OP_LINEAR_SILU_MUL = 5
+  NVFP4_OP_LINEAR_SILU_MUL = 5,
+  NVFP4_OP_QAT_BACKWARD = 6
 } nvfp4_op;
 
 #define NVFP4_DEFAULT_DIVISOR 2688.0f /* 6 (E2M1 max) * 448 (E4M3 max) */
@@ -220,6 +221,38 @@ nvfp4_status nvfp4_linear(const void* X, int64_t M, const nvfp4_weight* W, void*
 nvfp4_status nvfp4_linear_silu_mul(const void* X, int64_t M, const nvfp4_weight* W, void* Y,
                                    int out_dtype, void* workspace, size_t workspace_bytes,
                                    cudaStream_t stream);
+
+/*
+ * NVFP4 -> bf16: out[r, k] = bf16(binary32(value(code) * value(scale) * ts)),
+ * the product value(code) * value(scale) exact, one binary32 rounding for the
+ * tensor scale, then round to nearest even bf16.
+ *   codes [rows, K/2], scales_mma (MMA tiling), tensor_scale (1 float): device
+ *   out   device bf16 [rows, K]
+ */
+nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales_mma,
+                              const float* tensor_scale, int64_t rows, int64_t K, void* out,
+                              cudaStream_t stream);
+
+/*
+ * Backward pass of the FP4-forward linear layer Y = X_hat W_hat^T for
+ * quantisation-aware training ("SOAR 2026 Recap ...", section "3. EAGLE-3
+ * speculative decoding and hybrid architecture adaptation", paragraph
+ * "NVFP4 QAT": the forward GEMM runs in FP4, nvfp4_gemm_w4a4 here, and the
+ * gradients pass straight through the quantisers to bf16 master weights):
+ *   dX = dY W_hat     (bf16 [M, K]; skipped if dX is NULL)
+ *   dW = dY^T X_hat   (fp32 [N, K]; skipped if dW is NULL)
+ * with W_hat, X_hat the nvfp4_dequantize bf16 values of W and of the
+ * quantised activations (a_codes, a_scales_mma, a_tensor_scale from
+ * nvfp4_quantize_act or nvfp4_quantize_fos), fp32 accumulation (cuBLAS).
+ *   dY         in: device bf16 [M, N]
+ *   workspace  nvfp4_workspace_bytes(NVFP4_OP_QAT_BACKWARD, M, N, K) bytes
+ * Not capturable in a CUDA graph (the library's cuBLAS handle is created on
+ * first use and shared, under a lock, by all callers on the device).
+ */
+nvfp4_status nvfp4_qat_backward(const void* dY, int64_t M, const nvfp4_weight* W,
+                                const uint8_t* a_codes, const uint8_t* a_scales_mma,
+                                const float* a_tensor_scale, void* dX, void* dW, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
 
 /* Size of the scratch array built into the library for nvfp4_linear_noalloc
  * (32 MiB, held on every GPU that loads the library until the process exits). */

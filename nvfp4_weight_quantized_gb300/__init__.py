@@ -22,7 +22,8 @@ import torch
 __all__ = [
     "NVFP4Error", "NVFP4Weight", "NVFP4Act", "lib", "library_path", "declared_functions",
     "nvfp4_scales_mma_bytes", "nvfp4_workspace_bytes", "nvfp4_quantize_fos", "nvfp4_quantize_act",
-    "nvfp4_gemm_w4a16", "nvfp4_gemm_w4a4", "nvfp4_linear", "nvfp4_linear_silu_mul", "nvfp4_linear_noalloc", "nvfp4_set_crossover",
+    "nvfp4_gemm_w4a16", "nvfp4_gemm_w4a4", "nvfp4_linear", "nvfp4_linear_silu_mul", "nvfp4_linear_noalloc",
+    "nvfp4_dequantize", "nvfp4_qat_backward", "nvfp4_set_crossover",
     "nvfp4_get_crossover", "nvfp4_set_w4a16_rf_max_m", "nvfp4_get_w4a16_rf_max_m",
     "nvfp4_set_w4a16_sk_max_m", "nvfp4_get_w4a16_sk_max_m", "nvfp4_set_weight_prefetch",
     "nvfp4_get_weight_prefetch", "nvfp4_set_w4a4_cluster", "nvfp4_get_w4a4_cluster", "nvfp4_set_act_fos", "nvfp4_get_act_fos", "nvfp4_get_device_status",
@@ -38,7 +39,8 @@ OK = 0
 ERR_INVALID_ARG, ERR_SHAPE, ERR_ALIGN, ERR_WORKSPACE = 1, 2, 3, 4
 ERR_NONFINITE, ERR_TIMEOUT, ERR_CUDA, ERR_UNSUPPORTED = 5, 6, 7, 8
 OUT_BF16, OUT_F32 = 0, 1
-OP_QUANTIZE_FOS, OP_QUANTIZE_ACT, OP_GEMM_W4A16, OP_GEMM_W4A4, OP_LINEAR, OP_LINEAR_SILU_MUL = 0, 1, 2, 3, 4, 5
+OP_QUANTIZE_FOS, OP_QUANTIZE_ACT, OP_GEMM_W4A16, OP_GEMM_W4A4, OP_LINEAR, OP_LINEAR_SILU_MUL, OP_QAT_BACKWARD = \
+    0, 1, 2, 3, 4, 5, 6
 DEFAULT_DIVISOR = 2688.0
 
 
@@ -76,6 +78,8 @@ def lib() -> ctypes.CDLL:
             "nvfp4_linear": (st, [vp, i64, wp, vp, ctypes.c_int, vp, sz, vp]),
             "nvfp4_linear_noalloc": (st, [vp, i64, wp, vp, ctypes.c_int, vp]),
             "nvfp4_linear_silu_mul": (st, [vp, i64, wp, vp, ctypes.c_int, vp, sz, vp]),
+            "nvfp4_dequantize": (st, [vp, vp, vp, i64, i64, vp, vp]),
+            "nvfp4_qat_backward": (st, [vp, i64, wp, vp, vp, vp, vp, vp, vp, sz, vp]),
             "nvfp4_set_crossover": (st, [i64, i64, i64]),
             "nvfp4_get_crossover": (i64, [i64, i64]),
             "nvfp4_set_w4a16_rf_max_m": (st, [i64]),
@@ -345,3 +349,34 @@ def nvfp4_linear_noalloc(X: torch.Tensor, W: NVFP4Weight, out_dtype: int = OUT_B
     _check(lib().nvfp4_linear_noalloc(X.data_ptr(), M, ctypes.byref(d), Y.data_ptr(), out_dtype,
                                       _stream(stream)), "nvfp4_linear_noalloc")
     return Y
+
+
+def nvfp4_dequantize(codes: torch.Tensor, scales_mma: torch.Tensor, tensor_scale: torch.Tensor, rows: int, K: int,
+                     out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """NVFP4 [rows, K] -> bf16 [rows, K] (nvfp4_dequantize)."""
+    _require_cuda(codes, out)
+    Y = out if out is not None else torch.empty((rows, K), dtype=torch.bfloat16, device=codes.device)
+    _check(lib().nvfp4_dequantize(codes.data_ptr(), scales_mma.data_ptr(), tensor_scale.data_ptr(), rows, K,
+                                  Y.data_ptr(), _stream(stream)), "nvfp4_dequantize")
+    return Y
+
+
+def nvfp4_qat_backward(dY: torch.Tensor, W: NVFP4Weight, A: Optional[NVFP4Act], want_dx: bool = True,
+                       want_dw: bool = True, stream=None):
+    """(dX bf16 [M, K], dW fp32 [N, K]) of the FP4-forward linear Y = X_hat W_hat^T
+    with straight-through gradients (nvfp4_qat_backward); None for a skipped one."""
+    _require_cuda(dY)
+    M = dY.shape[0]
+    dev = dY.device
+    dX = torch.empty((M, W.K), dtype=torch.bfloat16, device=dev) if want_dx else None
+    dW = torch.empty((W.N, W.K), dtype=torch.float32, device=dev) if want_dw else None
+    ws = _workspace(nvfp4_workspace_bytes(OP_QAT_BACKWARD, M, W.N, W.K), dev)
+    d = W.descriptor()
+    _check(lib().nvfp4_qat_backward(dY.data_ptr(), M, ctypes.byref(d),
+                                    A.codes.data_ptr() if A is not None else None,
+                                    A.scales_mma.data_ptr() if A is not None else None,
+                                    A.tensor_scale.data_ptr() if A is not None else None,
+                                    dX.data_ptr() if dX is not None else None,
+                                    dW.data_ptr() if dW is not None else None, ws.data_ptr(), ws.numel(),
+                                    _stream(stream)), "nvfp4_qat_backward")
+    return dX, dW

@@ -179,6 +179,10 @@ size_t nvfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
       // sized for the W4A4 branch whatever the current crossover is
       if (M <= 0) return 0;
       return linear_ws_layout(M, K).total;
+    case NVFP4_OP_QAT_BACKWARD:
+      // bf16 W_hat [N, K] and X_hat [M, K]
+      if (M <= 0 || N <= 0) return 0;
+      return align256((size_t)N * (size_t)K * 2) + align256((size_t)M * (size_t)K * 2);
     case NVFP4_OP_LINEAR_SILU_MUL:
       // the linear workspace, then fp32 [min(M, chunk), N] for an unfused silu(G) * U
       if (M <= 0 || N <= 0) return 0;
@@ -346,6 +350,56 @@ nvfp4_status nvfp4_linear_silu_mul(const void* X, int64_t M, const nvfp4_weight*
     if ((err = nvfp4::launch_silu_mul(y2, mc, F, static_cast<uint8_t*>(Y) + (size_t)r0 * F * out_elt, f32,
                                       stream)) != cudaSuccess)
       return fail_cuda(err, "silu_mul launch");
+  }
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales_mma, const float* tensor_scale,
+                              int64_t rows, int64_t K, void* out, cudaStream_t stream) {
+  if (codes == nullptr || scales_mma == nullptr || tensor_scale == nullptr || out == nullptr)
+    return fail(NVFP4_ERR_INVALID_ARG, "dequantize: codes, scales_mma, tensor_scale and out are required");
+  if (rows < 0 || K < 16 || K % 16 != 0 || rows > kMaxElems / K)
+    return fail(NVFP4_ERR_SHAPE, "dequantize: need rows >= 0, K >= 16, K % 16 == 0");
+  if (!aligned(codes, 16) || !aligned(scales_mma, 16) || !aligned(tensor_scale, 4) || !aligned(out, 16))
+    return fail(NVFP4_ERR_ALIGN, "dequantize: pointers must be 16-byte aligned");
+  if (rows == 0) return NVFP4_OK;
+  nvfp4_status st;
+  const DeviceInfo* d = nullptr;
+  if ((st = device_info(&d)) != NVFP4_OK) return st;
+  const cudaError_t err = nvfp4::launch_dequant_bf16(codes, scales_mma, tensor_scale, rows, K, out, d->num_sms, stream);
+  if (err != cudaSuccess) return fail_cuda(err, "dequantize launch");
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_qat_backward(const void* dY, int64_t M, const nvfp4_weight* W, const uint8_t* a_codes,
+                                const uint8_t* a_scales_mma, const float* a_tensor_scale, void* dX, void* dW,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  nvfp4_status st = check_weight(W);
+  if (st != NVFP4_OK) return st;
+  const int64_t N = W->N, K = W->K;
+  if (M < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX || M > kMaxElems / K || M > kMaxElems / N)
+    return fail(NVFP4_ERR_SHAPE, "qat_backward: bad M");
+  if (M == 0 || (dX == nullptr && dW == nullptr)) return NVFP4_OK;
+  if (dY == nullptr || (dW != nullptr && (a_codes == nullptr || a_scales_mma == nullptr || a_tensor_scale == nullptr)))
+    return fail(NVFP4_ERR_INVALID_ARG, "qat_backward: dY (and the quantised activations for dW) are required");
+  if (!aligned(dY, 16) || (dX != nullptr && !aligned(dX, 16)) || (dW != nullptr && !aligned(dW, 16)))
+    return fail(NVFP4_ERR_ALIGN, "qat_backward: pointers must be 16-byte aligned");
+  const size_t wbytes = align256((size_t)N * (size_t)K * 2);
+  if (workspace == nullptr || !aligned(workspace, 256) ||
+      workspace_bytes < nvfp4_workspace_bytes(NVFP4_OP_QAT_BACKWARD, M, N, K))
+    return fail(NVFP4_ERR_WORKSPACE, "qat_backward: workspace missing, not 256-byte aligned or too small");
+  uint8_t* w_hat = static_cast<uint8_t*>(workspace);
+  uint8_t* x_hat = w_hat + wbytes;
+  if (dX != nullptr && (st = nvfp4_dequantize(W->codes, W->scales_mma, W->tensor_scale, N, K, w_hat, stream)) !=
+                           NVFP4_OK)
+    return st;
+  if (dW != nullptr &&
+      (st = nvfp4_dequantize(a_codes, a_scales_mma, a_tensor_scale, M, K, x_hat, stream)) != NVFP4_OK)
+    return st;
+  const int bst = nvfp4::qat_backward_gemms(dY, w_hat, x_hat, M, N, K, dX, dW, stream);
+  if (bst != 0) {
+    nvfp4::set_last_error("qat_backward: cuBLAS GEMM failed");
+    return NVFP4_ERR_CUDA;
   }
   return NVFP4_OK;
 }

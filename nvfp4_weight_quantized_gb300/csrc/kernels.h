@@ -59,6 +59,14 @@ cudaError_t launch_gemm_w4a4_gate_up(const uint8_t* a_codes, const uint8_t* a_sc
 // Y[m, f] = silu(y2[m, f]) * y2[m, F + f] for y2 fp32 [M, 2F]; Y [M, F].
 cudaError_t launch_silu_mul(const float* y2, int64_t M, int64_t F, void* y, bool out_f32, cudaStream_t stream);
 
+// NVFP4 [R, K] (codes, MMA-tiled scales, device tensor scale) -> bf16 [R, K].
+cudaError_t launch_dequant_bf16(const uint8_t* codes, const uint8_t* scales_mma, const float* ts, int64_t R,
+                                int64_t K, void* out, int num_sms, cudaStream_t stream);
+// dX = dY W_hat (bf16 [M, K], skipped if null) and dW = dY^T X_hat (fp32
+// [N, K], skipped if null) on cuBLAS; 0 or a cublasStatus_t.
+int qat_backward_gemms(const void* dy, const void* w_hat, const void* x_hat, int64_t M, int64_t N, int64_t K,
+                       void* dx, void* dw, cudaStream_t stream);
+
 // CTAs per cluster for M > 128: 4 (two CTA pairs sharing A rows by TMA
 // multicast), 2 (one pair, cta_group::2 MMAs on 256 x 256 tiles) or 1 (single
 // CTAs on 128 x 256 tiles).  The setter rejects anything else.

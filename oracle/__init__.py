@@ -8,7 +8,9 @@ for the GEMM references); this module compiles it with gcc and wraps it with
 ctypes + numpy.
 
 Method sources (web pages about the SOAR 2026 inference contest):
-  * "SOAR 2026 Recap ...", section "1. Quantization and GEMM dispatch";
+  * "SOAR 2026 Recap ...", section "1. Quantization and GEMM dispatch", and
+    section "3. EAGLE-3 speculative decoding ..." (NVFP4 QAT, for the
+    dequantisation and straight-through gradients);
   * "SOAR Weekly Champion Notes 07 ... NVFP4 Quantization Improvements",
     sections "01 Background" and "02 FourOverSix".
 """
@@ -93,6 +95,8 @@ def _load():
         lib.oracle_gemm_w4a4.argtypes = [u8p, u8p, ctypes.c_float, i64, u8p, u8p, ctypes.c_float,
                                          i64, i64, f64p]
         lib.oracle_gemm_w4a4.restype = ctypes.c_int
+        lib.oracle_dequant_bf16.argtypes = [u8p, u8p, ctypes.c_float, i64, i64, u16p]
+        lib.oracle_dequant_bf16.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -289,3 +293,31 @@ def gemm_w4a4(a_codes, a_scales, a_ts, w_codes, w_scales, w_ts) -> np.ndarray:
     if st:
         raise OracleError(st)
     return y
+
+
+def dequant_bf16(codes: np.ndarray, scales: np.ndarray, ts: float) -> np.ndarray:
+    """NVFP4 [R, K] (codes [R, K/2], logical scales [R, K/16]) -> bf16 bits,
+    value(code) * value(scale) exact, times ts rounded to binary32, then to
+    bfloat16 (the operand of the QAT backward's bf16 GEMMs)."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    R, K = codes.shape[0], codes.shape[1] * 2
+    out = np.zeros((R, K), np.uint16)
+    st = _load().oracle_dequant_bf16(_ptr(codes, ctypes.c_uint8),
+                                     _ptr(np.ascontiguousarray(scales, dtype=np.uint8), ctypes.c_uint8), ts,
+                                     R, K, _ptr(out, ctypes.c_uint16))
+    if st:
+        raise OracleError(st)
+    return out
+
+
+def qat_backward(dy_bits: np.ndarray, w_hat_bits: np.ndarray, x_hat_bits: np.ndarray):
+    """Gradients of Y = X_hat W_hat^T under the straight-through estimator
+    ("SOAR 2026 Recap ...", section "3. EAGLE-3 speculative decoding and
+    hybrid architecture adaptation", paragraph "NVFP4 QAT": the FP4 forward's
+    gradients pass straight through to the bf16 master weights): dX = dY W_hat and
+    dW = dY^T X_hat, binary64 products (numpy matmul) of the bf16 operands.
+    dy [M, N], w_hat [N, K], x_hat [M, K] as bf16 bits."""
+    dy = bf16_to_f32(dy_bits).astype(np.float64)
+    w = bf16_to_f32(w_hat_bits).astype(np.float64)
+    x = bf16_to_f32(x_hat_bits).astype(np.float64)
+    return dy @ w, dy.T @ x

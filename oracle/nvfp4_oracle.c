@@ -345,3 +345,38 @@ int oracle_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, float a_ts
     }
   return OR_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Dequantisation to bf16 (the operand of the QAT backward GEMMs)            */
+/* ------------------------------------------------------------------------ */
+
+/* Round a finite binary32 to bfloat16, to nearest, ties to the even bit
+ * pattern: the 16 dropped bits are compared with half of the last kept bit. */
+static uint16_t bf16_round(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  uint32_t kept = u >> 16, dropped = u & 0xFFFFu;
+  if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u))) kept += 1u;
+  return (uint16_t)kept;
+}
+
+/* "SOAR 2026 Recap ...", section "3. EAGLE-3 speculative decoding and hybrid
+ * architecture adaptation", paragraph "NVFP4 QAT": the draft's forward GEMM
+ * runs in FP4 and its gradients go straight through to bf16 master weights,
+ * so the backward GEMMs take bf16 operands.  Reading: its NVFP4 operand is taken to
+ * bf16 in two steps, value(code) * value(scale) (exact: at most 2 + 4
+ * significant bits) times the tensor scale rounded once to binary32, then
+ * rounded to bfloat16.  codes [R, K/2], scales logical [R, K/16]. */
+int oracle_dequant_bf16(const uint8_t* codes, const uint8_t* scales, float ts, int64_t R, int64_t K,
+                        uint16_t* out) {
+  if (R < 0 || K <= 0 || K % 16 != 0) return OR_ERR_SHAPE;
+  for (int64_t r = 0; r < R; ++r)
+    for (int64_t k = 0; k < K; ++k) {
+      uint8_t byte = codes[r * (K / 2) + k / 2];
+      uint8_t code = (k & 1) ? (byte >> 4) : (byte & 15);
+      float vs = (float)(oracle_e2m1_value(code) * oracle_e4m3_value(scales[r * (K / 16) + k / 16]));
+      float q = vs * ts; /* binary32, one rounding */
+      out[r * K + k] = bf16_round(q);
+    }
+  return OR_OK;
+}

@@ -402,3 +402,83 @@ def test_fos_error_never_worse_than_m6_on_a_tensor():
             sse_m6 += r["sse6"]
     assert sse_fos <= sse_m6
     assert np.sum((wf - deq) ** 2) == pytest.approx(sse_fos, rel=1e-5)
+
+
+# ------------------------------------------- dequantisation and QAT backward ---
+
+# E2M1 magnitudes as the pages print them (codes 0..7); sign bit 3
+_E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def _e4m3(byte: int) -> float:
+    """E4M3 by its definition (bias 7, subnormals 0.m * 2^-6)."""
+    e, m = (byte >> 3) & 15, byte & 7
+    return (m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def _exact_dequant(codes, scales, ts):
+    R, K = codes.shape[0], codes.shape[1] * 2
+    out = np.zeros((R, K))
+    for r in range(R):
+        for k in range(K):
+            c = (codes[r, k // 2] >> (4 * (k & 1))) & 15
+            v = _E2M1[c & 7] * (-1.0 if c & 8 else 1.0)
+            out[r, k] = v * _e4m3(int(scales[r, k // 16])) * ts
+    return out
+
+
+def test_dequant_bf16_exact_when_representable():
+    """With ts a power of two every value(code) * value(scale) * ts has at
+    most 6 significant bits, so its bf16 is exact: the oracle must return it."""
+    rng = np.random.default_rng(11)
+    codes = rng.integers(0, 256, size=(6, 32), dtype=np.uint8)
+    scales = rng.integers(0, 0x7F, size=(6, 4), dtype=np.uint8)  # below the NaN pattern
+    for ts in (1.0, 2.0 ** -10, 2.0 ** 5):
+        got = synth.bf16_bits_to_f32(oracle.dequant_bf16(codes, scales, ts)).astype(np.float64)
+        assert np.array_equal(got, _exact_dequant(codes, scales, ts))
+
+
+def test_dequant_bf16_rounding_bound():
+    """For any tensor scale the result is the exact value rounded twice
+    (binary32 then bf16): within half a bf16 step plus 2^-24 relative, and
+    monotone in the exact value within a row."""
+    rng = np.random.default_rng(12)
+    codes = rng.integers(0, 256, size=(4, 64), dtype=np.uint8)
+    scales = rng.integers(0x08, 0x7F, size=(4, 8), dtype=np.uint8)
+    for ts in (0.0123456789, 3.3e-5, 171.7):
+        ts32 = float(np.float32(ts))
+        exact = _exact_dequant(codes, scales, ts32)
+        got = synth.bf16_bits_to_f32(oracle.dequant_bf16(codes, scales, ts32)).astype(np.float64)
+        err = np.abs(got - exact)
+        assert np.all(err <= np.abs(exact) * (2.0 ** -8 + 2.0 ** -24) + 1e-300)
+        o = np.argsort(exact, axis=None, kind="stable")
+        assert np.all(np.diff(got.reshape(-1)[o]) >= 0)
+
+
+def test_dequant_bf16_agrees_with_gemm_oracle():
+    """Against the GEMM oracle's own binary64 dequantisation (unit-vector
+    activations pick out W_hat): equal up to the two roundings."""
+    w = synth.weight_normal(8, 64, seed=13, outlier_frac=0.05)
+    q = oracle.quantize_fos(w)
+    eye = synth.f32_to_bf16_bits(np.eye(64, dtype=np.float32))
+    w_hat = oracle.gemm_w4a16(eye, q["codes"], q["scales"], q["ts"]).T  # [8, 64]
+    got = synth.bf16_bits_to_f32(oracle.dequant_bf16(q["codes"], q["scales"], q["ts"])).astype(np.float64)
+    assert np.all(np.abs(got - w_hat) <= np.abs(w_hat) * (2.0 ** -8 + 2.0 ** -24))
+
+
+def test_qat_backward_brute_force():
+    """dX = dY W_hat and dW = dY^T X_hat against explicit sums on a tiny case."""
+    rng = np.random.default_rng(14)
+    M, N, K = 3, 4, 16
+    dy = synth.f32_to_bf16_bits(rng.standard_normal((M, N)).astype(np.float32))
+    w = synth.f32_to_bf16_bits(rng.standard_normal((N, K)).astype(np.float32))
+    x = synth.f32_to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    dx, dw = oracle.qat_backward(dy, w, x)
+    f = lambda b: synth.bf16_bits_to_f32(b).astype(np.float64)  # noqa: E731
+    DY, W, X = f(dy), f(w), f(x)
+    for m in range(M):
+        for k in range(K):
+            assert np.isclose(dx[m, k], sum(DY[m, n] * W[n, k] for n in range(N)), rtol=1e-14, atol=1e-14)
+    for n in range(N):
+        for k in range(K):
+            assert np.isclose(dw[n, k], sum(DY[m, n] * X[m, k] for m in range(M)), rtol=1e-14, atol=1e-14)

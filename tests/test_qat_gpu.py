@@ -1,0 +1,63 @@
+"""NVFP4 dequantisation and the straight-through backward pass of the
+FP4-forward linear layer (quantisation-aware training) on the GPU, against
+the oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from nvfp4_testutil import THREADS, assert_gemm_close, to_dev, y_to_np
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+import nvfp4_weight_quantized_gb300 as nv  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from nvfp4_weight_quantized_gb300 import build
+    build.build()
+    nv.lib()
+
+
+def _bits(t):
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("shape", [(1, 16), (130, 320), (256, 4096), (300, 1024)])
+def test_dequantize_bit_exact(shape):
+    R, K = shape
+    w = synth.weight_normal(R, K, seed=R + K, outlier_frac=0.02)
+    q = nv.nvfp4_quantize_fos(to_dev(w))
+    got = _bits(nv.nvfp4_dequantize(q.codes, q.scales_mma, q.tensor_scale, R, K))
+    ref = oracle.quantize_fos(w)
+    want = oracle.dequant_bf16(ref["codes"], ref["scales"], ref["ts"])
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("MNK", [(1, 64, 64), (37, 200, 320), (300, 512, 1024)])
+def test_qat_backward(MNK):
+    """dX = dY W_hat (bf16) and dW = dY^T X_hat (fp32) against the binary64
+    oracle on the same bf16 operands (GEMM tolerance: fp32 accumulation)."""
+    M, N, K = MNK
+    w = synth.weight_normal(N, K, seed=N + 3 * K, outlier_frac=0.01)
+    x = synth.act_student_t(M, K, seed=M + 5)
+    rng = np.random.default_rng(M * 7 + N)
+    dy = synth.f32_to_bf16_bits(rng.standard_normal((M, N)).astype(np.float32))
+    W = nv.nvfp4_quantize_fos(to_dev(w))
+    A = nv.nvfp4_quantize_act(to_dev(x))
+    dX, dW = nv.nvfp4_qat_backward(to_dev(dy), W, A)
+    torch.cuda.synchronize()
+    wref = oracle.quantize_fos(w)
+    aref = oracle.quantize_rows(x, oracle.tensor_scale(x), False, THREADS)
+    w_hat = oracle.dequant_bf16(wref["codes"], wref["scales"], wref["ts"])
+    x_hat = oracle.dequant_bf16(aref["codes"], aref["scales"], aref["ts"])
+    dx_ref, dw_ref = oracle.qat_backward(dy, w_hat, x_hat)
+    assert_gemm_close(y_to_np(dX), dx_ref, bf16=True, what=f"dX {MNK}")
+    assert_gemm_close(dW.cpu().numpy().astype(np.float64), dw_ref, bf16=False, what=f"dW {MNK}")
+    # either gradient alone
+    dX2, none = nv.nvfp4_qat_backward(to_dev(dy), W, None, want_dw=False)
+    assert none is None and torch.equal(dX2, dX)
+    none, dW2 = nv.nvfp4_qat_backward(to_dev(dy), W, A, want_dx=False)
+    assert none is None and torch.equal(dW2, dW)
