@@ -378,6 +378,7 @@ def prefill_sweep(nv, dev, stream):
         X = torch.from_numpy(synth.prefill_act(M).view(np.int16)).view(torch.bfloat16).to(dev)
         a = nv.nvfp4_quantize_act(X)
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        torch.cuda.synchronize()  # made on the default stream, used on `stream`
         reps = 5
         with torch.cuda.stream(stream):
             for _ in range(2):
@@ -414,6 +415,7 @@ def act_fos_compare(nv, dev, stream, M=1024):
     bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
     qp = nv.nvfp4_quantize_fos(bf(synth.prefill_weight()), logical_scales=False, choice=False)
     X = bf(synth.prefill_act(M))
+    torch.cuda.synchronize()  # inputs were made on the default stream
     with torch.cuda.stream(stream):
         y16 = nv.nvfp4_gemm_w4a16(X, qp, nv.OUT_F32, stream=stream).double()
         a6 = nv.nvfp4_quantize_act(X, stream=stream)
@@ -465,6 +467,7 @@ def gate_up_bench(nv, dev, stream):
     N, K = q.N, q.K
     copies = [q] + [nv.NVFP4Weight(q.codes.clone(), q.scales_mma.clone(), q.tensor_scale.clone(), N, K)
                      for _ in range(3)]
+    torch.cuda.synchronize()  # made on the default stream, used on `stream`
 
     def timed(fn, reps):
         with torch.cuda.stream(stream):
@@ -523,6 +526,7 @@ def qat_bench(nv, dev, stream, M=4096):
     dY = (torch.randn(M, N, device=dev, generator=torch.Generator(device=dev).manual_seed(7))).to(torch.bfloat16)
     Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     A = nv.nvfp4_quantize_act(X)
+    torch.cuda.synchronize()  # made on the default stream, used on `stream`
 
     def fwd():
         nv.nvfp4_gemm_w4a4(nv.nvfp4_quantize_act(X, stream=stream), qp, out=Y, stream=stream)
@@ -587,6 +591,8 @@ def model_quantizer(nv, dev, stream, layers=32, distinct=2):
                                          qws.numel(), stream.cuda_stream)
         assert st == 0, nv.nvfp4_status_string(st)
 
+    # the layers and the counter were made on the default stream
+    torch.cuda.synchronize()
     # fraction of M=4 blocks over the distinct layers (outside the timed region)
     n4, nblk = 0, 0
     with torch.cuda.stream(stream):
