@@ -683,21 +683,28 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t vg[16], vu[16], p[8];
-          tmem_ld_32x32b_x16(tmem + lane_base + 16 * c, vg);
-          tmem_ld_32x32b_x16(tmem + lane_base + 128 + 16 * c, vu);
+        for (int c2 = 0; c2 < 4; ++c2) {  // 32 features per step: chunks 2 c2, 2 c2 + 1 of 16
+          uint32_t vg[32], vu[32];
+          tmem_ld_32x32b_x32(tmem + lane_base + 32 * c2, vg);
+          tmem_ld_32x32b_x32(tmem + lane_base + 128 + 32 * c2, vu);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            p[i] = bf16x2_rn(silu_mul(__uint_as_float(vg[2 * i]) * alpha, __uint_as_float(vu[2 * i]) * alpha),
-                             silu_mul(__uint_as_float(vg[2 * i + 1]) * alpha,
-                                      __uint_as_float(vu[2 * i + 1]) * alpha));
-          uint8_t* box = sm.ystage + (c >> 2) * (BM * 128) + r * 128;
+          for (int h = 0; h < 2; ++h) {
+            const int c = 2 * c2 + h;
+            uint32_t p[8];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int unit = ((c & 3) * 2 + u) ^ (r & 7);
-            *reinterpret_cast<uint4*>(box + unit * 16) = make_uint4(p[4 * u], p[4 * u + 1], p[4 * u + 2], p[4 * u + 3]);
+            for (int i = 0; i < 8; ++i) {
+              const int j = 16 * h + 2 * i;
+              p[i] = bf16x2_rn(silu_mul(__uint_as_float(vg[j]) * alpha, __uint_as_float(vu[j]) * alpha),
+                               silu_mul(__uint_as_float(vg[j + 1]) * alpha, __uint_as_float(vu[j + 1]) * alpha));
+            }
+            uint8_t* box = sm.ystage + (c >> 2) * (BM * 128) + r * 128;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int unit = ((c & 3) * 2 + u) ^ (r & 7);
+              *reinterpret_cast<uint4*>(box + unit * 16) =
+                  make_uint4(p[4 * u], p[4 * u + 1], p[4 * u + 2], p[4 * u + 3]);
+            }
           }
         }
         fence_before_sync();
@@ -723,23 +730,30 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");  // staging buffer free
         uint32_t hi[8][8];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {  // 16 columns per load
-          uint32_t v[16], p[8];
-          tmem_ld_32x32b_x16(tmem + lane_base + 16 * c, v);
+        for (int c2 = 0; c2 < 8; ++c2) {  // 32 columns per load: chunks 2 c2, 2 c2 + 1 of 16
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + lane_base + 32 * c2, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            p[i] = bf16x2_rn(__uint_as_float(v[2 * i]) * alpha, __uint_as_float(v[2 * i + 1]) * alpha);
-          if (c < 8) {
-            uint8_t* box = sm.ystage + (c >> 2) * (BM * 128) + r * 128;
+          for (int h = 0; h < 2; ++h) {
+            const int c = 2 * c2 + h;
+            uint32_t p[8];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int unit = ((c & 3) * 2 + u) ^ (r & 7);
-              *reinterpret_cast<uint4*>(box + unit * 16) = make_uint4(p[4 * u], p[4 * u + 1], p[4 * u + 2], p[4 * u + 3]);
+            for (int i = 0; i < 8; ++i)
+              p[i] = bf16x2_rn(__uint_as_float(v[16 * h + 2 * i]) * alpha,
+                               __uint_as_float(v[16 * h + 2 * i + 1]) * alpha);
+            if (c < 8) {
+              uint8_t* box = sm.ystage + (c >> 2) * (BM * 128) + r * 128;
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                const int unit = ((c & 3) * 2 + u) ^ (r & 7);
+                *reinterpret_cast<uint4*>(box + unit * 16) =
+                    make_uint4(p[4 * u], p[4 * u + 1], p[4 * u + 2], p[4 * u + 3]);
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) hi[c - 8][i] = p[i];
             }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) hi[c - 8][i] = p[i];
           }
         }
         fence_before_sync();
