@@ -39,6 +39,13 @@ def test_workspace_bytes(L):
     lin = nv.nvfp4_workspace_bytes(nv.OP_LINEAR, 1024, 11008, 4096)
     assert lin >= 1024 * 2048 + nv.nvfp4_scales_mma_bytes(1024, 4096)
     assert nv.nvfp4_workspace_bytes(99, 1, 1, 64) == 0
+    # gated MLP: the linear workspace plus fp32 [min(M, 1024), N] staging
+    lin300 = nv.nvfp4_workspace_bytes(nv.OP_LINEAR, 300, 2 * 11008, 4096)
+    assert nv.nvfp4_workspace_bytes(nv.OP_LINEAR_SILU_MUL, 300, 2 * 11008, 4096) == lin300 + 300 * 2 * 11008 * 4
+    big = nv.nvfp4_workspace_bytes(nv.OP_LINEAR_SILU_MUL, 5000, 2 * 11008, 4096)
+    assert big == nv.nvfp4_workspace_bytes(nv.OP_LINEAR, 5000, 2 * 11008, 4096) + 1024 * 2 * 11008 * 4
+    # QAT backward: bf16 W_hat [N, K] and X_hat [M, K], each 256-byte aligned
+    assert nv.nvfp4_workspace_bytes(nv.OP_QAT_BACKWARD, 37, 200, 320) == 128000 + 23808
 
 
 def test_crossover_table(L):
