@@ -333,6 +333,7 @@ def run_ours(args):
         detail["act_fos"] = act_fos_compare(nv, dev, stream)
         detail["gate_up_silu_mul"] = gate_up_bench(nv, dev, stream)
         detail["qat_step"] = qat_bench(nv, dev, stream)
+        detail["gptq_fos"] = gptq_bench(nv, dev, stream)
 
     e2e = measure_e2e(nv, dev, stream, w_bits, args, step_bytes, paths) if rank == 0 else None
 
@@ -552,6 +553,52 @@ def qat_bench(nv, dev, stream, M=4096):
     return {"M": M, "N": N, "K": K, "forward_us": round(tf * 1e6, 1), "forward_tflops": round(fl / tf / 1e12, 1),
             "backward_us": round(tb * 1e6, 1), "backward_tflops": round(2 * fl / tb / 1e12, 1),
             "timing": "eager calls (the backward's cuBLAS handle is not captured), CUDA events"}
+
+
+def gptq_bench(nv, dev, stream, T=4096):
+    """GPTQ inside FourOverSix scales on the decode weight [4096, 4096] with a
+    synthetic Hessian H = 2 X^T X / T (X: T tokens of N(0, 1) features, the
+    first quarter of the features x3), as an offline step: its time, and the
+    layer error tr(dW H dW^T) of its codes relative to FourOverSix
+    round-to-nearest with the same scales (dW = W - W_hat, binary64)."""
+    import torch
+    bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
+    W = bf(synth.decode_weight())
+    N, K = W.shape
+    g = torch.Generator(device=dev).manual_seed(11)
+    X = torch.randn(T, K, device=dev, generator=g)
+    X[:, : K // 4] *= 3.0
+    H = (2.0 / T) * (X.t() @ X)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        q = nv.nvfp4_gptq_fos(W, H, stream=stream)  # warm
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        q = nv.nvfp4_gptq_fos(W, H, stream=stream)
+        e1.record(stream)
+        f = nv.nvfp4_quantize_fos(W, stream=stream)
+    e1.synchronize()
+    assert nv.nvfp4_get_device_status(stream) == 0
+
+    e2 = torch.tensor([0, 0.5, 1, 1.5, 2, 3, 4, 6, 0, -0.5, -1, -1.5, -2, -3, -4, -6], dtype=torch.float64, device=dev)
+    e4 = torch.tensor([((b >> 3) & 15 and (1 + (b & 7) / 8.0) * 2.0 ** (((b >> 3) & 15) - 7)) or (b & 7) / 8.0 * 2 ** -6
+                       for b in range(128)], dtype=torch.float64, device=dev)
+
+    def dequant(codes, scales, ts):
+        c = codes.long()
+        v = e2[torch.stack([c & 15, c >> 4], dim=-1).reshape(N, K)]
+        return v * e4[scales.long()].repeat_interleave(16, dim=1) * float(ts.item())
+
+    W64, H64 = W.double(), H.double()
+
+    def layer_err(wq):
+        d = W64 - wq
+        return float(((d @ H64) * d).sum())
+    eg = layer_err(dequant(q.codes, q.scales, q.tensor_scale))
+    er = layer_err(dequant(f.codes, f.scales, f.tensor_scale))
+    return {"N": N, "K": K, "tokens": T, "ms": round(e0.elapsed_time(e1), 2),
+            "layer_err_gptq_over_rtn": round(eg / er, 4),
+            "scales_equal_fos": bool(torch.equal(q.scales, f.scales))}
 
 
 def model_quantizer(nv, dev, stream, layers=32, distinct=2):

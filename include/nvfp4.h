@@ -78,7 +78,8 @@ typedef enum nvfp4_op {
   NVFP4_OP_GEMM_W4A4 = 3,
   NVFP4_OP_LINEAR = 4,
   NVFP4_OP_LINEAR_SILU_MUL = 5,
-  NVFP4_OP_QAT_BACKWARD = 6
+  NVFP4_OP_QAT_BACKWARD = 6,
+  NVFP4_OP_GPTQ_FOS = 7
 } nvfp4_op;
 
 #define NVFP4_DEFAULT_DIVISOR 2688.0f /* 6 (E2M1 max) * 448 (E4M3 max) */
@@ -131,6 +132,33 @@ nvfp4_status nvfp4_quantize_fos(const void* W, int64_t N, int64_t K, float divis
                                 float* tensor_scale, uint8_t* choice,
                                 unsigned long long* m4_count, void* workspace,
                                 size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * GPTQ inside FourOverSix scales ("SOAR Weekly Champion Notes 07 ... NVFP4
+ * Quantization Improvements", section "03 How we integrated it": each
+ * block's M=4 / M=6 choice is fixed first, then GPTQ's error-compensating
+ * quantisation runs within it).  Scales, tensor scale (and scales_mma) are
+ * those of nvfp4_quantize_fos on W; the codes are GPTQ's: columns quantised
+ * in order with those fixed scales, each column's error divided by U[j][j]
+ * and spread over the columns not yet quantised along row j of U, the upper
+ * Cholesky factor of (H + d I)^-1, d = damp * mean(diag H), in blocks of 128
+ * columns.  Every step is binary32 in a fixed order (stated in
+ * csrc/gptq.cu), so the codes are reproducible bit for bit.
+ *   W        in:  device bf16 [N, K]
+ *   H        in:  device fp32 [K, K], symmetric positive semi-definite (the
+ *                 layer's Hessian, e.g. 2 X^T X / T over calibration tokens)
+ *   damp     in:  >= 0 (GPTQ's usual 0.01)
+ *   codes, scales (nullable), scales_mma (nullable), tensor_scale: as
+ *                 nvfp4_quantize_fos
+ *   workspace nvfp4_workspace_bytes(NVFP4_OP_GPTQ_FOS, 0, N, K) bytes
+ * A damped Hessian that is not positive definite sets NVFP4_ERR_NONFINITE in
+ * the device status word (nvfp4_get_device_status).  An offline step: about
+ * 2K kernel launches for the factorisation.
+ */
+nvfp4_status nvfp4_gptq_fos(const void* W, int64_t N, int64_t K, const float* H, float damp,
+                            uint8_t* codes, uint8_t* scales, uint8_t* scales_mma,
+                            float* tensor_scale, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
 
 /*
  * Online NVFP4 quantisation of activations for the W4A4 path (the pages give

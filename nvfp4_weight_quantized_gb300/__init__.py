@@ -23,7 +23,7 @@ __all__ = [
     "NVFP4Error", "NVFP4Weight", "NVFP4Act", "lib", "library_path", "declared_functions",
     "nvfp4_scales_mma_bytes", "nvfp4_workspace_bytes", "nvfp4_quantize_fos", "nvfp4_quantize_act",
     "nvfp4_gemm_w4a16", "nvfp4_gemm_w4a4", "nvfp4_linear", "nvfp4_linear_silu_mul", "nvfp4_linear_noalloc",
-    "nvfp4_dequantize", "nvfp4_qat_backward", "nvfp4_set_crossover",
+    "nvfp4_dequantize", "nvfp4_qat_backward", "nvfp4_gptq_fos", "nvfp4_set_crossover",
     "nvfp4_get_crossover", "nvfp4_set_w4a16_rf_max_m", "nvfp4_get_w4a16_rf_max_m",
     "nvfp4_set_w4a16_sk_max_m", "nvfp4_get_w4a16_sk_max_m", "nvfp4_set_weight_prefetch",
     "nvfp4_get_weight_prefetch", "nvfp4_set_w4a4_cluster", "nvfp4_get_w4a4_cluster", "nvfp4_set_act_fos", "nvfp4_get_act_fos", "nvfp4_get_device_status",
@@ -39,8 +39,8 @@ OK = 0
 ERR_INVALID_ARG, ERR_SHAPE, ERR_ALIGN, ERR_WORKSPACE = 1, 2, 3, 4
 ERR_NONFINITE, ERR_TIMEOUT, ERR_CUDA, ERR_UNSUPPORTED = 5, 6, 7, 8
 OUT_BF16, OUT_F32 = 0, 1
-OP_QUANTIZE_FOS, OP_QUANTIZE_ACT, OP_GEMM_W4A16, OP_GEMM_W4A4, OP_LINEAR, OP_LINEAR_SILU_MUL, OP_QAT_BACKWARD = \
-    0, 1, 2, 3, 4, 5, 6
+OP_QUANTIZE_FOS, OP_QUANTIZE_ACT, OP_GEMM_W4A16, OP_GEMM_W4A4, OP_LINEAR, OP_LINEAR_SILU_MUL, OP_QAT_BACKWARD, \
+    OP_GPTQ_FOS = 0, 1, 2, 3, 4, 5, 6, 7
 DEFAULT_DIVISOR = 2688.0
 
 
@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
             "nvfp4_linear_noalloc": (st, [vp, i64, wp, vp, ctypes.c_int, vp]),
             "nvfp4_linear_silu_mul": (st, [vp, i64, wp, vp, ctypes.c_int, vp, sz, vp]),
             "nvfp4_dequantize": (st, [vp, vp, vp, i64, i64, vp, vp]),
+            "nvfp4_gptq_fos": (st, [vp, i64, i64, vp, ctypes.c_float, vp, vp, vp, vp, vp, sz, vp]),
             "nvfp4_qat_backward": (st, [vp, i64, wp, vp, vp, vp, vp, vp, vp, sz, vp]),
             "nvfp4_set_crossover": (st, [i64, i64, i64]),
             "nvfp4_get_crossover": (i64, [i64, i64]),
@@ -380,3 +381,21 @@ def nvfp4_qat_backward(dY: torch.Tensor, W: NVFP4Weight, A: Optional[NVFP4Act], 
                                     dW.data_ptr() if dW is not None else None, ws.data_ptr(), ws.numel(),
                                     _stream(stream)), "nvfp4_qat_backward")
     return dX, dW
+
+
+def nvfp4_gptq_fos(W: torch.Tensor, H: torch.Tensor, damp: float = 0.01, stream=None) -> NVFP4Weight:
+    """GPTQ inside FourOverSix scales (nvfp4_gptq_fos): W bf16 [N, K], H fp32 [K, K]."""
+    _require_cuda(W, H)
+    if W.dtype != torch.bfloat16 or W.dim() != 2 or H.dtype != torch.float32 or not H.is_contiguous():
+        raise ValueError("W must be a 2-D bfloat16 tensor and H a contiguous float32 [K, K] tensor")
+    N, K = W.shape
+    dev = W.device
+    codes = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+    scales = torch.empty((N, K // 16), dtype=torch.uint8, device=dev)
+    smma = torch.empty(nvfp4_scales_mma_bytes(N, K), dtype=torch.uint8, device=dev)
+    ts = torch.empty(1, dtype=torch.float32, device=dev)
+    ws = _workspace(nvfp4_workspace_bytes(OP_GPTQ_FOS, 0, N, K), dev)
+    _check(lib().nvfp4_gptq_fos(W.contiguous().data_ptr(), N, K, H.data_ptr(), float(damp), codes.data_ptr(),
+                                scales.data_ptr(), smma.data_ptr(), ts.data_ptr(), ws.data_ptr(), ws.numel(),
+                                _stream(stream)), "nvfp4_gptq_fos")
+    return NVFP4Weight(codes=codes, scales_mma=smma, tensor_scale=ts, N=N, K=K, scales=scales)

@@ -179,6 +179,11 @@ size_t nvfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
       // sized for the W4A4 branch whatever the current crossover is
       if (M <= 0) return 0;
       return linear_ws_layout(M, K).total;
+    case NVFP4_OP_GPTQ_FOS:
+      // the GPTQ working set, logical scales, the quantiser's partials
+      if (N <= 0) return 0;
+      return nvfp4::gptq_workspace_bytes(N, K) + align256((size_t)N * (size_t)(K / 16)) +
+             align256(nvfp4::quant_workspace_bytes());
     case NVFP4_OP_QAT_BACKWARD:
       // bf16 W_hat [N, K] and X_hat [M, K]
       if (M <= 0 || N <= 0) return 0;
@@ -351,6 +356,34 @@ nvfp4_status nvfp4_linear_silu_mul(const void* X, int64_t M, const nvfp4_weight*
                                       stream)) != cudaSuccess)
       return fail_cuda(err, "silu_mul launch");
   }
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_gptq_fos(const void* W, int64_t N, int64_t K, const float* H, float damp, uint8_t* codes,
+                            uint8_t* scales, uint8_t* scales_mma, float* tensor_scale, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream) {
+  if (W == nullptr || H == nullptr || codes == nullptr || tensor_scale == nullptr)
+    return fail(NVFP4_ERR_INVALID_ARG, "gptq_fos: W, H, codes and tensor_scale are required");
+  if (!(damp >= 0.0f) || !std::isfinite(damp)) return fail(NVFP4_ERR_INVALID_ARG, "gptq_fos: damp must be >= 0");
+  if (N <= 0 || K < 16 || K % 16 != 0 || N > kMaxElems / K || K > 65536)
+    return fail(NVFP4_ERR_SHAPE, "gptq_fos: need N >= 1, 16 <= K <= 65536, K % 16 == 0");
+  if (!aligned(H, 16)) return fail(NVFP4_ERR_ALIGN, "gptq_fos: H must be 16-byte aligned");
+  const size_t gws = nvfp4::gptq_workspace_bytes(N, K), sbytes = align256((size_t)N * (size_t)(K / 16));
+  if (workspace == nullptr || !aligned(workspace, 256) ||
+      workspace_bytes < nvfp4_workspace_bytes(NVFP4_OP_GPTQ_FOS, 0, N, K))
+    return fail(NVFP4_ERR_WORKSPACE, "gptq_fos: workspace missing, not 256-byte aligned or too small");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* lscales = scales != nullptr ? scales : ws + gws;
+  // 1. FourOverSix on the original weights fixes every block's scale (and ts)
+  nvfp4_status st = quantize_common(W, N, K, NVFP4_DEFAULT_DIVISOR, true, codes, lscales, scales_mma, tensor_scale,
+                                    nullptr, nullptr, ws + gws + sbytes, workspace_bytes - gws - sbytes, stream);
+  if (st != NVFP4_OK) return st;
+  const DeviceInfo* d = nullptr;
+  if ((st = device_info(&d)) != NVFP4_OK) return st;
+  // 2. GPTQ inside those scales rewrites the codes
+  const cudaError_t err =
+      nvfp4::launch_gptq(W, N, K, H, damp, lscales, tensor_scale, codes, workspace, d->status, stream);
+  if (err != cudaSuccess) return fail_cuda(err, "gptq launch");
   return NVFP4_OK;
 }
 

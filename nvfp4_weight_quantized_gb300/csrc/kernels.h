@@ -67,6 +67,14 @@ cudaError_t launch_dequant_bf16(const uint8_t* codes, const uint8_t* scales_mma,
 int qat_backward_gemms(const void* dy, const void* w_hat, const void* x_hat, int64_t M, int64_t N, int64_t K,
                        void* dx, void* dw, cudaStream_t stream);
 
+// GPTQ inside FourOverSix scales (see gptq.cu): W bf16 [N, K], H fp32 [K, K],
+// scales logical [N, K/16] and ts from the FourOverSix quantiser on W; codes
+// [N, K/2] are overwritten.  workspace of gptq_workspace_bytes(N, K).
+size_t gptq_workspace_bytes(int64_t N, int64_t K);
+cudaError_t launch_gptq(const void* W, int64_t N, int64_t K, const float* H, float damp, const uint8_t* scales,
+                        const float* ts, uint8_t* codes, void* workspace, unsigned int* status,
+                        cudaStream_t stream);
+
 // CTAs per cluster for M > 128: 4 (two CTA pairs sharing A rows by TMA
 // multicast), 2 (one pair, cta_group::2 MMAs on 256 x 256 tiles) or 1 (single
 // CTAs on 128 x 256 tiles).  The setter rejects anything else.

@@ -97,6 +97,8 @@ def _load():
         lib.oracle_gemm_w4a4.restype = ctypes.c_int
         lib.oracle_dequant_bf16.argtypes = [u8p, u8p, ctypes.c_float, i64, i64, u16p]
         lib.oracle_dequant_bf16.restype = ctypes.c_int
+        lib.oracle_gptq_fos.argtypes = [u16p, i64, i64, f32p, ctypes.c_float, i64, u8p, u8p, f32p, f32p]
+        lib.oracle_gptq_fos.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -321,3 +323,31 @@ def qat_backward(dy_bits: np.ndarray, w_hat_bits: np.ndarray, x_hat_bits: np.nda
     w = bf16_to_f32(w_hat_bits).astype(np.float64)
     x = bf16_to_f32(x_hat_bits).astype(np.float64)
     return dy @ w, dy.T @ x
+
+
+def gptq_fos(w_bits: np.ndarray, H: np.ndarray, damp: float = 0.01, block: int = 128,
+             want_u: bool = False) -> dict:
+    """GPTQ inside FourOverSix scales ("SOAR Weekly Champion Notes 07 ...",
+    section "03 How we integrated it": each block's M is fixed first, then
+    GPTQ runs within it).  w_bits bf16 [N, K]; H float32 [K, K] (the layer's
+    Hessian, e.g. 2 X^T X / T from calibration activations).  Returns codes,
+    logical scales, ts (and U, the upper Cholesky factor of the damped
+    inverse Hessian) computed in the binary32 order stated in nvfp4_oracle.c."""
+    w_bits = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    N, K = w_bits.shape
+    H = np.ascontiguousarray(H, dtype=np.float32)
+    assert H.shape == (K, K)
+    codes = np.zeros((N, K // 2), np.uint8)
+    scales = np.zeros((N, K // 16), np.uint8)
+    ts = np.zeros(1, np.float32)
+    U = np.zeros((K, K), np.float32) if want_u else None
+    st = _load().oracle_gptq_fos(_ptr(w_bits, ctypes.c_uint16), N, K, _ptr(H, ctypes.c_float), damp, block,
+                                 _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8),
+                                 _ptr(ts, ctypes.c_float),
+                                 _ptr(U, ctypes.c_float) if want_u else None)
+    if st:
+        raise OracleError(st)
+    out = {"codes": codes, "scales": scales, "ts": float(ts[0])}
+    if want_u:
+        out["U"] = U
+    return out

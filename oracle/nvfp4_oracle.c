@@ -57,11 +57,13 @@
 #include <math.h>
 #include <stdint.h>
 #include <stddef.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define OR_OK 0
 #define OR_ERR_SHAPE 2
 #define OR_ERR_NONFINITE 5
+#define DEFAULT_DIVISOR_F 2688.0f /* 6 * 448 */
 
 /* ------------------------------------------------------------------------ */
 /* Formats                                                                  */
@@ -379,4 +381,125 @@ int oracle_dequant_bf16(const uint8_t* codes, const uint8_t* scales, float ts, i
       out[r * K + k] = bf16_round(q);
     }
   return OR_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* GPTQ with FourOverSix scales                                             */
+/* ------------------------------------------------------------------------ */
+
+/* "SOAR Weekly Champion Notes 07 ... NVFP4 Quantization Improvements",
+ * section "03 How we integrated it": FourOverSix first fixes each block's
+ * scale (M=4 or M=6), then GPTQ quantises inside that choice.  GPTQ itself (the method the pages
+ * combine it with) quantises the columns of W in order and spreads each
+ * column's error, divided by the diagonal of U, over the columns still to be
+ * quantised through the rows of U, the upper Cholesky factor of the inverse
+ * of the damped Hessian (H + d I, d = damp * mean(diag H)), in blocks of
+ * `block` columns: inside a block the error goes to the block's remaining
+ * columns at once, to the columns after the block once per block.
+ *
+ * Every step below is binary32 with one rounding per operation, in the order
+ * written (the kernel's precision: the codes are decided in binary32):
+ *   d      = damp * ((sum_k H[k][k], k ascending) / K)
+ *   A      = J (H + d I) J, J the index reversal
+ *   L      = chol(A), right-looking: for j: L[j][j] = sqrt(A[j][j]),
+ *            L[i][j] = A[i][j] / L[j][j], then A[i][c] = fma(-L[i][j], L[c][j], A[i][c])
+ *            for j < c <= i
+ *   Linv   = L^-1 by columns: x[j] = 1 / L[j][j]; for i > j:
+ *            s = sum_{k=j}^{i-1} fma(L[i][k], x[k], s) (k ascending), x[i] = -s / L[i][i]
+ *   U      = J Linv J  (then H'^-1 = U^T U)
+ *   column j of row n, block scale eff = value(scale) * ts:
+ *            q = e2m1(RN(w / eff)) (q = sign only when eff == 0),
+ *            e = fma(-value(q), eff, w) / U[j][j],
+ *            w[n][c] = fma(-e, U[j][c], w[n][c]) for the block's later columns c,
+ *   after a block, for every later column c:
+ *            s = sum_{j in block} fma(E[n][j], U[j][c], s) (j ascending), w[n][c] -= s.
+ * Scales and ts are those of oracle_quantize_fos on the original W.  H is
+ * [K, K] row-major (symmetric); U_out (nullable) receives U [K, K].
+ * Returns OR_ERR_NONFINITE if a Cholesky pivot is not positive. */
+int oracle_gptq_fos(const uint16_t* W, int64_t N, int64_t K, const float* H, float damp, int64_t block,
+                    uint8_t* codes, uint8_t* scales, float* ts_out, float* U_out) {
+  if (N <= 0 || K <= 0 || K % 16 != 0 || block <= 0 || block % 16 != 0) return OR_ERR_SHAPE;
+  int st = oracle_quantize_fos(W, N, K, DEFAULT_DIVISOR_F, codes, scales, NULL, ts_out, NULL);
+  if (st != OR_OK) return st;
+  const float ts = *ts_out;
+  float* A = (float*)malloc(sizeof(float) * K * K);
+  float* Li = (float*)malloc(sizeof(float) * K * K);
+  float* Wc = (float*)malloc(sizeof(float) * N * K);
+  float* E = (float*)malloc(sizeof(float) * N * block);
+  if (!A || !Li || !Wc || !E) {
+    free(A); free(Li); free(Wc); free(E);
+    return OR_ERR_SHAPE;
+  }
+  float dsum = 0.0f;
+  for (int64_t k = 0; k < K; ++k) dsum += H[k * K + k];
+  const float dval = damp * (dsum / (float)K);
+  for (int64_t i = 0; i < K; ++i)
+    for (int64_t j = 0; j < K; ++j) {
+      float h = H[(K - 1 - i) * K + (K - 1 - j)];
+      A[i * K + j] = (i == j) ? h + dval : h;
+    }
+  /* Cholesky, lower triangle of A in place */
+  for (int64_t j = 0; j < K && st == OR_OK; ++j) {
+    if (!(A[j * K + j] > 0.0f)) {
+      st = OR_ERR_NONFINITE;
+      break;
+    }
+    const float p = sqrtf(A[j * K + j]);
+    A[j * K + j] = p;
+    for (int64_t i = j + 1; i < K; ++i) A[i * K + j] = A[i * K + j] / p;
+    for (int64_t i = j + 1; i < K; ++i)
+      for (int64_t c = j + 1; c <= i; ++c) A[i * K + c] = fmaf(-A[i * K + j], A[c * K + j], A[i * K + c]);
+  }
+  if (st == OR_OK) {
+    /* inverse of the lower factor, column by column */
+    memset(Li, 0, sizeof(float) * K * K);
+    for (int64_t j = 0; j < K; ++j) {
+      Li[j * K + j] = 1.0f / A[j * K + j];
+      for (int64_t i = j + 1; i < K; ++i) {
+        float s = 0.0f;
+        for (int64_t k = j; k < i; ++k) s = fmaf(A[i * K + k], Li[k * K + j], s);
+        Li[i * K + j] = -s / A[i * K + i];
+      }
+    }
+#define U_AT(i, j) Li[(K - 1 - (i)) * K + (K - 1 - (j))]
+    if (U_out)
+      for (int64_t i = 0; i < K; ++i)
+        for (int64_t j = 0; j < K; ++j) U_out[i * K + j] = U_AT(i, j);
+    for (int64_t i = 0; i < N * K; ++i) Wc[i] = oracle_bf16_value(W[i]);
+    const int64_t nb = K / 16;
+    for (int64_t b0 = 0; b0 < K; b0 += block) {
+      const int64_t b1 = b0 + block < K ? b0 + block : K;
+      for (int64_t n = 0; n < N; ++n) {
+        float* w = Wc + n * K;
+        for (int64_t j = b0; j < b1; ++j) {
+          const float eff = (float)oracle_e4m3_value(scales[n * nb + j / 16]) * ts;
+          uint8_t q;
+          float d;
+          if (eff == 0.0f) {
+            q = signbit(w[j]) ? 8 : 0;
+            d = w[j];
+          } else {
+            q = oracle_e2m1_encode(w[j] / eff);
+            d = fmaf(-(float)oracle_e2m1_value(q), eff, w[j]);
+          }
+          const float e = d / U_AT(j, j);
+          E[n * block + (j - b0)] = e;
+          for (int64_t c = j + 1; c < b1; ++c) w[c] = fmaf(-e, U_AT(j, c), w[c]);
+          uint8_t* byte = codes + n * (K / 2) + j / 2;
+          *byte = (j & 1) ? (uint8_t)((*byte & 15) | (q << 4)) : (uint8_t)((*byte & 0xF0) | q);
+        }
+        for (int64_t c = b1; c < K; ++c) {
+          float s = 0.0f;
+          for (int64_t j = b0; j < b1; ++j) s = fmaf(E[n * block + (j - b0)], U_AT(j, c), s);
+          w[c] = w[c] - s;
+        }
+      }
+    }
+#undef U_AT
+  }
+  free(A);
+  free(Li);
+  free(Wc);
+  free(E);
+  return st;
 }

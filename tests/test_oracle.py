@@ -482,3 +482,63 @@ def test_qat_backward_brute_force():
     for n in range(N):
         for k in range(K):
             assert np.isclose(dw[n, k], sum(DY[m, n] * X[m, k] for m in range(M)), rtol=1e-14, atol=1e-14)
+
+
+# ------------------------------------------------------------ GPTQ + FOS ---
+
+def _hessian(K, T, seed):
+    rng = np.random.default_rng(seed)
+    X = rng.standard_normal((T, K)).astype(np.float32)
+    X[:, : K // 4] *= 3.0  # unequal feature scales
+    return (2.0 * X.T @ X / T).astype(np.float32)
+
+
+def _dequant64(codes, scales, ts):
+    N, K = codes.shape[0], codes.shape[1] * 2
+    e2 = np.array([oracle.e2m1_value(c) for c in range(16)])
+    e4 = np.array([oracle.e4m3_value(b) if (b & 0x7F) != 0x7F else 0.0 for b in range(256)])
+    q = np.stack([codes & 15, codes >> 4], axis=-1).reshape(N, K)
+    return e2[q] * np.repeat(e4[scales], 16, axis=1) * ts
+
+
+def test_gptq_identity_hessian_is_rtn():
+    """With H = c I the inverse Hessian's Cholesky factor is diagonal, so no
+    error is spread and GPTQ must return the FourOverSix round-to-nearest
+    codes and scales exactly."""
+    w = synth.weight_normal(48, 256, seed=21, outlier_frac=0.02)
+    f = oracle.quantize_fos(w)
+    for c in (1.0, 0.37):
+        g = oracle.gptq_fos(w, np.eye(256, dtype=np.float32) * c, block=64)
+        assert np.array_equal(g["codes"], f["codes"]) and np.array_equal(g["scales"], f["scales"])
+        assert g["ts"] == f["ts"]
+
+
+def test_gptq_inverse_cholesky_factor():
+    """U^T U is the inverse of the damped Hessian (numpy binary64 inverse)."""
+    K = 192
+    H = _hessian(K, 400, 22)
+    g = oracle.gptq_fos(synth.weight_normal(8, K, seed=23), H, damp=0.01, want_u=True)
+    U = g["U"].astype(np.float64)
+    assert np.all(np.tril(U, -1) == 0) and np.all(np.diag(U) > 0)
+    Hd = H.astype(np.float64) + 0.01 * np.mean(np.diag(H.astype(np.float64))) * np.eye(K)
+    inv = np.linalg.inv(Hd)
+    assert np.abs(U.T @ U - inv).max() <= 1e-4 * np.abs(inv).max()
+
+
+def test_gptq_lowers_layer_error():
+    """GPTQ's purpose: the layer output error tr(dW H dW^T) of its codes is
+    below that of round-to-nearest with the same FourOverSix scales, while
+    the scales (the M=4 / M=6 choices) are unchanged."""
+    K = 256
+    w = synth.weight_normal(96, K, seed=24, outlier_frac=0.01)
+    H = _hessian(K, 512, 25)
+    f = oracle.quantize_fos(w)
+    g = oracle.gptq_fos(w, H, block=64)
+    assert np.array_equal(g["scales"], f["scales"])
+    W = synth.bf16_bits_to_f32(w).astype(np.float64)
+    H64 = H.astype(np.float64)
+
+    def err(codes):
+        d = W - _dequant64(codes, f["scales"], f["ts"])
+        return float(np.einsum("nk,kl,nl->", d, H64, d))
+    assert err(g["codes"]) < 0.9 * err(f["codes"])
