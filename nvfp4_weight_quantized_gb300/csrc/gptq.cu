@@ -19,7 +19,7 @@
 //                         L[j][j] = sqrt(A[j][j]); L[i][j] = A[i][j] / L[j][j];
 //                         A[i][c] = fma(-L[i][j], L[c][j], A[i][c]), j < c <= i
 //   trinv_kernel          Linv = L^-1 by columns: x[j] = 1 / L[j][j],
-//                         x[i] = -(sum_{k<i} fma(L[i][k], x[k], .)) / L[i][i]
+//                         x[i] = -(sum_{k=j}^{i-1} fma(L[i][k], x[k], .)) / L[i][i]
 //                         (U = J Linv J, read through reversed indices)
 //   gptq_block_kernel     one thread per row: for each column j of the block,
 //                         q = e2m1(RN(w / eff)), e = fma(-value(q), eff, w) / U[j][j],
@@ -86,18 +86,32 @@ __global__ void chol_update_kernel(float* __restrict__ A, int64_t K, int64_t j) 
   A[i * K + c] = __fmaf_rn(-A[i * K + j], A[c * K + j], A[i * K + c]);
 }
 
-// Inverse of the lower factor, one column per thread; a warp shares each L[i][k]
-// (broadcast) and reads consecutive columns of Linv.  Terms with k < j add
-// fma(L[i][k], 0, s) = s exactly, so starting every column at k = 0 gives the
-// same bits as starting at k = j.
-__global__ void trinv_kernel(const float* __restrict__ L, int64_t K, float* __restrict__ li) {
-  const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= K) return;
-  li[j * K + j] = __fdiv_rn(1.0f, L[j * K + j]);
-  for (int64_t i = j + 1; i < K; ++i) {
-    float s = 0.0f;
-    for (int64_t k = j; k < i; ++k) s = __fmaf_rn(L[i * K + k], li[k * K + j], s);
-    li[i * K + j] = __fdiv_rn(-s, L[i * K + i]);
+// Inverse of the lower factor: a CTA (one warp, kInvCols active lanes) owns
+// kInvCols consecutive columns j0 .. and keeps their entries x[k], k >= j0,
+// in shared memory ([k][lane], conflict-free); each L[i][k] is a broadcast
+// load.  A lane starts its sum at k = j0 instead of its own j: the extra
+// terms are fma(L[i][k], 0, s) = s exactly (x[k] = 0 for k < j; s starts at
+// +0), so every column gets the bits of the sum taken from k = j.
+constexpr int kInvCols = 4;
+
+__global__ void __launch_bounds__(32) trinv_kernel(const float* __restrict__ L, int64_t K, float* __restrict__ li) {
+  extern __shared__ float xs[];  // [(K - j0)][kInvCols]
+  const int lane = threadIdx.x;
+  const int64_t j0 = (int64_t)blockIdx.x * kInvCols, j = j0 + lane;
+  for (int64_t e = lane; e < (K - j0) * kInvCols; e += 32) xs[e] = 0.0f;
+  __syncwarp();
+  if (lane >= kInvCols || j >= K) return;
+  for (int64_t i = j; i < K; ++i) {
+    float x;
+    if (i == j) {
+      x = __fdiv_rn(1.0f, L[j * K + j]);
+    } else {
+      float s = 0.0f;
+      for (int64_t k = j0; k < i; ++k) s = __fmaf_rn(L[i * K + k], xs[(k - j0) * kInvCols + lane], s);
+      x = __fdiv_rn(-s, L[i * K + i]);
+    }
+    xs[(i - j0) * kInvCols + lane] = x;
+    li[i * K + j] = x;
   }
 }
 
@@ -168,6 +182,8 @@ __global__ void gptq_trail_kernel(float* __restrict__ wc, int64_t N, int64_t K, 
 
 }  // namespace
 
+int64_t gptq_max_k() { return (int64_t)(227 * 1024) / (kInvCols * (int64_t)sizeof(float)); }
+
 size_t gptq_workspace_bytes(int64_t N, int64_t K) {
   auto a256 = [](size_t b) { return (b + 255) & ~(size_t)255; };
   return 2 * a256((size_t)K * K * 4) + a256((size_t)N * K * 4) + a256((size_t)N * kBlock * 4) + a256((size_t)K * 4) +
@@ -202,7 +218,11 @@ cudaError_t launch_gptq(const void* W, int64_t N, int64_t K, const float* H, flo
   chol_diag_kernel<<<(unsigned)((K + 255) / 256), 256, 0, stream>>>(A, K, piv);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   if ((err = cudaMemsetAsync(li, 0, (size_t)K * K * 4, stream)) != cudaSuccess) return err;
-  trinv_kernel<<<(unsigned)((K + 63) / 64), 64, 0, stream>>>(A, K, li);
+  const size_t inv_smem = (size_t)K * kInvCols * sizeof(float);
+  if ((err = cudaFuncSetAttribute(trinv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)inv_smem)) !=
+      cudaSuccess)
+    return err;
+  trinv_kernel<<<(unsigned)((K + kInvCols - 1) / kInvCols), 32, inv_smem, stream>>>(A, K, li);
   bf16_to_f32_kernel<<<1024, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(W), N * K, wc);
   const size_t smem = (size_t)2 * kBlock * kPitch * sizeof(float);
   if ((err = cudaFuncSetAttribute(gptq_block_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=

@@ -71,6 +71,7 @@ int qat_backward_gemms(const void* dy, const void* w_hat, const void* x_hat, int
 // scales logical [N, K/16] and ts from the FourOverSix quantiser on W; codes
 // [N, K/2] are overwritten.  workspace of gptq_workspace_bytes(N, K).
 size_t gptq_workspace_bytes(int64_t N, int64_t K);
+int64_t gptq_max_k();  // largest K the triangular inverse's shared memory holds
 cudaError_t launch_gptq(const void* W, int64_t N, int64_t K, const float* H, float damp, const uint8_t* scales,
                         const float* ts, uint8_t* codes, void* workspace, unsigned int* status,
                         cudaStream_t stream);
