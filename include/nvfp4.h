@@ -144,8 +144,8 @@ nvfp4_status nvfp4_quantize_fos(const void* W, int64_t N, int64_t K, float divis
  * Cholesky factor of (H + d I)^-1, d = damp * mean(diag H), in blocks of 128
  * columns.  Every step is binary32 in a fixed order (stated in
  * csrc/gptq.cu), so the codes are reproducible bit for bit.
- *   W        in:  device bf16 [N, K], K <= 14528 (the triangular inverse
- *                 keeps 4 columns of K floats in shared memory)
+ *   W        in:  device bf16 [N, K], K <= 11616 (the triangular inverse
+ *                 keeps 5 vectors of K floats in shared memory)
  *   H        in:  device fp32 [K, K], symmetric positive semi-definite (the
  *                 layer's Hessian, e.g. 2 X^T X / T over calibration tokens)
  *   damp     in:  >= 0 (GPTQ's usual 0.01)

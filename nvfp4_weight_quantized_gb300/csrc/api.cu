@@ -366,7 +366,7 @@ nvfp4_status nvfp4_gptq_fos(const void* W, int64_t N, int64_t K, const float* H,
     return fail(NVFP4_ERR_INVALID_ARG, "gptq_fos: W, H, codes and tensor_scale are required");
   if (!(damp >= 0.0f) || !std::isfinite(damp)) return fail(NVFP4_ERR_INVALID_ARG, "gptq_fos: damp must be >= 0");
   if (N <= 0 || K < 16 || K % 16 != 0 || N > kMaxElems / K || K > nvfp4::gptq_max_k())
-    return fail(NVFP4_ERR_SHAPE, "gptq_fos: need N >= 1, 16 <= K <= 14528, K % 16 == 0");
+    return fail(NVFP4_ERR_SHAPE, "gptq_fos: need N >= 1, 16 <= K <= 11616, K % 16 == 0");
   if (!aligned(H, 16)) return fail(NVFP4_ERR_ALIGN, "gptq_fos: H must be 16-byte aligned");
   const size_t gws = nvfp4::gptq_workspace_bytes(N, K), sbytes = align256((size_t)N * (size_t)(K / 16));
   if (workspace == nullptr || !aligned(workspace, 256) ||

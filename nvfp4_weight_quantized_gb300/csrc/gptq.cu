@@ -86,32 +86,51 @@ __global__ void chol_update_kernel(float* __restrict__ A, int64_t K, int64_t j) 
   A[i * K + c] = __fmaf_rn(-A[i * K + j], A[c * K + j], A[i * K + c]);
 }
 
-// Inverse of the lower factor: a CTA (one warp, kInvCols active lanes) owns
-// kInvCols consecutive columns j0 .. and keeps their entries x[k], k >= j0,
-// in shared memory ([k][lane], conflict-free); each L[i][k] is a broadcast
-// load.  A lane starts its sum at k = j0 instead of its own j: the extra
-// terms are fma(L[i][k], 0, s) = s exactly (x[k] = 0 for k < j; s starts at
-// +0), so every column gets the bits of the sum taken from k = j.
+// Inverse of the lower factor: a CTA (one warp) owns kInvCols consecutive
+// columns j0 .. and keeps their entries x[k], k >= j0, in shared memory
+// ([k][lane], conflict-free).  For each row i all 32 lanes first copy
+// L[i][j0 .. i] into shared memory (coalesced), then the kInvCols lanes take
+// their dot products from there.  A lane starts its sum at k = j0 instead of
+// its own j: the extra terms are fma(L[i][k], 0, s) = s exactly (x[k] = 0 for
+// k < j; s starts at +0), so every column gets the bits of the sum taken from
+// k = j.
 constexpr int kInvCols = 4;
 
 __global__ void __launch_bounds__(32) trinv_kernel(const float* __restrict__ L, int64_t K, float* __restrict__ li) {
-  extern __shared__ float xs[];  // [(K - j0)][kInvCols]
+  extern __shared__ float xs[];  // [(K - j0)][kInvCols], then row [K - j0]
   const int lane = threadIdx.x;
   const int64_t j0 = (int64_t)blockIdx.x * kInvCols, j = j0 + lane;
+  float* row = xs + (K - j0) * kInvCols;
   for (int64_t e = lane; e < (K - j0) * kInvCols; e += 32) xs[e] = 0.0f;
-  __syncwarp();
-  if (lane >= kInvCols || j >= K) return;
-  for (int64_t i = j; i < K; ++i) {
-    float x;
-    if (i == j) {
-      x = __fdiv_rn(1.0f, L[j * K + j]);
-    } else {
-      float s = 0.0f;
-      for (int64_t k = j0; k < i; ++k) s = __fmaf_rn(L[i * K + k], xs[(k - j0) * kInvCols + lane], s);
-      x = __fdiv_rn(-s, L[i * K + i]);
+  const bool mine = lane < kInvCols && j < K;
+  for (int64_t i = j0; i < K; ++i) {
+    {  // four loads in flight per lane
+      const float* src = L + i * K;
+      int64_t k = j0 + lane;
+      for (; k + 96 <= i; k += 128) {
+        const float v0 = src[k], v1 = src[k + 32], v2 = src[k + 64], v3 = src[k + 96];
+        row[k - j0] = v0;
+        row[k + 32 - j0] = v1;
+        row[k + 64 - j0] = v2;
+        row[k + 96 - j0] = v3;
+      }
+      for (; k <= i; k += 32) row[k - j0] = src[k];
     }
-    xs[(i - j0) * kInvCols + lane] = x;
-    li[i * K + j] = x;
+    __syncwarp();
+    if (mine && i >= j) {
+      float x;
+      if (i == j) {
+        x = __fdiv_rn(1.0f, row[i - j0]);
+      } else {
+        float s = 0.0f;
+#pragma unroll 8
+        for (int64_t k = j0; k < i; ++k) s = __fmaf_rn(row[k - j0], xs[(k - j0) * kInvCols + lane], s);
+        x = __fdiv_rn(-s, row[i - j0]);
+      }
+      xs[(i - j0) * kInvCols + lane] = x;
+      li[i * K + j] = x;
+    }
+    __syncwarp();  // the row buffer is rewritten next
   }
 }
 
@@ -182,7 +201,7 @@ __global__ void gptq_trail_kernel(float* __restrict__ wc, int64_t N, int64_t K, 
 
 }  // namespace
 
-int64_t gptq_max_k() { return (int64_t)(227 * 1024) / (kInvCols * (int64_t)sizeof(float)); }
+int64_t gptq_max_k() { return (int64_t)(227 * 1024) / ((kInvCols + 1) * (int64_t)sizeof(float)) / 16 * 16; }
 
 size_t gptq_workspace_bytes(int64_t N, int64_t K) {
   auto a256 = [](size_t b) { return (b + 255) & ~(size_t)255; };
@@ -218,7 +237,7 @@ cudaError_t launch_gptq(const void* W, int64_t N, int64_t K, const float* H, flo
   chol_diag_kernel<<<(unsigned)((K + 255) / 256), 256, 0, stream>>>(A, K, piv);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   if ((err = cudaMemsetAsync(li, 0, (size_t)K * K * 4, stream)) != cudaSuccess) return err;
-  const size_t inv_smem = (size_t)K * kInvCols * sizeof(float);
+  const size_t inv_smem = (size_t)K * (kInvCols + 1) * sizeof(float);
   if ((err = cudaFuncSetAttribute(trinv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)inv_smem)) !=
       cudaSuccess)
     return err;
