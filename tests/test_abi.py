@@ -182,3 +182,33 @@ def test_product_path_has_no_oracle_dependency():
     for path in glob.glob(os.path.join(pkg, "**", "*"), recursive=True):
         if path.endswith((".py", ".cu", ".cuh", ".h")):
             assert not pat.search(open(path).read()), path
+
+
+def test_new_call_argument_errors(L):
+    """Argument checks of the gated-MLP, GPTQ, dequantisation and QAT calls
+    return before any device work."""
+    sm = L.nvfp4_linear_silu_mul
+    assert sm(FAKE, 4, ctypes.byref(_w(N=255)), FAKE, 0, FAKE, 1 << 30, None) == nv.ERR_SHAPE  # odd N
+    assert sm(FAKE, -1, ctypes.byref(_w()), FAKE, 0, FAKE, 1 << 30, None) == nv.ERR_SHAPE
+    assert sm(None, 4, ctypes.byref(_w()), FAKE, 0, FAKE, 1 << 30, None) == nv.ERR_INVALID_ARG
+    assert sm(FAKE + 8, 4, ctypes.byref(_w()), FAKE, 0, FAKE, 1 << 30, None) == nv.ERR_ALIGN
+    assert sm(FAKE, 4, ctypes.byref(_w()), FAKE, 0, FAKE, 16, None) == nv.ERR_WORKSPACE
+    assert sm(FAKE, 4, ctypes.byref(_w()), FAKE, 9, FAKE, 1 << 30, None) == nv.ERR_INVALID_ARG
+    assert sm(None, 0, ctypes.byref(_w()), None, 0, None, 0, None) == nv.OK
+    gq = L.nvfp4_gptq_fos
+    assert gq(FAKE, 64, 256, None, 0.01, FAKE, None, FAKE, FAKE, FAKE, 1 << 30, None) == nv.ERR_INVALID_ARG
+    assert gq(FAKE, 64, 256, FAKE, -1.0, FAKE, None, FAKE, FAKE, FAKE, 1 << 30, None) == nv.ERR_INVALID_ARG
+    assert gq(FAKE, 64, 250, FAKE, 0.01, FAKE, None, FAKE, FAKE, FAKE, 1 << 30, None) == nv.ERR_SHAPE
+    assert gq(FAKE, 64, 16384, FAKE, 0.01, FAKE, None, FAKE, FAKE, FAKE, 1 << 40, None) == nv.ERR_SHAPE
+    assert gq(FAKE, 64, 256, FAKE + 4, 0.01, FAKE, None, FAKE, FAKE, FAKE, 1 << 30, None) == nv.ERR_ALIGN
+    assert gq(FAKE, 64, 256, FAKE, 0.01, FAKE, None, FAKE, FAKE, FAKE, 1024, None) == nv.ERR_WORKSPACE
+    dq = L.nvfp4_dequantize
+    assert dq(None, FAKE, FAKE, 4, 64, FAKE, None) == nv.ERR_INVALID_ARG
+    assert dq(FAKE, FAKE, FAKE, 4, 40, FAKE, None) == nv.ERR_SHAPE
+    assert dq(FAKE, FAKE, FAKE, 4, 64, FAKE + 2, None) == nv.ERR_ALIGN
+    assert dq(FAKE, FAKE, FAKE, 0, 64, FAKE, None) == nv.OK
+    qb = L.nvfp4_qat_backward
+    assert qb(FAKE, 4, ctypes.byref(_w()), None, None, None, None, None, FAKE, 1 << 30, None) == nv.OK  # nothing asked
+    assert qb(None, 4, ctypes.byref(_w()), None, None, None, FAKE, None, FAKE, 1 << 30, None) == nv.ERR_INVALID_ARG
+    assert qb(FAKE, 4, ctypes.byref(_w()), None, None, None, None, FAKE, FAKE, 1 << 30, None) == nv.ERR_INVALID_ARG
+    assert qb(FAKE, 4, ctypes.byref(_w()), None, None, None, FAKE, None, FAKE, 16, None) == nv.ERR_WORKSPACE
