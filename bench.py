@@ -802,6 +802,9 @@ def profile_case(which: str, m_decode: int):
         qp = nv.nvfp4_quantize_fos(bf(synth.prefill_weight()), logical_scales=False, choice=False)
         a = nv.nvfp4_quantize_act(bf(synth.prefill_act(2048)))
         nv.nvfp4_gemm_w4a4(a, qp)
+    if which == "gate_up":  # the gated MLP projection, fused form, on the config-3 gate/up weight
+        qg = nv.nvfp4_quantize_fos(bf(synth.mlp_weights()[0]), logical_scales=False, choice=False)
+        nv.nvfp4_linear_silu_mul(bf(synth.prefill_act(2048)), qg)
     torch.cuda.synchronize()
     print("profile case", which, "status", nv.nvfp4_status_string(nv.nvfp4_get_device_status()))
 
@@ -816,7 +819,7 @@ def main():
     ap.add_argument("--cpu-rows-reference", type=int, default=64)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["all", "quant", "w4a16", "w4a4"],
+    ap.add_argument("--profile-case", choices=["all", "quant", "w4a16", "w4a4", "gate_up"],
                     help="launch each hot kernel once on a small case (for ncu) and exit")
     ap.add_argument("--profile-m", type=int, default=16, help="decode M of --profile-case")
     args = ap.parse_args()
