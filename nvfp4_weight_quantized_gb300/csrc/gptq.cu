@@ -15,9 +15,11 @@
 // the same bits):
 //   gptq_damp_kernel      d = damp * ((sum_k H[k][k], k ascending) / K)
 //   gptq_reverse_kernel   A = J (H + d I) J  (J reverses indices)
-//   chol_col_kernel / chol_update_kernel, once per column j (right-looking):
+//   chol_panel_kernel / chol_trail_kernel, right-looking, column j in order:
 //                         L[j][j] = sqrt(A[j][j]); L[i][j] = A[i][j] / L[j][j];
 //                         A[i][c] = fma(-L[i][j], L[c][j], A[i][c]), j < c <= i
+//                         (in 32-column panels: the same operations on every
+//                         element in the same order, 2K / 32 launches)
 //   trinv_kernel          Linv = L^-1 by columns: x[j] = 1 / L[j][j],
 //                         x[i] = -(sum_{k=j}^{i-1} fma(L[i][k], x[k], .)) / L[i][i]
 //                         (U = J Linv J, read through reversed indices)
@@ -56,34 +58,101 @@ __global__ void gptq_reverse_kernel(const float* __restrict__ H, int64_t K, cons
   }
 }
 
-// Column j of the factor: the pivot (kept in piv[j]; A[j][j] is still read
-// by every CTA of this launch, and later launches never read it) and the
-// scaled column below it.
-__global__ void chol_col_kernel(float* __restrict__ A, int64_t K, int64_t j, float* __restrict__ piv,
-                                unsigned int* __restrict__ status) {
-  const float a = A[j * K + j];
-  if (!(a > 0.0f)) {  // not positive definite (or non-finite): flag it
-    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, kStatusNonfinite);
-    return;
+// Panelled form of the column loop: 32 columns at a time in two launches,
+// each element receiving the same fused multiply-adds in the same order.
+// chol_panel_kernel: every CTA redundantly factors the panel's top 32 x 32
+// block in shared memory (identical arithmetic in every CTA), CTA 0 writes
+// it back, and each CTA then finishes its own rows below the panel top:
+// for j in the panel, L[i][j] = A[i][j] / p_j, then the panel's later
+// columns of the row get fma(-L[i][j], L[c][j], .).
+constexpr int kPanel = 32;
+constexpr int kPanelRows = 256;  // rows below the top block per CTA (one per thread)
+
+__global__ void __launch_bounds__(kPanelRows)
+chol_panel_kernel(float* __restrict__ A, int64_t K, int64_t p0, float* __restrict__ piv,
+                  unsigned int* __restrict__ status) {
+  __shared__ float top[kPanel][kPanel + 1];
+  __shared__ float pv[kPanel];
+  const int pw = (int)(K - p0 < kPanel ? K - p0 : kPanel);
+  const int t = threadIdx.x;
+  for (int e = t; e < pw * pw; e += blockDim.x) {
+    const int r = e / pw, c = e - r * pw;
+    top[r][c] = A[(p0 + r) * K + p0 + c];
   }
-  const float p = __fsqrt_rn(a);
-  for (int64_t i = j + 1 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < K; i += (int64_t)gridDim.x * blockDim.x)
-    A[i * K + j] = __fdiv_rn(A[i * K + j], p);
-  if (blockIdx.x == 0 && threadIdx.x == 0) piv[j] = p;
+  __syncthreads();
+  // the top block, column by column (lower triangle, c <= r)
+  for (int j = 0; j < pw; ++j) {
+    if (t == 0) {
+      const float a = top[j][j];
+      if (!(a > 0.0f)) atomicOr(status, kStatusNonfinite);
+      pv[j] = __fsqrt_rn(a);
+    }
+    __syncthreads();
+    const float p = pv[j];
+    for (int r = j + 1 + t; r < pw; r += blockDim.x) top[r][j] = __fdiv_rn(top[r][j], p);
+    __syncthreads();
+    for (int e = t; e < pw * pw; e += blockDim.x) {
+      const int r = e / pw, c = e - r * pw;
+      if (r > j && c > j && c <= r) top[r][c] = __fmaf_rn(-top[r][j], top[c][j], top[r][c]);
+    }
+    __syncthreads();
+  }
+  if (blockIdx.x == 0) {
+    for (int e = t; e < pw * pw; e += blockDim.x) {
+      const int r = e / pw, c = e - r * pw;
+      if (c < r) A[(p0 + r) * K + p0 + c] = top[r][c];
+      else if (c == r) piv[p0 + r] = pv[r];
+    }
+  }
+  // rows below the top block
+  const int64_t i = p0 + pw + (int64_t)blockIdx.x * kPanelRows + t;
+  if (i >= K) return;
+  float w[kPanel];
+#pragma unroll
+  for (int c = 0; c < kPanel; ++c) w[c] = c < pw ? A[i * K + p0 + c] : 0.0f;
+#pragma unroll
+  for (int j = 0; j < kPanel; ++j) {
+    if (j < pw) {
+      w[j] = __fdiv_rn(w[j], pv[j]);
+#pragma unroll
+      for (int c = j + 1; c < kPanel; ++c)
+        if (c < pw) w[c] = __fmaf_rn(-w[j], top[c][j], w[c]);
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < kPanel; ++c)
+    if (c < pw) A[i * K + p0 + c] = w[c];
+}
+
+// Elements (i, c), pend <= c <= i < K: the panel's updates in column order,
+// 32 columns x 8 rows per CTA with the panel rows of those columns and rows
+// in shared memory.
+__global__ void __launch_bounds__(256)
+chol_trail_kernel(float* __restrict__ A, int64_t K, int64_t p0, int pw) {
+  __shared__ float lc[32][kPanel + 1], lr[8][kPanel + 1];
+  const int64_t pend = p0 + pw;
+  const int64_t c0 = pend + (int64_t)blockIdx.x * 32, i0 = pend + (int64_t)blockIdx.y * 8;
+  if (i0 + 7 < c0) return;  // wholly above the diagonal
+  const int tx = threadIdx.x, ty = threadIdx.y, t = ty * 32 + tx;
+  for (int e = t; e < 32 * pw; e += 256) {
+    const int r = e / pw, q = e - r * pw;
+    lc[r][q] = c0 + r < K ? A[(c0 + r) * K + p0 + q] : 0.0f;
+  }
+  for (int e = t; e < 8 * pw; e += 256) {
+    const int r = e / pw, q = e - r * pw;
+    lr[r][q] = i0 + r < K ? A[(i0 + r) * K + p0 + q] : 0.0f;
+  }
+  __syncthreads();
+  const int64_t c = c0 + tx, i = i0 + ty;
+  if (i >= K || c > i) return;
+  float v = A[i * K + c];
+  for (int q = 0; q < pw; ++q) v = __fmaf_rn(-lr[ty][q], lc[tx][q], v);
+  A[i * K + c] = v;
 }
 
 __global__ void chol_diag_kernel(float* __restrict__ A, int64_t K, const float* __restrict__ piv) {
   for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < K; j += (int64_t)gridDim.x * blockDim.x)
     A[j * K + j] = piv[j];
-}
-
-// Rank-1 update of the trailing lower triangle: rows i in (j, K) on y, columns
-// c in (j, i] on x.
-__global__ void chol_update_kernel(float* __restrict__ A, int64_t K, int64_t j) {
-  const int64_t i = j + 1 + (int64_t)blockIdx.y * blockDim.y + threadIdx.y;
-  const int64_t c = j + 1 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= K || c > i) return;
-  A[i * K + c] = __fmaf_rn(-A[i * K + j], A[c * K + j], A[i * K + c]);
 }
 
 // Inverse of the lower factor: a CTA (one warp) owns kInvCols consecutive
@@ -226,12 +295,14 @@ cudaError_t launch_gptq(const void* W, int64_t N, int64_t K, const float* H, flo
   cudaError_t err;
   gptq_damp_kernel<<<1, 32, 0, stream>>>(H, K, damp, d);
   gptq_reverse_kernel<<<1024, 256, 0, stream>>>(H, K, d, A);
-  for (int64_t j = 0; j < K; ++j) {
-    chol_col_kernel<<<(unsigned)std::max<int64_t>(1, (K - j + 255) / 256), 256, 0, stream>>>(A, K, j, piv, status);
-    const int64_t m = K - j - 1;
-    if (m > 0) {
-      dim3 blk(32, 8), grid((unsigned)((m + 31) / 32), (unsigned)((m + 7) / 8));
-      chol_update_kernel<<<grid, blk, 0, stream>>>(A, K, j);
+  for (int64_t p0 = 0; p0 < K; p0 += kPanel) {
+    const int pw = (int)std::min<int64_t>(kPanel, K - p0);
+    const int64_t below = K - p0 - pw;
+    chol_panel_kernel<<<(unsigned)std::max<int64_t>(1, (below + kPanelRows - 1) / kPanelRows), kPanelRows, 0,
+                        stream>>>(A, K, p0, piv, status);
+    if (below > 0) {
+      dim3 blk(32, 8), grid((unsigned)((below + 31) / 32), (unsigned)((below + 7) / 8));
+      chol_trail_kernel<<<grid, blk, 0, stream>>>(A, K, p0, pw);
     }
   }
   chol_diag_kernel<<<(unsigned)((K + 255) / 256), 256, 0, stream>>>(A, K, piv);
