@@ -230,8 +230,10 @@ nvfp4_status nvfp4_linear(const void* X, int64_t M, const nvfp4_weight* W, void*
                           cudaStream_t stream);
 
 /*
- * Gated MLP input projection (the survey's next-2 fusion; the pages fuse
- * elementwise epilogues of other layers the same way): W is the concatenated
+ * Gated MLP input projection.  "SOAR 2026 Recap ...", section "2. Hybrid
+ * attention backend optimization" (GLA linear attention, kernel fusion),
+ * fuses an output gate's elementwise work into one kernel with the values
+ * kept in registers; this call applies that idea to the MLP's gate: W is the concatenated
  * gate/up weight [2F, K] (rows [0, F) gate, [F, 2F) up), and
  *   Y[m, f] = silu(G[m, f]) * U[m, f],  silu(g) = g / (1 + e^-g),
  * with G = X W_gate^T and U = X W_up^T computed as nvfp4_linear would (same
