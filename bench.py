@@ -162,6 +162,24 @@ def traffic_from_profiles(kernel_key: str, src_files: dict):
         return None
 
 
+def max_over_ranks(x: float, dev) -> float:
+    """The largest x over all ranks (the replicas' common clock: the job is as
+    slow as its slowest replica); x itself without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], device=dev, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(step_bytes: int, steps: int, world: int, elapsed: float) -> float:
+    """Whole-job GB/s of `world` replicas that each ran `steps` steps of
+    `step_bytes` in at most `elapsed` seconds."""
+    return step_bytes * steps * world / elapsed / 1e9
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -283,17 +301,13 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    elapsed = t_start.elapsed_time(t_end) * 1e-3
-    if world > 1:
-        t = torch.tensor([elapsed], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(t_start.elapsed_time(t_end) * 1e-3, dev)
 
     step_bytes = q_bytes(N, K) + sum(
         w4a16_bytes(M, N, K) if paths[M] == "w4a16" else actq_bytes(M, K) + w4a4_bytes(M, N, K)
         for M in DECODE_M)
     ms_per_step = elapsed / K_steps * 1e3
-    value = step_bytes * K_steps * world / elapsed / 1e9
+    value = replica_value(step_bytes, K_steps, world, elapsed)
 
     # dominant kernel family of the step
     w16_time = sum(lin_avg[M] for M in DECODE_M if paths[M] == "w4a16")
