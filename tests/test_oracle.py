@@ -542,3 +542,20 @@ def test_gptq_lowers_layer_error():
         d = W - _dequant64(codes, f["scales"], f["ts"])
         return float(np.einsum("nk,kl,nl->", d, H64, d))
     assert err(g["codes"]) < 0.9 * err(f["codes"])
+
+
+def test_silu_mul_reference_closed_forms():
+    """The binary64 silu(g) * u of the test utilities at points with closed
+    forms: 0 at g = 0, the logistic value at g = 1, the limits g (g >> 0) and
+    0 (g << 0, where exp overflows), the identity silu(g) - silu(-g) = g, and
+    linearity in u."""
+    from nvfp4_testutil import silu_mul_ref
+    g = np.array([0.0, 1.0, -1.0, 40.0, -40.0, 800.0, -800.0, 2.5])
+    u = np.ones_like(g)
+    y = silu_mul_ref(g, u)
+    assert y[0] == 0.0
+    assert y[1] == pytest.approx(1.0 / (1.0 + np.exp(-1.0)), rel=1e-15)
+    assert y[1] - y[2] == pytest.approx(1.0, rel=1e-15)        # silu(g) - silu(-g) = g
+    assert y[3] == pytest.approx(40.0, rel=1e-15) and abs(y[4]) < 1e-15
+    assert y[5] == 800.0 and y[6] == 0.0                        # exp overflow handled
+    assert silu_mul_ref(np.array([2.5]), np.array([-3.0]))[0] == pytest.approx(-3.0 * y[7], rel=1e-15)
