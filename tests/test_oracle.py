@@ -559,3 +559,41 @@ def test_silu_mul_reference_closed_forms():
     assert y[3] == pytest.approx(40.0, rel=1e-15) and abs(y[4]) < 1e-15
     assert y[5] == 800.0 and y[6] == 0.0                        # exp overflow handled
     assert silu_mul_ref(np.array([2.5]), np.array([-3.0]))[0] == pytest.approx(-3.0 * y[7], rel=1e-15)
+
+
+@pytest.mark.parametrize("damp,block", [(0.01, 16), (0.5, 128)])
+def test_gptq_codes_round_the_least_squares_continuation(damp, block):
+    """GPTQ's defining property, checked without its Cholesky steps: when
+    column i is quantised, the working row is the minimiser of the layer error
+    (w0 - w) Hd (w0 - w)^T over the columns >= i with the columns < i held at
+    their quantised values (Hd = H + damp * mean(diag H) * I).  That
+    continuation is w0[i:] + Hd[i:, i:]^-1 Hd[i:, :i] (w0 - q)[:i], solved
+    here in binary64 for every column; each code must be the E2M1 value
+    nearest to its column under the block's fixed scale (saturating at 6).
+    Elements within 1e-3 of a rounding midpoint are skipped."""
+    N, K = 6, 64
+    w = synth.weight_normal(N, K, seed=26, outlier_frac=0.02)
+    H = _hessian(K, 1024, 27)
+    g = oracle.gptq_fos(w, H, damp=damp, block=block)
+    W0 = synth.bf16_bits_to_f32(w).astype(np.float64)
+    H64 = H.astype(np.float64)
+    Hd = H64 + damp * np.mean(np.diag(H64)) * np.eye(K)
+    Q = _dequant64(g["codes"], g["scales"], g["ts"])
+    e4 = np.array([oracle.e4m3_value(b) if (b & 0x7F) != 0x7F else 0.0 for b in range(256)])
+    unit = np.repeat(e4[g["scales"]], 16, axis=1) * g["ts"]
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    checked = 0
+    for r in range(N):
+        for i in range(K):
+            assert unit[r, i] > 0
+            eF = W0[r, :i] - Q[r, :i]
+            u = W0[r, i:] + (np.linalg.solve(Hd[i:, i:], Hd[i:, :i] @ eF) if i else 0.0)
+            x = u[0] / unit[r, i]
+            d = np.sort(np.abs(grid - abs(x)))
+            if d[1] - d[0] < 1e-3:
+                continue
+            want = np.copysign(grid[np.argmin(np.abs(grid - abs(x)))], x)
+            assert Q[r, i] / unit[r, i] == want, (r, i, x)
+            checked += 1
+    assert checked >= 0.95 * N * K
+    assert not np.array_equal(g["codes"], oracle.quantize_fos(w)["codes"])  # errors were spread
