@@ -455,6 +455,29 @@ def test_dequant_bf16_rounding_bound():
         assert np.all(np.diff(got.reshape(-1)[o]) >= 0)
 
 
+def test_dequant_bf16_ties_by_hand():
+    """Round-to-nearest-even at both steps, worked by hand on a block with
+    scale 0x38 (value 1):
+    - code 2 (+1) and code 0xA (-1) times ts = 1 + 2^-8: the binary32 product
+      is exact and is the midpoint of the bf16 values 1 (0x3f80) and 1 + 2^-7
+      (0x3f81), so the even 0x3f80; with ts = 1 + 3 * 2^-8 the midpoint of
+      0x3f81 and 0x3f82, so 0x3f82;
+    - code 3 (+1.5) and 0xB (-1.5) times ts = 11228502 * 2^-24: the exact
+      product is 1 + 2^-8 + 2^-24, a binary32 tie that rounds to the even
+      1 + 2^-8, itself a bf16 tie, so 0x3f80 (rounding the exact product to
+      bf16 in one step would give 0x3f81)."""
+    scales = np.array([[0x38]], np.uint8)
+    cases = [(0x02 | (0x0A << 4), 1.0 + 2.0 ** -8, 0x3F80),
+             (0x02 | (0x0A << 4), 1.0 + 3 * 2.0 ** -8, 0x3F82),
+             (0x03 | (0x0B << 4), 11228502 * 2.0 ** -24, 0x3F80)]
+    for byte, ts, want in cases:
+        assert float(np.float32(ts)) == ts
+        codes = np.array([[byte] + [0] * 7], np.uint8)
+        got = oracle.dequant_bf16(codes, scales, ts)[0]
+        assert list(got[:2]) == [want, want | 0x8000], (hex(byte), ts)
+        assert not got[2:].any()
+
+
 def test_dequant_bf16_agrees_with_gemm_oracle():
     """Against the GEMM oracle's own binary64 dequantisation (unit-vector
     activations pick out W_hat): equal up to the two roundings."""

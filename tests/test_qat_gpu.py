@@ -61,3 +61,21 @@ def test_qat_backward(MNK):
     assert none is None and torch.equal(dX2, dX)
     none, dW2 = nv.nvfp4_qat_backward(to_dev(dy), W, A, want_dx=False)
     assert none is None and torch.equal(dW2, dW)
+
+
+def test_dequantize_ties_by_hand():
+    """The oracle's by-hand round-to-nearest-even cases on the GPU: block
+    scale 0x38 (value 1), codes +-1 or +-1.5, tensor scales that make the
+    binary32 product a bf16 midpoint (exactly, or after a binary32 tie)."""
+    cases = [(0x02 | (0x0A << 4), 1.0 + 2.0 ** -8, 0x3F80),
+             (0x02 | (0x0A << 4), 1.0 + 3 * 2.0 ** -8, 0x3F82),
+             (0x03 | (0x0B << 4), 11228502 * 2.0 ** -24, 0x3F80)]
+    smma = np.zeros(512, np.uint8)  # one 128 x 4 scale tile; scale (0, 0) at byte 0
+    smma[0] = 0x38
+    for byte, ts, want in cases:
+        codes = np.array([[byte] + [0] * 7], np.uint8)
+        Y = nv.nvfp4_dequantize(torch.from_numpy(codes).cuda(), torch.from_numpy(smma).cuda(),
+                                torch.tensor([ts], dtype=torch.float32, device="cuda"), 1, 16)
+        got = _bits(Y)[0]
+        assert list(got[:2]) == [want, want | 0x8000] and not got[2:].any(), (hex(byte), ts)
+        assert np.array_equal(got, oracle.dequant_bf16(codes, np.array([[0x38]], np.uint8), ts)[0])
