@@ -178,6 +178,56 @@ def test_block_scale_ties_on_the_e4m3_grid():
     check_fos(w)
 
 
+def _blocks_to_rows(blocks, per_row=64):
+    """Blocks [n, 16] of bf16 bits laid out as rows of per_row blocks (zero
+    blocks pad the last row)."""
+    rows = -(-len(blocks) // per_row)
+    pad = np.zeros((rows * per_row - len(blocks), 16), np.uint16)
+    return np.concatenate([blocks, pad]).reshape(rows, per_row * 16)
+
+
+def every_bf16_below_block_max():
+    """Every finite bf16 value of magnitude <= 6, both signs, 15 to a block
+    behind a 6; one leading block holds 2688 so that the tensor scale is 1."""
+    pos = np.arange(0, 0x40C0 + 1, dtype=np.uint16)  # +0 .. 6.0
+    vals = np.concatenate([pos, pos | np.uint16(0x8000)])
+    n = -(-len(vals) // 15)
+    vals = np.concatenate([vals, np.zeros(n * 15 - len(vals), np.uint16)])
+    blocks = np.zeros((n + 1, 16), np.uint16)
+    blocks[0, 0] = 0x4528  # 2688
+    blocks[1:, 0] = 0x40C0  # 6.0
+    blocks[1:, 1:] = vals.reshape(n, 15)
+    return _blocks_to_rows(blocks)
+
+
+def every_bf16_as_block_max():
+    """Every positive finite bf16 value up to 2688 as the maximum of its own
+    block, beside a partner of 0.3 times it; 2688 itself makes ts = 1."""
+    v = np.arange(1, 0x4528 + 1, dtype=np.uint16)
+    partner = synth.f32_to_bf16_bits((synth.bf16_bits_to_f32(v) * np.float32(0.3)).astype(np.float32))
+    blocks = np.zeros((len(v), 16), np.uint16)
+    blocks[:, 0] = v
+    blocks[:, 7] = partner
+    return _blocks_to_rows(blocks)
+
+
+def test_every_bf16_value_below_the_block_max():
+    """With ts = 1 and block maximum 6 the M=6 candidate divides by 1 and the
+    M=4 candidate by 1.5: every finite bf16 input of magnitude <= 6 goes
+    through both E2M1 roundings, in the weight and the activation quantiser."""
+    w = every_bf16_below_block_max()
+    assert check_fos(w)["ts"] == 1.0
+    check_act(w)
+
+
+def test_every_bf16_value_as_a_block_max():
+    """Every M=6 scale E4M3(v / 6) for v over all positive finite bf16 values
+    up to 2688 (subnormal scales to 448), and the M=4 scale derived from it."""
+    w = every_bf16_as_block_max()
+    assert check_fos(w)["ts"] == 1.0
+    check_act(w)
+
+
 def test_zero_and_negative_zero():
     z = np.zeros((4, 64), np.uint16)
     z[1, 5] = 0x8000
