@@ -212,3 +212,15 @@ def test_new_call_argument_errors(L):
     assert qb(None, 4, ctypes.byref(_w()), None, None, None, FAKE, None, FAKE, 1 << 30, None) == nv.ERR_INVALID_ARG
     assert qb(FAKE, 4, ctypes.byref(_w()), None, None, None, None, FAKE, FAKE, 1 << 30, None) == nv.ERR_INVALID_ARG
     assert qb(FAKE, 4, ctypes.byref(_w()), None, None, None, FAKE, None, FAKE, 16, None) == nv.ERR_WORKSPACE
+
+
+def test_crossover_rule_from_timings():
+    """The tuner's rule on hand-made timings {M: (t_w4a16, t_w4a4)}: the
+    largest M where W4A16 is no slower, scanning up until W4A4 wins twice
+    in a row (one noisy loss does not end the scan)."""
+    from nvfp4_weight_quantized_gb300.tune import crossover_from
+    assert crossover_from({1: (1, 2), 8: (1, 2), 16: (3, 2), 32: (3, 2), 48: (1, 2)}) == 8
+    assert crossover_from({1: (1, 2), 8: (3, 2), 16: (1, 2), 32: (3, 2), 64: (3, 2)}) == 16
+    assert crossover_from({1: (2, 2), 4: (2, 2)}) == 4        # a tie keeps W4A16
+    assert crossover_from({1: (3, 2), 2: (3, 2), 4: (1, 2)}) == 0
+    assert crossover_from({64: (1, 2), 1: (3, 2), 8: (1, 2)}) == 64  # keys are sorted
