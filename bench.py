@@ -316,11 +316,10 @@ def run_ours(args):
         dom = "gemm_w4a16 (w4a16_sk_kernel for M <= 8, w4a16_rf_kernel above)"
         achieved = w16_bytes / w16_time / 1e9
         csrc = os.path.join(ROOT, "nvfp4_weight_quantized_gb300", "csrc")
+        # DRAM bytes per launch, averaged over the decode M sweep
         traffic = traffic_from_profiles("w4a16_decode", {"sk": os.path.join(csrc, "gemm_w4a16_sk.cu"),
                                                          "rf": os.path.join(csrc, "gemm_w4a16_rf.cu")})
         launches = sum(1 for M in DECODE_M if paths[M] == "w4a16")
-        if traffic is not None:
-            traffic = traffic  # bytes per launch averaged over the M sweep
     else:
         dom = "quantize_fos"
         achieved = q_bytes(N, K) / q_avg / 1e9
