@@ -197,7 +197,7 @@ def run_ours(args):
     build.build()
     nv.lib()
 
-    hbm_peak, bf16_peak, peak_src = peaks()
+    hbm_peak, _, peak_src = peaks()
     N, K = N_DEC, K_DEC
     w_bits = synth.decode_weight()
     W0 = torch.from_numpy(w_bits.view(np.int16)).view(torch.bfloat16).to(dev)
@@ -400,7 +400,7 @@ def prefill_sweep(nv, dev, stream):
         stream.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for r in range(reps):
+            for _ in range(reps):
                 nv.nvfp4_gemm_w4a4(a, qp, out=Y, stream=stream)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):  # replay() launches on the current stream
