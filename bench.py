@@ -347,6 +347,7 @@ def run_ours(args):
         detail["gate_up_silu_mul"] = gate_up_bench(nv, dev, stream)
         detail["qat_step"] = qat_bench(nv, dev, stream)
         detail["gptq_fos"] = gptq_bench(nv, dev, stream)
+        detail["mlp_decode"] = guarded(mlp_decode_bench, nv, dev, stream)
 
     e2e = measure_e2e(nv, dev, stream, w_bits, args, step_bytes, paths) if rank == 0 else None
 
@@ -525,6 +526,69 @@ def gate_up_bench(nv, dev, stream):
             res[str(M)]["silu_mul_tflops"] = round(2 * M * N * K / t1 / 1e12, 1)
         del ws1, ws2, Y1, Y2, X
     return res
+
+
+def mlp_decode_bench(nv, dev, stream):
+    """The MLP-shaped linears at decode sizes (gate/up W [2 x 11008, 4096] and
+    down W [4096, 11008], N(0, 0.02^2) x per-row lognormal(0, 0.5);
+    X [M, K] ~ N(0, 1), M in {1, 8, 32, 48}): nvfp4_linear with enough weight
+    copies to rotate over more than 4x L2, so every call reads cold weights
+    (one CUDA graph of one call per copy, replayed once warm, then timed), and
+    the share of blocks that keep the M=4 scale on these weights."""
+    import torch
+    bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
+    hbm_peak = peaks()[0]
+    res = {}
+    for name, w in zip(("gate_up", "down"), synth.mlp_weights()):
+        q = nv.nvfp4_quantize_fos(bf(w), logical_scales=False, choice=True)
+        N, K = q.N, q.K
+        wbytes = N * K // 2 + nv.nvfp4_scales_mma_bytes(N, K)
+        n_copies = max(4, -(-4 * 126 * 2**20 // wbytes))
+        copies = [q] + [nv.NVFP4Weight(q.codes.clone(), q.scales_mma.clone(), q.tensor_scale.clone(), N, K)
+                        for _ in range(n_copies - 1)]
+        cross = nv.nvfp4_get_crossover(N, K)
+        torch.cuda.synchronize()  # made on the default stream, used on `stream`
+        row = {"N": N, "K": K, "weight_copies": n_copies, "crossover_m": cross,
+               "m4_block_fraction": round(float(q.m4_count.item()) / (N * K // 16), 4)}
+        for M in synth.MLP_M:
+            X = bf(synth.act_normal(M, K, seed=320 + M))
+            Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ws = torch.empty(max(nv.nvfp4_workspace_bytes(nv.OP_LINEAR, M, N, K), 256), dtype=torch.uint8,
+                             device=dev)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                nv.nvfp4_linear(X, copies[0], out=Y, workspace=ws, stream=stream)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for c in copies:
+                    nv.nvfp4_linear(X, c, out=Y, workspace=ws, stream=stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):  # replay() launches on the current stream
+                g.replay()
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+            e1.synchronize()
+            t = e0.elapsed_time(e1) * 1e-3 / n_copies
+            path = "w4a16" if M <= cross else "w4a4"
+            nbytes = w4a16_bytes(M, N, K) if path == "w4a16" else actq_bytes(M, K) + w4a4_bytes(M, N, K)
+            row[str(M)] = {"path": path, "us": round(t * 1e6, 2), "gbs": round(nbytes / t / 1e9, 1),
+                           "frac_hbm": round(nbytes / t / 1e9 / hbm_peak, 3)}
+            del g, X, Y, ws
+        res[name] = row
+        del copies, q
+        torch.cuda.synchronize()
+    return res
+
+
+def guarded(fn, *args):
+    """fn(*args), or {"error": ...} if it raises: a failing detail measurement
+    is reported in the JSON line instead of ending the run."""
+    try:
+        return fn(*args)
+    except Exception as e:  # noqa: BLE001
+        return {"error": f"{type(e).__name__}: {e}"}
 
 
 def qat_bench(nv, dev, stream, M=4096):
