@@ -42,7 +42,11 @@
  *     (nvfp4_set_w4a16_rf_max_m, nvfp4_set_w4a16_sk_max_m), the W4A4 kernel
  *     knob (nvfp4_set_w4a4_cluster), the activation FourOverSix flag
  *     (nvfp4_set_act_fos), the weight-prefetch flag
- *     (nvfp4_set_weight_prefetch) and the device status word.
+ *     (nvfp4_set_weight_prefetch) and the device status word, besides
+ *     host-side lookups made once (the driver's tensor-map encoder, per-kernel
+ *     occupancy, per-device attributes, one cuBLAS handle per device for
+ *     nvfp4_qat_backward) and the static scratch array of
+ *     nvfp4_linear_noalloc.  Tensor maps are encoded on every call.
  */
 #ifndef NVFP4_H_
 #define NVFP4_H_
@@ -64,7 +68,7 @@ typedef enum nvfp4_status {
   NVFP4_ERR_NONFINITE = 5,   /* an input held Inf or NaN (device-detected) */
   NVFP4_ERR_TIMEOUT = 6,     /* a bounded device-side wait ran out (device-detected) */
   NVFP4_ERR_CUDA = 7,        /* a CUDA runtime or driver call failed */
-  NVFP4_ERR_UNSUPPORTED = 8  /* no sm_100-family GPU, or a size the kernels do not handle */
+  NVFP4_ERR_UNSUPPORTED = 8  /* the current GPU is not an sm_103 (GB300), or a size the kernels do not handle */
 } nvfp4_status;
 
 /* Output element type of the GEMMs. */
@@ -109,9 +113,12 @@ size_t nvfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
  * For each 16-element block: s6 = E4M3((amax_block / 6) / ts),
  * s4 = E4M3(value(s6) * 1.5); each candidate quantises the block with
  * q = E2M1(x / (value(s) * ts)) and scores it by the binary32 sum of squared
- * dequantisation errors (fixed tree order); the block keeps s4 only if its
- * error is strictly smaller.  All steps are IEEE binary32, round to nearest
- * even, no FMA contraction; E4M3 and E2M1 conversions saturate (448, 6).
+ * dequantisation errors in a fixed order: d = x - value(q) * value(s) * ts
+ * rounded once, a_j = d_j^2 + d_(j+8)^2 with one rounding after the second
+ * square, then b_j = a_j + a_(j+4), c_j = b_j + b_(j+2), SSE = c_0 + c_1; the
+ * block keeps s4 only if its SSE is strictly smaller.  Every step is IEEE
+ * binary32, round to nearest even, with no other fused or reordered
+ * operation; E4M3 and E2M1 conversions saturate (448, 6).
  *
  *   W            in:  device bf16 [N, K]
  *   N, K         N >= 1, K >= 16, K % 16 == 0
