@@ -173,11 +173,15 @@ nvfp4_status nvfp4_gptq_fos(const void* W, int64_t N, int64_t K, const float* H,
  * no activation rule; this library uses the standard M=6 scale only, with the
  * same binary32 steps and tensor scale as the weight quantiser).
  *
- *   X            in:  device bf16 [M, K], M >= 1, K % 16 == 0
+ *   X            in:  device bf16 [M, K], M >= 1, K >= 16, K % 16 == 0
+ *   divisor      tensor-scale divisor; <= 0 or non-finite selects 6 * 448
  *   codes        out: device [M, K/2]                           (required)
  *   scales       out: device [M, K/16] logical                  (nullable)
  *   scales_mma   out: device, nvfp4_scales_mma_bytes(M, K) bytes (nullable)
  *   tensor_scale out: device, 1 float                           (required)
+ *   workspace    device scratch of nvfp4_workspace_bytes(NVFP4_OP_QUANTIZE_ACT, M, 0, K)
+ * At least one of scales / scales_mma must be given.  A non-finite input is
+ * recorded as in nvfp4_quantize_fos.
  */
 nvfp4_status nvfp4_quantize_act(const void* X, int64_t M, int64_t K, float divisor,
                                 uint8_t* codes, uint8_t* scales, uint8_t* scales_mma,
@@ -188,7 +192,8 @@ nvfp4_status nvfp4_quantize_act(const void* X, int64_t M, int64_t K, float divis
  * W4A16 GEMM ("SOAR 2026 Recap", section "1. Quantization and GEMM dispatch":
  * the path for M <= 48 on the pages' GPU):
  *   Y[m, n] = ts * sum_k X[m, k] * value(code[n, k]) * value(scale[n, k/16]),
- * bf16 activations, weights dequantised exactly to bf16, fp32 accumulation.
+ * bf16 activations, weights dequantised exactly (value(code) * value(scale)
+ * has at most 6 significant bits), fp32 accumulation.
  *   X      in:  device bf16 [M, K];  M >= 0 (M == 0 launches nothing)
  *   W      in:  quantised weight; K % 64 == 0
  *   Y      out: device [M, N] of out_dtype
@@ -201,7 +206,10 @@ nvfp4_status nvfp4_quantize_act(const void* X, int64_t M, int64_t K, float divis
  * For M <= nvfp4_get_w4a16_rf_max_m(): one CTA per tile and K slice, bf16
  * warp-level MMAs, the slices summed across a cluster.  Above that, weights
  * dequantised into tensor memory for tcgen05 MMAs.  All give the same result
- * up to fp32 summation order.  The workspace arguments are unused (NULL, 0).
+ * up to fp32 summation order, except that the split-K kernel's f16 copy of X
+ * rounds elements more than 2^29 below their token's largest magnitude in a
+ * K slice (an absolute error below 2^-25 of that magnitude).  The workspace
+ * arguments are unused (NULL, 0).
  */
 nvfp4_status nvfp4_gemm_w4a16(const void* X, int64_t M, const nvfp4_weight* W, void* Y,
                               int out_dtype, void* workspace, size_t workspace_bytes,
@@ -215,8 +223,12 @@ nvfp4_status nvfp4_gemm_w4a16(const void* X, int64_t M, const nvfp4_weight* W, v
  *   a_codes      in: device [M, K/2] (from nvfp4_quantize_act)
  *   a_scales_mma in: device, nvfp4_scales_mma_bytes(M, K) bytes
  *   a_tensor_scale in: device, 1 float
+ *   M            >= 0 (M == 0 launches nothing)
  *   W            in: quantised weight; K % 64 == 0
  *   Y            out: device [M, N] of out_dtype
+ * Above 128 tokens the kernel runs on CTA pairs (nvfp4_set_w4a4_cluster).
+ * NVFP4_ERR_UNSUPPORTED if no kernel configuration fits the size.  The
+ * workspace arguments are unused (NULL, 0).
  */
 nvfp4_status nvfp4_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma,
                              const float* a_tensor_scale, int64_t M, const nvfp4_weight* W,
