@@ -277,7 +277,9 @@ nvfp4_status nvfp4_linear_silu_mul(const void* X, int64_t M, const nvfp4_weight*
  * the product value(code) * value(scale) exact, one binary32 rounding for the
  * tensor scale, then round to nearest even bf16.
  *   codes [rows, K/2], scales_mma (MMA tiling), tensor_scale (1 float): device
+ *   rows >= 0 (0 launches nothing), K >= 16, K % 16 == 0
  *   out   device bf16 [rows, K]
+ * Pointers 16-byte aligned (the tensor scale 4-byte).  No workspace.
  */
 nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales_mma,
                               const float* tensor_scale, int64_t rows, int64_t K, void* out,
@@ -312,8 +314,8 @@ nvfp4_status nvfp4_qat_backward(const void* dY, int64_t M, const nvfp4_weight* W
  * nvfp4_linear without a caller-provided workspace, for callers that cannot
  * allocate device memory: code running while a CUDA graph is being captured
  * (where cudaMalloc is not allowed), plugins inside a host framework that owns
- * every allocation, embedded runtimes with no device allocator.  The paper has
- * no counterpart; this is a convenience of this library.
+ * every allocation, embedded runtimes with no device allocator.  The source pages
+ * have no counterpart; this is a convenience of this library.
  *
  * Same arguments and result as nvfp4_linear, minus the workspace.  The W4A4
  * branch keeps its scratch (the online-quantised activations) in a fixed
