@@ -12,7 +12,8 @@ Method sources (web pages about the SOAR 2026 inference contest):
     section "3. EAGLE-3 speculative decoding ..." (NVFP4 QAT, for the
     dequantisation and straight-through gradients);
   * "SOAR Weekly Champion Notes 07 ... NVFP4 Quantization Improvements",
-    sections "01 Background" and "02 FourOverSix".
+    sections "01 Background", "02 FourOverSix" and "03 How we integrated it"
+    (GPTQ inside the FourOverSix scales).
 """
 from __future__ import annotations
 

@@ -28,8 +28,9 @@
  *   - 16-element blocks along K, E4M3 block scales, one FP32 tensor scale
  *     ts = amax(|W|) / D with D = 6 * 448 by default; an all-zero tensor
  *     gets ts = 1.
- *   - Every step of the quantiser is IEEE binary32 with round-to-nearest-even
- *     and no fused multiply-add (build with -ffp-contract=off):
+ *   - Every step of the quantiser is IEEE binary32 with round-to-nearest-even;
+ *     the only fused multiply-adds are the explicit fmaf calls (build with
+ *     -ffp-contract=off so the compiler adds none):
  *       r6  = (amax_block / 6) / ts,      s6 = E4M3(r6)
  *       s4  = E4M3(value(s6) * 1.5)
  *       eff = value(s) * ts
@@ -52,7 +53,10 @@
  *
  * parity pinned: see the test suite (format tables against a third-party
  * library, worked examples computed by hand, brute-force scale search,
- * invariants).
+ * invariants; the GEMMs against a library matmul; the bf16 dequantisation
+ * by exact cases and hand-worked ties; GPTQ by the identity-Hessian case, its
+ * inverse factor against a library inverse and the least-squares
+ * continuation of every row).
  */
 #include <math.h>
 #include <stdint.h>
