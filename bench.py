@@ -341,13 +341,11 @@ def run_ours(args):
                    for M in DECODE_M},
     }
     if not args.no_prefill and rank == 0:
-        detail["w4a4_prefill"] = prefill_sweep(nv, dev, stream)
-        detail["model_quantizer"] = model_quantizer(nv, dev, stream)
-        detail["act_fos"] = act_fos_compare(nv, dev, stream)
-        detail["gate_up_silu_mul"] = gate_up_bench(nv, dev, stream)
-        detail["qat_step"] = qat_bench(nv, dev, stream)
-        detail["gptq_fos"] = gptq_bench(nv, dev, stream)
-        detail["mlp_decode"] = guarded(mlp_decode_bench, nv, dev, stream)
+        # each detail runs guarded: an exception is reported in the line
+        for key, fn in (("w4a4_prefill", prefill_sweep), ("model_quantizer", model_quantizer),
+                        ("act_fos", act_fos_compare), ("gate_up_silu_mul", gate_up_bench),
+                        ("qat_step", qat_bench), ("gptq_fos", gptq_bench), ("mlp_decode", mlp_decode_bench)):
+            detail[key] = guarded(fn, nv, dev, stream)
 
     e2e = measure_e2e(nv, dev, stream, w_bits, args, step_bytes, paths) if rank == 0 else None
 
