@@ -325,9 +325,10 @@ nvfp4_status nvfp4_qat_backward(const void* dY, int64_t M, const nvfp4_weight* W
  * branch needs M * (K/2 + K/16) bytes, so at K = 4096 up to about 14,500 rows
  * fit; the W4A16 branch needs none.  No allocator is called.
  *
- * The first call on each device looks up the array's device address (with
- * that device current) and caches it; make that first call before any stream
- * capture.  All calls share the one array and it keeps the previous call's
+ * The first call on each device that takes the W4A4 branch looks up the
+ * array's device address (with that device current) and caches it; make that
+ * first call before any stream capture.  Calls on the W4A16 branch, M == 0
+ * and argument errors never touch the array.  All calls share the one array and it keeps the previous call's
  * contents (nothing in it needs to start at zero): calls that may overlap on
  * the GPU -- on different streams, or from different threads -- race on it
  * and must be serialised by the caller.

@@ -51,16 +51,18 @@ extern "C" nvfp4_status nvfp4_linear_noalloc(const void* X, int64_t M, const nvf
   // invalid shapes are left to nvfp4_linear to report
   const bool shape_ok = W->N > 0 && W->K >= 256 && W->K % 64 == 0 && M > 0;
   const bool needs_scratch = shape_ok && M > nvfp4_get_crossover(W->N, W->K);
-  if (needs_scratch) {
-    const size_t need = nvfp4_workspace_bytes(NVFP4_OP_LINEAR, M, W->N, W->K);
-    if (need == 0 || need > NVFP4_NOALLOC_SCRATCH_BYTES) {
-      char msg[160];
-      snprintf(msg, sizeof msg,
-               "nvfp4_linear_noalloc: M=%lld, K=%lld needs %zu scratch bytes, more than the built-in %u",
-               (long long)M, (long long)W->K, need, (unsigned)NVFP4_NOALLOC_SCRATCH_BYTES);
-      nvfp4::set_last_error(msg);
-      return NVFP4_ERR_WORKSPACE;
-    }
+  // the W4A16 branch ignores the workspace, M == 0 launches nothing and bad
+  // arguments are reported before any device call: none of them needs the
+  // scratch, so none of them looks up its address
+  if (!needs_scratch) return nvfp4_linear(X, M, W, Y, out_dtype, nullptr, 0, stream);
+  const size_t need = nvfp4_workspace_bytes(NVFP4_OP_LINEAR, M, W->N, W->K);
+  if (need == 0 || need > NVFP4_NOALLOC_SCRATCH_BYTES) {
+    char msg[160];
+    snprintf(msg, sizeof msg,
+             "nvfp4_linear_noalloc: M=%lld, K=%lld needs %zu scratch bytes, more than the built-in %u",
+             (long long)M, (long long)W->K, need, (unsigned)NVFP4_NOALLOC_SCRATCH_BYTES);
+    nvfp4::set_last_error(msg);
+    return NVFP4_ERR_WORKSPACE;
   }
   void* scratch = nullptr;
   const nvfp4_status st = scratch_address(&scratch);

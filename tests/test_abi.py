@@ -224,3 +224,19 @@ def test_crossover_rule_from_timings():
     assert crossover_from({1: (2, 2), 4: (2, 2)}) == 4        # a tie keeps W4A16
     assert crossover_from({1: (3, 2), 2: (3, 2), 4: (1, 2)}) == 0
     assert crossover_from({64: (1, 2), 1: (3, 2), 8: (1, 2)}) == 64  # keys are sorted
+
+
+def test_noalloc_argument_paths(L):
+    """nvfp4_linear_noalloc reports argument errors, accepts M == 0 and
+    rejects scratch needs beyond its built-in array, all before any device
+    call (no GPU here)."""
+    na = L.nvfp4_linear_noalloc
+    assert na(FAKE, 4, None, FAKE, 0, None) == nv.ERR_INVALID_ARG
+    assert na(FAKE, 4, ctypes.byref(_w(K=48)), FAKE, 0, None) == nv.ERR_SHAPE
+    assert na(FAKE, -2, ctypes.byref(_w()), FAKE, 0, None) == nv.ERR_SHAPE
+    assert na(None, 0, ctypes.byref(_w()), None, 0, None) == nv.OK
+    big = _w(N=256, K=4096)
+    M = 16384
+    assert nv.nvfp4_workspace_bytes(nv.OP_LINEAR, M, 256, 4096) > nv.NOALLOC_SCRATCH_BYTES
+    assert na(FAKE, M, ctypes.byref(big), FAKE, 0, None) == nv.ERR_WORKSPACE
+    assert b"scratch" in L.nvfp4_last_error()
