@@ -581,12 +581,12 @@ def mlp_decode_bench(nv, dev, stream):
 
 
 def guarded(fn, *args):
-    """fn(*args), or {"error": ...} if it raises: a failing detail measurement
-    is reported in the JSON line instead of ending the run."""
+    """fn(*args), or {"exception": ...} if it raises: a failing detail
+    measurement is reported in the JSON line instead of ending the run."""
     try:
         return fn(*args)
     except Exception as e:  # noqa: BLE001
-        return {"error": f"{type(e).__name__}: {e}"}
+        return {"exception": f"{type(e).__name__}: {e}"}
 
 
 def qat_bench(nv, dev, stream, M=4096):
