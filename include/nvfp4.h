@@ -398,6 +398,14 @@ int nvfp4_get_w4a4_cluster(void);
  * current device: NVFP4_OK, NVFP4_ERR_NONFINITE or NVFP4_ERR_TIMEOUT. */
 nvfp4_status nvfp4_get_device_status(cudaStream_t stream);
 
+/* Self-test of the bounded device-side wait (the failure path of every
+ * pipeline wait in the GEMM kernels): launches one thread that waits on an
+ * mbarrier nothing completes.  The wait gives up after its cycle limit (about
+ * 1.5 s at 2 GHz) and records NVFP4_ERR_TIMEOUT in the device status word, which
+ * the next nvfp4_get_device_status() returns; the CUDA context stays usable.
+ * Returns NVFP4_OK once launched. */
+nvfp4_status nvfp4_selftest_wait_timeout(cudaStream_t stream);
+
 /* Static text for a status code. */
 const char* nvfp4_status_string(nvfp4_status status);
 

@@ -27,6 +27,7 @@ __all__ = [
     "nvfp4_get_crossover", "nvfp4_set_w4a16_rf_max_m", "nvfp4_get_w4a16_rf_max_m",
     "nvfp4_set_w4a16_sk_max_m", "nvfp4_get_w4a16_sk_max_m", "nvfp4_set_weight_prefetch",
     "nvfp4_get_weight_prefetch", "nvfp4_set_w4a4_cluster", "nvfp4_get_w4a4_cluster", "nvfp4_set_act_fos", "nvfp4_get_act_fos", "nvfp4_get_device_status",
+    "nvfp4_selftest_wait_timeout",
     "nvfp4_status_string",
 ]
 
@@ -94,6 +95,7 @@ def lib() -> ctypes.CDLL:
             "nvfp4_get_act_fos": (ctypes.c_int, []),
             "nvfp4_get_w4a4_cluster": (ctypes.c_int, []),
             "nvfp4_get_device_status": (st, [vp]),
+            "nvfp4_selftest_wait_timeout": (st, [vp]),
             "nvfp4_status_string": (ctypes.c_char_p, [st]),
             "nvfp4_last_error": (ctypes.c_char_p, []),
         }
@@ -201,6 +203,12 @@ def nvfp4_get_act_fos() -> bool:
 def nvfp4_get_device_status(stream=None) -> int:
     """Synchronises the stream and returns (and clears) the device status word."""
     return lib().nvfp4_get_device_status(_stream(stream))
+
+
+def nvfp4_selftest_wait_timeout(stream=None) -> None:
+    """Launch the bounded-wait self-test (nvfp4_selftest_wait_timeout); the
+    next nvfp4_get_device_status() returns ERR_TIMEOUT."""
+    _check(lib().nvfp4_selftest_wait_timeout(_stream(stream)), "nvfp4_selftest_wait_timeout")
 
 
 @dataclasses.dataclass

@@ -488,6 +488,15 @@ int64_t nvfp4_get_crossover(int64_t N, int64_t K) {
   return it == g_crossover.end() ? g_default_crossover : it->second;
 }
 
+nvfp4_status nvfp4_selftest_wait_timeout(cudaStream_t stream) {
+  const DeviceInfo* d = nullptr;
+  const nvfp4_status st = device_info(&d);
+  if (st != NVFP4_OK) return st;
+  const cudaError_t err = nvfp4::launch_wait_timeout_selftest(d->status, stream);
+  if (err != cudaSuccess) return fail_cuda(err, "wait-timeout self-test launch");
+  return NVFP4_OK;
+}
+
 nvfp4_status nvfp4_get_device_status(cudaStream_t stream) {
   cudaError_t err = cudaStreamSynchronize(stream);
   if (err != cudaSuccess) return fail_cuda(err, "cudaStreamSynchronize");

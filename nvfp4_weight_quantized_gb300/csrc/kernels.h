@@ -82,4 +82,8 @@ cudaError_t launch_gptq(const void* W, int64_t N, int64_t K, const float* H, flo
 bool w4a4_set_cluster_ctas(int ctas);
 int w4a4_get_cluster_ctas();
 
+// One thread waits on an mbarrier nothing completes; when the bounded wait
+// gives up it sets the timeout bit of `status` (selftest.cu).
+cudaError_t launch_wait_timeout_selftest(unsigned int* status, cudaStream_t stream);
+
 }  // namespace nvfp4

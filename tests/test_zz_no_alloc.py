@@ -4,7 +4,8 @@ runtimes without a device allocator).  It keeps its scratch in an array built
 into the library; its output must match nvfp4_linear (same tolerance as the
 other GEMM tests) on consecutive calls that share that array.
 
-This file is collected last on purpose: if it fails, every other test has run."""
+This file is collected after the parity tests on purpose: if it fails, they
+have all run."""
 import ctypes
 
 import numpy as np
