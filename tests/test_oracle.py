@@ -620,3 +620,30 @@ def test_gptq_codes_round_the_least_squares_continuation(damp, block):
             checked += 1
     assert checked >= 0.95 * N * K
     assert not np.array_equal(g["codes"], oracle.quantize_fos(w)["codes"])  # errors were spread
+
+
+def test_threaded_oracle_splits_match_single_calls():
+    """The parity tests split oracle work over threads by row; every split
+    (more threads than rows included) must give exactly the single-call
+    result, on a ragged row count."""
+    from nvfp4_testutil import oracle_w4a16, oracle_w4a4
+    w = synth.weight_normal(37, 128, seed=31, outlier_frac=0.02)
+    ref = oracle.quantize_fos(w)
+    x = synth.act_student_t(13, 128, seed=32)
+    a = oracle.quantize_act(x)
+    y16 = oracle.gemm_w4a16(x, ref["codes"], ref["scales"], ref["ts"])
+    y4 = oracle.gemm_w4a4(a["codes"], a["scales"], a["ts"], ref["codes"], ref["scales"], ref["ts"])
+    cols = np.array([36, 0, 5, 17])
+    for threads in (1, 3, 7, 64):
+        q = oracle.quantize_rows(w, ref["ts"], True, threads)
+        for k in ("codes", "scales", "choice"):
+            assert np.array_equal(q[k], ref[k]), (k, threads)
+        assert q["m4_count"] == ref["m4_count"]
+        assert np.array_equal(oracle_w4a16(x, ref["codes"], ref["scales"], ref["ts"], threads=threads), y16)
+        assert np.array_equal(oracle_w4a16(x, ref["codes"], ref["scales"], ref["ts"], n_rows=cols,
+                                           threads=threads), y16[:, cols])
+        assert np.array_equal(oracle_w4a4(a["codes"], a["scales"], a["ts"], ref["codes"], ref["scales"],
+                                          ref["ts"], threads=threads), y4)
+        assert np.array_equal(oracle_w4a4(a["codes"], a["scales"], a["ts"], ref["codes"], ref["scales"],
+                                          ref["ts"], m_rows=np.array([12, 3]), n_rows=cols, threads=threads),
+                              y4[np.ix_([12, 3], cols)])
