@@ -647,3 +647,37 @@ def test_threaded_oracle_splits_match_single_calls():
         assert np.array_equal(oracle_w4a4(a["codes"], a["scales"], a["ts"], ref["codes"], ref["scales"],
                                           ref["ts"], m_rows=np.array([12, 3]), n_rows=cols, threads=threads),
                               y4[np.ix_([12, 3], cols)])
+
+
+def test_gemm_tolerance_checker():
+    """The comparator every GEMM parity test uses: per output row,
+    |y - ref| <= GEMM_REL_TOL * max|ref_row| (+ half a bf16 ulp of ref for
+    bf16 outputs), each row on its own scale; non-finite outputs fail."""
+    from nvfp4_testutil import GEMM_REL_TOL, assert_gemm_close, bf16_half_ulp
+    hu = bf16_half_ulp(np.array([1.0, 1.5, 2.0, -3.0, 0.0, 2.0 ** -130, 2.0 ** -126, 3e38]))
+    assert list(hu[:6]) == [2.0 ** -8, 2.0 ** -8, 2.0 ** -7, 2.0 ** -7, 2.0 ** -134, 2.0 ** -134]
+    assert hu[6] == 2.0 ** -134 and hu[7] == 2.0 ** 119
+    ref = np.array([[1.0, -0.5, 0.25], [1e-6, -2e-6, 3e-6]])
+    tol = GEMM_REL_TOL * np.max(np.abs(ref), axis=1, keepdims=True)
+    assert_gemm_close(ref + 0.99 * tol, ref, bf16=False)
+    with pytest.raises(AssertionError):
+        assert_gemm_close(ref + 1.01 * tol * np.array([[0, 0, 0], [0, 1, 0]]), ref, bf16=False)  # small row
+    with pytest.raises(AssertionError):
+        assert_gemm_close(ref + 1.01 * tol * np.array([[1, 0, 0], [0, 0, 0]]), ref, bf16=False)
+    half = bf16_half_ulp(ref)
+    assert_gemm_close(ref + 0.99 * tol + 0.9 * half, ref, bf16=True)
+    with pytest.raises(AssertionError):
+        assert_gemm_close(ref + 0.99 * tol + 1.2 * half, ref, bf16=False)
+    with pytest.raises(AssertionError):
+        assert_gemm_close(ref + tol + 1.1 * half, ref, bf16=True)
+    bad = ref.copy()
+    bad[0, 1] = np.nan
+    with pytest.raises(AssertionError):
+        assert_gemm_close(bad, ref, bf16=False)
+    with pytest.raises(AssertionError):
+        assert_gemm_close(ref[:, :2], ref, bf16=False)
+    # bf16 rounding of an exact result always passes
+    rng = np.random.default_rng(33)
+    exact = rng.standard_normal((6, 50)) * np.exp(rng.uniform(-20, 20, (6, 1)))
+    rounded = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(exact.astype(np.float32))).astype(np.float64)
+    assert_gemm_close(rounded, exact, bf16=True)
