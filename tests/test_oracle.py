@@ -681,3 +681,21 @@ def test_gemm_tolerance_checker():
     exact = rng.standard_normal((6, 50)) * np.exp(rng.uniform(-20, 20, (6, 1)))
     rounded = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(exact.astype(np.float32))).astype(np.float64)
     assert_gemm_close(rounded, exact, bf16=True)
+
+
+def test_silu_mul_tolerance_checker():
+    """The gated projection's comparator: |y - silu(g) u| within
+    SILU_MUL_REL_TOL * max|g_row| * max|u_row| (+ half a bf16 ulp)."""
+    from nvfp4_testutil import SILU_MUL_REL_TOL, assert_silu_mul_close, silu_mul_ref
+    rng = np.random.default_rng(34)
+    g = rng.standard_normal((3, 40)) * 3
+    u = rng.standard_normal((3, 40))
+    y = silu_mul_ref(g, u)
+    tol = SILU_MUL_REL_TOL * np.max(np.abs(g), axis=1, keepdims=True) * np.max(np.abs(u), axis=1, keepdims=True)
+    assert_silu_mul_close(y + 0.99 * tol, g, u, bf16=False)
+    bump = np.zeros_like(y)
+    bump[2, 7] = 1.01
+    with pytest.raises(AssertionError):
+        assert_silu_mul_close(y + bump * tol, g, u, bf16=False)
+    with pytest.raises(AssertionError):
+        assert_silu_mul_close(silu_mul_ref(u, g), g, u, bf16=False)  # gate and up swapped
