@@ -240,3 +240,10 @@ def test_noalloc_argument_paths(L):
     assert nv.nvfp4_workspace_bytes(nv.OP_LINEAR, M, 256, 4096) > nv.NOALLOC_SCRATCH_BYTES
     assert na(FAKE, M, ctypes.byref(big), FAKE, 0, None) == nv.ERR_WORKSPACE
     assert b"scratch" in L.nvfp4_last_error()
+
+
+def test_binding_declares_every_signature(L):
+    """Every function of the header has its argument and result types set in
+    the binding (an unset signature would pass 64-bit sizes as C ints)."""
+    for n in nv.declared_functions():
+        assert getattr(L, n).argtypes is not None, f"{n}: no ctypes signature in the binding"
