@@ -27,7 +27,7 @@ def _built():
 
 def test_bounded_wait_gives_up_and_reports_timeout():
     torch.cuda.synchronize()
-    assert nv.nvfp4_get_device_status() == nv.OK
+    nv.nvfp4_get_device_status()  # clears whatever an earlier test left in the word
     t0 = time.perf_counter()
     nv.nvfp4_selftest_wait_timeout()
     assert nv.nvfp4_get_device_status() == nv.ERR_TIMEOUT  # synchronises the stream
