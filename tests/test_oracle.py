@@ -584,7 +584,7 @@ def test_silu_mul_reference_closed_forms():
     assert silu_mul_ref(np.array([2.5]), np.array([-3.0]))[0] == pytest.approx(-3.0 * y[7], rel=1e-15)
 
 
-@pytest.mark.parametrize("damp,block", [(0.01, 16), (0.5, 128)])
+@pytest.mark.parametrize("damp,block", [(0.01, 16), (0.5, 128), (0.1, 48)])  # 48: a ragged last block
 def test_gptq_codes_round_the_least_squares_continuation(damp, block):
     """GPTQ's defining property, checked without its Cholesky steps: when
     column i is quantised, the working row is the minimiser of the layer error
