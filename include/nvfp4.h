@@ -312,10 +312,10 @@ nvfp4_status nvfp4_qat_backward(const void* dY, int64_t M, const nvfp4_weight* W
 
 /*
  * nvfp4_linear without a caller-provided workspace, for callers that cannot
- * allocate device memory: code running while a CUDA graph is being captured
- * (where cudaMalloc is not allowed), plugins inside a host framework that owns
- * every allocation, embedded runtimes with no device allocator.  The source pages
- * have no counterpart; this is a convenience of this library.
+ * allocate device memory: plugins inside a host framework that owns every
+ * allocation and hands them only its own tensors, embedded runtimes with no
+ * device allocator.  The source pages have no counterpart; this is a
+ * convenience of this library.
  *
  * Same arguments and result as nvfp4_linear, minus the workspace.  The W4A4
  * branch keeps its scratch (the online-quantised activations) in a fixed
@@ -325,13 +325,16 @@ nvfp4_status nvfp4_qat_backward(const void* dY, int64_t M, const nvfp4_weight* W
  * branch needs M * (K/2 + K/16) bytes, so at K = 4096 up to about 14,500 rows
  * fit; the W4A16 branch needs none.  No allocator is called.
  *
- * The first call on each device that takes the W4A4 branch looks up the
- * array's device address (with that device current) and caches it; make that
- * first call before any stream capture.  Calls on the W4A16 branch, M == 0
- * and argument errors never touch the array.  All calls share the one array and it keeps the previous call's
- * contents (nothing in it needs to start at zero): calls that may overlap on
- * the GPU -- on different streams, or from different threads -- race on it
- * and must be serialised by the caller.
+ * The branch is chosen once per call (M against the crossover table) and the
+ * scratch size is checked for that branch.  The first call on each device
+ * that takes the W4A4 branch looks up the array's device address (with that
+ * device current) and caches it for the current CUDA context (a context
+ * re-created after cudaDeviceReset is looked up again); make that first call
+ * before any stream capture.  Calls on the W4A16 branch, M == 0 and argument
+ * errors never touch the array.  All calls share the one array and it keeps
+ * the previous call's contents (nothing in it needs to start at zero): calls
+ * that may overlap on the GPU -- on different streams, or from different
+ * threads -- race on it and must be serialised by the caller.
  */
 nvfp4_status nvfp4_linear_noalloc(const void* X, int64_t M, const nvfp4_weight* W, void* Y,
                                   int out_dtype, cudaStream_t stream);
@@ -382,13 +385,9 @@ int nvfp4_get_act_fos(void);
 /* W4A4 kernel for M > 128: CTAs per thread-block cluster (default 2).
  *   2: a pair of CTAs shares each 256 x 256 output tile through cta_group::2
  *      MMAs (each CTA stages half of the A rows and half of the B rows of
- *      every K stage);
- *   4: two such pairs compute adjacent tiles of the same 256 rows and share
- *      those A rows by TMA multicast (each CTA fetches a quarter of them);
+ *      every K stage, each with its own loads);
  *   1: one CTA per 128 x 256 tile.
- * On GB300, 4 measured no faster than 2 (fewer SMs hold clusters of four).
- * Where a cluster of the requested size cannot be resident the next smaller
- * one is used.  All compute the same product with the same fp32 accumulation
+ * Where a pair cannot be resident single CTAs are used.  All compute the same product with the same fp32 accumulation
  * order per output.  A tuning knob; thread-safe; NVFP4_ERR_INVALID_ARG for
  * any other value. */
 nvfp4_status nvfp4_set_w4a4_cluster(int ctas);

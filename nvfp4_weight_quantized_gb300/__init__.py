@@ -183,7 +183,7 @@ def nvfp4_get_weight_prefetch() -> bool:
 
 
 def nvfp4_set_w4a4_cluster(ctas: int) -> None:
-    """CTAs per cluster of the W4A4 kernel above 128 tokens: 4, 2 or 1."""
+    """CTAs per cluster of the W4A4 kernel above 128 tokens: 2 or 1."""
     _check(lib().nvfp4_set_w4a4_cluster(ctas), "nvfp4_set_w4a4_cluster")
 
 

@@ -1,5 +1,7 @@
 // api.cu -- the C ABI (include/nvfp4.h): argument checks, workspace layout,
 // dispatch between the W4A16 and W4A4 paths, device status word.
+#include <cuda.h>
+
 #include <cmath>
 #include <atomic>
 #include <cstdio>
@@ -43,7 +45,7 @@ std::atomic<bool> g_act_fos{false};
 
 struct DeviceInfo {
   bool ready = false;
-  nvfp4_status st = NVFP4_ERR_CUDA;
+  unsigned long long ctx_id = 0;  // the context the addresses below belong to
   int num_sms = 0;
   unsigned int* status = nullptr;
 };
@@ -60,16 +62,21 @@ nvfp4_status fail_cuda(cudaError_t err, const char* where) {
   return NVFP4_ERR_CUDA;
 }
 
-// Per-device set-up, done once with that device current: SM count, a check
+// Per-device set-up, done with that device current, once per CUDA context
+// on it (a context re-created after cudaDeviceReset loads the library's
+// device image again, at possibly different addresses): SM count, a check
 // that this is an sm_103 GPU, and the device address of the status word.
 nvfp4_status device_info(const DeviceInfo** out) {
   int dev = -1;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return fail_cuda(err, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(NVFP4_ERR_UNSUPPORTED, "device index out of range");
+  unsigned long long ctx = 0;
+  if (!nvfp4::current_context_id(&ctx)) return fail(NVFP4_ERR_CUDA, "cannot identify the current CUDA context");
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceInfo& d = g_dev[dev];
-  if (!d.ready) {
+  if (!d.ready || d.ctx_id != ctx) {
+    d.ready = false;
     int major = 0, minor = 0;
     err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     if (err == cudaSuccess) err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
@@ -81,6 +88,7 @@ nvfp4_status device_info(const DeviceInfo** out) {
     err = cudaGetSymbolAddress(&p, g_device_status);
     if (err != cudaSuccess) return fail_cuda(err, "cudaGetSymbolAddress(status)");
     d.status = static_cast<unsigned int*>(p);
+    d.ctx_id = ctx;
     d.ready = true;
   }
   *out = &d;
@@ -158,6 +166,35 @@ LinearWs linear_ws_layout(int64_t M, int64_t K) {
 
 namespace nvfp4 {
 void set_last_error(const char* what) { t_last_error = what; }
+
+bool current_context_id(unsigned long long* id) {
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  if (get_current == nullptr || get_id == nullptr) return false;
+  CUcontext c = nullptr;
+  if (get_current(&c) != CUDA_SUCCESS) return false;
+  if (c == nullptr) {
+    // the runtime has not made its primary context current on this thread
+    // yet (a call that binds it; never reached while a stream is captured,
+    // since capturing needs the context already)
+    if (cudaFree(nullptr) != cudaSuccess || get_current(&c) != CUDA_SUCCESS || c == nullptr) return false;
+  }
+  return get_id(c, id) == CUDA_SUCCESS;
+}
 }  // namespace nvfp4
 
 extern "C" {
@@ -279,9 +316,24 @@ nvfp4_status nvfp4_linear(const void* X, int64_t M, const nvfp4_weight* W, void*
                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   nvfp4_status st = check_weight(W);
   if (st != NVFP4_OK) return st;
+  return nvfp4::linear_branch(X, M, W, Y, out_dtype, workspace, workspace_bytes, stream,
+                              nvfp4::linear_takes_w4a4(M, W->N, W->K));
+}
+
+}  // extern "C"
+
+namespace nvfp4 {
+
+bool linear_takes_w4a4(int64_t M, int64_t N, int64_t K) {
   // the tensor-core path needs at least one full 256-wide K stage
-  if (M <= nvfp4_get_crossover(W->N, W->K) || W->K < 256)
-    return nvfp4_gemm_w4a16(X, M, W, Y, out_dtype, workspace, workspace_bytes, stream);
+  return !(M <= nvfp4_get_crossover(N, K) || K < 256);
+}
+
+nvfp4_status linear_branch(const void* X, int64_t M, const nvfp4_weight* W, void* Y, int out_dtype,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream, bool w4a4) {
+  nvfp4_status st = check_weight(W);
+  if (st != NVFP4_OK) return st;
+  if (!w4a4 || W->K < 256) return nvfp4_gemm_w4a16(X, M, W, Y, out_dtype, workspace, workspace_bytes, stream);
   if ((st = check_out_dtype(out_dtype)) != NVFP4_OK) return st;
   if (M > kMaxElems / W->K) return fail(NVFP4_ERR_SHAPE, "bad M");
   const LinearWs l = linear_ws_layout(M, W->K);
@@ -297,6 +349,10 @@ nvfp4_status nvfp4_linear(const void* X, int64_t M, const nvfp4_weight* W, void*
   if (st != NVFP4_OK) return st;
   return nvfp4_gemm_w4a4(a_codes, a_smma, a_ts, M, W, Y, out_dtype, nullptr, 0, stream);
 }
+
+}  // namespace nvfp4
+
+extern "C" {
 
 nvfp4_status nvfp4_linear_silu_mul(const void* X, int64_t M, const nvfp4_weight* W, void* Y, int out_dtype,
                                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
@@ -462,7 +518,7 @@ nvfp4_status nvfp4_set_w4a16_sk_max_m(int64_t M) {
 int64_t nvfp4_get_w4a16_sk_max_m(void) { return g_w4a16_sk_max_m.load(std::memory_order_relaxed); }
 
 nvfp4_status nvfp4_set_w4a4_cluster(int ctas) {
-  if (!nvfp4::w4a4_set_cluster_ctas(ctas)) return fail(NVFP4_ERR_INVALID_ARG, "w4a4 cluster size must be 1, 2 or 4");
+  if (!nvfp4::w4a4_set_cluster_ctas(ctas)) return fail(NVFP4_ERR_INVALID_ARG, "w4a4 cluster size must be 1 or 2");
   return NVFP4_OK;
 }
 

@@ -424,12 +424,8 @@ w4a4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 //     commit that arrives on empty[s] of both CTAs; acc_full likewise;
 //   epilogue (warps 0-3, each CTA): drains its accumulator lanes, then
 //     arrives on the even CTA's acc_free (8 arrivals).
-// With kPairs = 2 a cluster holds two pairs that compute horizontally
-// adjacent tiles (same A rows, weight tiles 2j and 2j + 1): CTA r of pair p
-// loads 64 of its 128 A rows per stage and multicasts them to CTA r of both
-// pairs, so each CTA fetches 8 KB of A per stage instead of 16 KB.  A stage
-// buffer is then written by both pairs, so each pair's leader commits the
-// stage's completion to all four CTAs (empty[s] counts kPairs arrivals).
+// Every CTA loads its own operand tiles (no TMA multicast); rows both CTAs of
+// different pairs need are shared through L2.
 constexpr int kPairStages = 5;
 // The pair kernel's loads are issued by three producer warps (A rows and
 // their scales; B rows; B scales): one thread waits ~130-170 cycles per
@@ -463,7 +459,7 @@ constexpr uint32_t kPairIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(256 >> 3) <
 // F features: a tile covers 128 features, CTA 0 of the pair staging their
 // gate rows and CTA 1 their up rows, so accumulator column j (< 128) of every
 // row holds G[m, f0 + j] and column 128 + j holds U[m, f0 + j].
-template <int kPairs, bool kF32, bool kGateUp = false>
+template <bool kF32, bool kGateUp = false>
 __global__ void __launch_bounds__(kPairThreads, 1)
 w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                  const __grid_constant__ CUtensorMap tmap_y, int tma_store, const uint8_t* __restrict__ a_smma,
@@ -474,25 +470,23 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
   extern __shared__ uint8_t smem_raw[];
   PairSmem& sm = *reinterpret_cast<PairSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kCtas = 2 * kPairs;
-  const uint32_t crank = cluster_rank();
-  const uint32_t rank = crank & 1u, pidx = crank >> 1, lead = crank & ~1u;  // CTA in pair, pair, its even CTA
-  const uint16_t pair_mask = (uint16_t)(3u << lead), all_mask = (uint16_t)((1u << kCtas) - 1u);
-  const int64_t cl = blockIdx.x / kCtas, ncl = gridDim.x / kCtas;
+  const uint32_t rank = cluster_rank();  // CTA in the pair; CTA 0 issues the MMAs
+  constexpr uint32_t lead = 0;
+  constexpr uint16_t pair_mask = 3u;
+  const int64_t cl = blockIdx.x / 2, ncl = gridDim.x / 2;
   const int kb64 = (int)(K / 64);
   const int kt = (kb64 + 3) / 4;
-  static_assert(!kGateUp || (kPairs == 1 && !kF32), "gate/up epilogue: one pair per cluster, bf16 output");
+  static_assert(!kGateUp || !kF32, "gate/up epilogue: bf16 output");
   const int64_t b_row_tiles = (N + 127) / 128;
   const int64_t F = N / 2;  // features of a gate/up weight
   const int64_t n_tiles = kGateUp ? F / 128 : (N + 255) / 256;
-  const int64_t n_groups = (n_tiles + kPairs - 1) / kPairs;  // a cluster's unit: kPairs adjacent tiles
-  const int64_t n_work = ((M + 255) / 256) * n_groups;
+  const int64_t n_work = ((M + 255) / 256) * n_tiles;
 
   if (warp == kProducerWarp && lane == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&sm.full[s], kPairProducers);
       mbar_init(&sm.sf_full[s], 2 * kSfWarps);
-      mbar_init(&sm.empty[s], kPairs);
+      mbar_init(&sm.empty[s], 1);
     }
     mbar_init(&sm.acc_full, 1);
     mbar_init(&sm.acc_free, 2 * kEpiWarps);
@@ -514,17 +508,14 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
       griddep_wait();
       int g = 0;
       for (int64_t w = cl; w < n_work && !failed; w += ncl) {
-        const int64_t m_tile = w / n_groups, n_tile = (w - m_tile * n_groups) * kPairs + pidx;
+        const int64_t m_tile = w / n_tiles, n_tile = w - m_tile * n_tiles;
         const int64_t arow = m_tile * 256 + 128 * rank;
-        const int64_t n0 = n_tile * (kGateUp ? 128 : 256);  // past N for the idle pair of a ragged last unit
+        const int64_t n0 = n_tile * (kGateUp ? 128 : 256);
         const int64_t brow = kGateUp ? n0 + F * rank : n0 + 128 * rank;
         // a CTA whose A (or B) rows all lie past M (N) loads nothing for them:
         // its accumulator rows (or the tile's columns from that half) are never stored
         const bool has_a = arow < M, has_b = brow < N;
-        // with kPairs = 2 the two 64-row halves of the A rows come from the two
-        // pairs; a half that lies wholly past M is not loaded by either side
-        const uint32_t a_bytes = kPairs == 1 ? (has_a ? kABytes : 0)
-                                             : (has_a ? kABytes / 2 : 0) + (arow + 64 < M ? kABytes / 2 : 0);
+        const uint32_t a_bytes = has_a ? kABytes : 0;
         const int64_t sfb_left = b_row_tiles - n0 / 128;
         const int nsfb = kGateUp ? 2 : sfb_left <= 0 ? 0 : sfb_left < 2 ? (int)sfb_left : 2;
         for (int ks = 0; ks < kt; ++ks, ++g) {
@@ -537,14 +528,7 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
           const uint32_t sf_bytes = (uint32_t)kk_n * kScaleTileBytes;
           if (warp == kProducerWarp) {
             mbar_arrive_expect_tx(&sm.full[s], a_bytes + (has_a ? sf_bytes : 0));
-            if (kPairs == 1) {
-              if (has_a) tma_load_2d(sm.a[s], &tmap_a, ks * (BK / 2), (int)arow, &sm.full[s]);
-            } else if (arow + 64 * pidx < M) {
-              // rows [64 pidx, +64) of this CTA's 128, to this CTA and its
-              // counterpart in the other pair
-              tma_load_2d_mc(sm.a[s] + pidx * (kABytes / 2), &tmap_a, ks * (BK / 2), (int)(arow + 64 * pidx),
-                             &sm.full[s], (uint16_t)((1u << rank) | (1u << (rank + 2))));
-            }
+            if (has_a) tma_load_2d(sm.a[s], &tmap_a, ks * (BK / 2), (int)arow, &sm.full[s]);
             if (has_a)
               bulk_load(sm.sfa[s], a_smma + ((arow / 128) * kb64 + 4 * ks) * kScaleTileBytes, sf_bytes,
                         &sm.full[s]);
@@ -597,7 +581,7 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
           for (int kk = 0; kk < kk_n; ++kk)
             mma_mxf4nvf4_pair(tmem, adesc + 2ull * kk, bdesc + 2ull * kk, kPairIdesc, sfa_t + 4 * kk,
                               sfb_t + 8 * kk, (ks | kk) != 0);
-          commit_pair(&sm.empty[s], all_mask);
+          commit_pair(&sm.empty[s], pair_mask);
         }
         if (!failed) commit_pair(&sm.acc_full, pair_mask);
       }
@@ -658,7 +642,7 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
     const int r = warp * 32 + lane;
     int t = 0;
     for (int64_t w = cl; w < n_work; w += ncl, ++t) {
-      const int64_t m_tile = w / n_groups, n_tile = (w - m_tile * n_groups) * kPairs + pidx;
+      const int64_t m_tile = w / n_tiles, n_tile = w - m_tile * n_tiles;
       const int64_t m0 = m_tile * 256 + 128 * rank, n0 = n_tile * (kGateUp ? 128 : 256);
       const int64_t row = m0 + r;
       const bool ok = __all_sync(0xffffffffu, !failed && mbar_wait(&sm.acc_full, (uint32_t)t & 1u));
@@ -887,16 +871,15 @@ cudaError_t launch_bn(const uint8_t* a_codes, const uint8_t* a_smma, const float
 
 std::atomic<int> g_cluster_ctas{2};
 
-// Pair-kernel launch: clusters of 2 * kPairs CTAs, one CTA per SM (the
-// shared-memory request is above half an SM's), as many clusters as fit at
-// once or as there are work units.  cudaErrorNotSupported when no cluster of
-// that shape can be resident.
-template <int kPairs, bool kGateUp = false>
+// Pair-kernel launch: clusters of 2 CTAs, one CTA per SM (the shared-memory
+// request is above half an SM's), as many clusters as fit at once or as there
+// are work units.  cudaErrorNotSupported when no pair can be resident.
+template <bool kGateUp = false>
 cudaError_t launch_pairs(const uint8_t* a_codes, const uint8_t* a_smma, const float* a_ts, int64_t M,
                          const uint8_t* w_codes, const uint8_t* w_smma, const float* w_ts, int64_t N, int64_t K,
                          void* y, bool out_f32, unsigned int* status, cudaStream_t stream) {
   CUtensorMap ma, mb, my;
-  if (!make_map(&ma, a_codes, (uint64_t)M, (uint64_t)K / 2, 128 / kPairs) ||
+  if (!make_map(&ma, a_codes, (uint64_t)M, (uint64_t)K / 2, 128) ||
       !make_map(&mb, w_codes, (uint64_t)N, (uint64_t)K / 2, 128))
     return cudaErrorInvalidValue;
   const int64_t n_out = kGateUp ? N / 2 : N;  // columns of Y
@@ -905,11 +888,11 @@ cudaError_t launch_pairs(const uint8_t* a_codes, const uint8_t* a_smma, const fl
   if (tma_store && !make_y_map(&my, y, (uint64_t)M, (uint64_t)n_out)) tma_store = 0;
   if (kGateUp && !tma_store) return cudaErrorNotSupported;
   const size_t smem = sizeof(PairSmem) + 1024;
-  auto kern = out_f32 ? w4a4_pair_kernel<kPairs, true> : w4a4_pair_kernel<kPairs, false>;
-  if constexpr (kGateUp) kern = w4a4_pair_kernel<kPairs, false, true>;
+  auto kern = out_f32 ? w4a4_pair_kernel<true> : w4a4_pair_kernel<false>;
+  if constexpr (kGateUp) kern = w4a4_pair_kernel<false, true>;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2 * kPairs;
+  attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -928,7 +911,7 @@ cudaError_t launch_pairs(const uint8_t* a_codes, const uint8_t* a_smma, const fl
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return;
     cudaLaunchConfig_t q = cfg;
-    q.gridDim = dim3(2 * kPairs);
+    q.gridDim = dim3(2);
     q.numAttrs = 1;  // the cluster shape only
     int n = 0;
     err = cudaOccupancyMaxActiveClusters(&n, kern, &q);
@@ -938,8 +921,8 @@ cudaError_t launch_pairs(const uint8_t* a_codes, const uint8_t* a_smma, const fl
   const int mc = max_clusters[out_f32 ? 1 : 0];
   if (mc < 1) return cudaErrorNotSupported;
   const int64_t tiles_n = kGateUp ? N / 2 / 128 : (N + 255) / 256;
-  const int64_t work = ((M + 255) / 256) * ((tiles_n + kPairs - 1) / kPairs);
-  cfg.gridDim = dim3((unsigned)(2 * kPairs * std::min<int64_t>(work, mc)));
+  const int64_t work = ((M + 255) / 256) * tiles_n;
+  cfg.gridDim = dim3((unsigned)(2 * std::min<int64_t>(work, mc)));
   return cudaLaunchKernelEx(&cfg, kern, ma, mb, my, tma_store, a_smma, w_smma, a_ts, w_ts, M, N, K, y, status);
 }
 
@@ -951,12 +934,12 @@ cudaError_t launch_gemm_w4a4_gate_up(const uint8_t* a_codes, const uint8_t* a_sc
                                      cudaStream_t stream) {
   if (M <= 0) return cudaSuccess;
   if (N % 256 != 0 || K < BK || K % 64 != 0 || M > INT32_MAX || N > INT32_MAX) return cudaErrorNotSupported;
-  return launch_pairs<1, true>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, false, status,
+  return launch_pairs<true>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, false, status,
                                stream);
 }
 
 bool w4a4_set_cluster_ctas(int ctas) {
-  if (ctas != 1 && ctas != 2 && ctas != 4) return false;
+  if (ctas != 1 && ctas != 2) return false;
   g_cluster_ctas.store(ctas, std::memory_order_relaxed);
   return true;
 }
@@ -973,11 +956,8 @@ cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma
                          num_sms, stream);
   const int ctas = w4a4_get_cluster_ctas();
   cudaError_t err = cudaErrorNotSupported;
-  if (ctas == 4)
-    err = launch_pairs<2>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, out_f32, status,
-                          stream);
-  if (ctas >= 2 && err == cudaErrorNotSupported)
-    err = launch_pairs<1>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, out_f32, status,
+  if (ctas == 2)
+    err = launch_pairs<false>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, out_f32, status,
                           stream);
   if (err != cudaErrorNotSupported) return err;
   return launch_bn<256>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, out_f32, status,

@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "nvfp4.h"
+
 namespace nvfp4 {
 
 // Maximum number of per-CTA amax partials (sizes the quantiser workspace).
@@ -15,6 +17,18 @@ size_t quant_workspace_bytes();
 
 // Records the text nvfp4_last_error() returns on this thread.
 void set_last_error(const char* what);
+
+// Unique id of the CUDA context current on this thread (the runtime's primary
+// context of the current device, made current if needed); false on failure.
+// Host-side caches of device addresses are keyed by it.
+bool current_context_id(unsigned long long* id);
+
+// nvfp4_linear's branch choice for an M-token call on an [N, K] weight.
+bool linear_takes_w4a4(int64_t M, int64_t N, int64_t K);
+// nvfp4_linear with the branch already chosen (w4a4 false: W4A16), so a
+// caller that sized its scratch for one branch runs exactly that branch.
+nvfp4_status linear_branch(const void* X, int64_t M, const nvfp4_weight* W, void* Y, int out_dtype,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream, bool w4a4);
 
 // Tensor amax + quantisation (FourOverSix when `fos`, else M=6 only).
 cudaError_t launch_quantize(const void* x, int64_t rows, int64_t K, float divisor, bool fos,
@@ -76,9 +90,9 @@ cudaError_t launch_gptq(const void* W, int64_t N, int64_t K, const float* H, flo
                         const float* ts, uint8_t* codes, void* workspace, unsigned int* status,
                         cudaStream_t stream);
 
-// CTAs per cluster for M > 128: 4 (two CTA pairs sharing A rows by TMA
-// multicast), 2 (one pair, cta_group::2 MMAs on 256 x 256 tiles) or 1 (single
-// CTAs on 128 x 256 tiles).  The setter rejects anything else.
+// CTAs per cluster for M > 128: 2 (one pair, cta_group::2 MMAs on 256 x 256
+// tiles) or 1 (single CTAs on 128 x 256 tiles).  The setter rejects anything
+// else.
 bool w4a4_set_cluster_ctas(int ctas);
 int w4a4_get_cluster_ctas();
 

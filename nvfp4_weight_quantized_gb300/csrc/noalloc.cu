@@ -3,13 +3,13 @@
 //
 // nvfp4_linear needs scratch for its W4A4 branch (the activations quantised
 // online: codes, MMA-tiled scales, tensor scale and the amax partials).  Some
-// callers have no way to provide it: code running while a CUDA graph is being
-// captured (where cudaMalloc is not allowed), plugins living inside a host
-// framework that owns every allocation, or embedded runtimes without a device
-// allocator.  This entry point keeps that scratch in a fixed array that is
-// part of the library's device image instead, so it calls no allocator at
-// all.  The array (NVFP4_NOALLOC_SCRATCH_BYTES) exists on every GPU that
-// loads the library until the process exits.
+// callers have no way to provide it: plugins living inside a host framework
+// that owns every allocation and hands out only the tensors it manages, or
+// embedded runtimes that have no device allocator at all.  This entry point
+// keeps that scratch in a fixed array that is part of the library's device
+// image instead, so it calls no allocator.  The array
+// (NVFP4_NOALLOC_SCRATCH_BYTES) exists on every GPU that loads the library
+// until the process exits.
 #include <cstdio>
 #include <mutex>
 
@@ -24,21 +24,31 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices];
+struct ScratchAddr {
+  unsigned long long ctx_id = 0;  // the context the address belongs to
+  void* addr = nullptr;
+};
+ScratchAddr g_scratch[kMaxDevices];
 
-// Device address of the scratch on the current device, looked up once per
-// device (with that device current) and cached.
+// Device address of the scratch on the current device, looked up with that
+// device current the first time it is needed in each CUDA context (a context
+// re-created after cudaDeviceReset loads the array again, possibly at another
+// address) and cached.
 nvfp4_status scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_CUDA;
+  unsigned long long ctx = 0;
+  if (!nvfp4::current_context_id(&ctx)) return NVFP4_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  ScratchAddr& s = g_scratch[dev];
+  if (s.addr == nullptr || s.ctx_id != ctx) {
     void* p = nullptr;
     const cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (err != cudaSuccess || p == nullptr) return NVFP4_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+    s.addr = p;
+    s.ctx_id = ctx;
   }
-  *out = g_scratch_addr[dev];
+  *out = s.addr;
   return NVFP4_OK;
 }
 
@@ -47,14 +57,16 @@ nvfp4_status scratch_address(void** out) {
 extern "C" nvfp4_status nvfp4_linear_noalloc(const void* X, int64_t M, const nvfp4_weight* W, void* Y,
                                              int out_dtype, cudaStream_t stream) {
   if (W == nullptr) return nvfp4_linear(X, M, W, Y, out_dtype, nullptr, 0, stream);  // reports the error
-  // M <= crossover takes the W4A16 branch, which needs no scratch at all;
-  // invalid shapes are left to nvfp4_linear to report
+  // The branch is chosen once, here, and passed down, so the scratch size
+  // checked below is the one the executed branch uses even if another thread
+  // changes the crossover table meanwhile.  Invalid shapes are left to
+  // nvfp4_linear's checks to report.
   const bool shape_ok = W->N > 0 && W->K >= 256 && W->K % 64 == 0 && M > 0;
-  const bool needs_scratch = shape_ok && M > nvfp4_get_crossover(W->N, W->K);
-  // the W4A16 branch ignores the workspace, M == 0 launches nothing and bad
+  const bool w4a4 = shape_ok && nvfp4::linear_takes_w4a4(M, W->N, W->K);
+  // the W4A16 branch needs no workspace, M == 0 launches nothing and bad
   // arguments are reported before any device call: none of them needs the
   // scratch, so none of them looks up its address
-  if (!needs_scratch) return nvfp4_linear(X, M, W, Y, out_dtype, nullptr, 0, stream);
+  if (!w4a4) return nvfp4::linear_branch(X, M, W, Y, out_dtype, nullptr, 0, stream, false);
   const size_t need = nvfp4_workspace_bytes(NVFP4_OP_LINEAR, M, W->N, W->K);
   if (need == 0 || need > NVFP4_NOALLOC_SCRATCH_BYTES) {
     char msg[160];
@@ -70,5 +82,5 @@ extern "C" nvfp4_status nvfp4_linear_noalloc(const void* X, int64_t M, const nvf
     nvfp4::set_last_error("nvfp4_linear_noalloc: cannot look up the scratch address on this device");
     return st;
   }
-  return nvfp4_linear(X, M, W, Y, out_dtype, scratch, NVFP4_NOALLOC_SCRATCH_BYTES, stream);
+  return nvfp4::linear_branch(X, M, W, Y, out_dtype, scratch, NVFP4_NOALLOC_SCRATCH_BYTES, stream, true);
 }

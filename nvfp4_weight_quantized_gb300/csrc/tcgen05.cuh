@@ -163,18 +163,6 @@ __device__ __forceinline__ void commit_pair(uint64_t* bar, uint16_t cta_mask) {
       : "memory");
 }
 
-// 2-D tiled TMA load of one box into the same shared-memory offset of every
-// CTA in `cta_mask`, each CTA's mbarrier at `bar`'s offset receiving the bytes
-// that land in it.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
-                                               uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(cta_mask)
-      : "memory");
-}
-
 // The pair form of mma_mxf4nvf4: M = 256 (128 rows in each CTA), B rows split
 // between the two CTAs' shared memory, scales and accumulator in each CTA's
 // TMEM at the same addresses.  Issued by one thread of the even CTA.

@@ -87,11 +87,11 @@ def test_w4a16_sk_knob(L):
 
 def test_w4a4_cluster_knob(L):
     saved = nv.nvfp4_get_w4a4_cluster()
-    assert saved in (1, 2, 4)
-    for v in (1, 2, 4):
+    assert saved in (1, 2)
+    for v in (1, 2):
         nv.nvfp4_set_w4a4_cluster(v)
         assert nv.nvfp4_get_w4a4_cluster() == v
-    for bad in (0, 3, 8):
+    for bad in (0, 3, 4, 8):
         with pytest.raises(nv.NVFP4Error):
             nv.nvfp4_set_w4a4_cluster(bad)
     nv.nvfp4_set_w4a4_cluster(saved)

@@ -234,11 +234,11 @@ def test_w4a4_small(shape, M):
 
 
 def each_w4a4_kernel(fn):
-    """Runs fn() with each W4A4 kernel for M > 128 forced in turn: two CTA
-    pairs sharing A, one CTA pair, single CTAs (M <= 128 has one kernel)."""
+    """Runs fn() with each W4A4 kernel for M > 128 forced in turn: CTA pairs,
+    single CTAs (M <= 128 has one kernel)."""
     saved = nv.nvfp4_get_w4a4_cluster()
     try:
-        for ctas in (4, 2, 1):
+        for ctas in (2, 1):
             nv.nvfp4_set_w4a4_cluster(ctas)
             fn()
     finally:
@@ -249,9 +249,9 @@ def each_w4a4_kernel(fn):
 @pytest.mark.parametrize("M", [129, 160, 200, 256, 300, 513])
 def test_w4a4_both_kernels(shape, M):
     """Every W4A4 kernel for M > 128 matches the oracle: ragged M (a CTA pair
-    whose second CTA has no rows, a 64-row half past M), ragged N (a tile whose
-    second weight half is empty or partial, an odd number of 256-wide tiles so
-    that one pair of a cluster idles), K with a partial last stage."""
+    whose second CTA has no rows), ragged N (a tile whose second weight half
+    is empty or partial, an odd number of 256-wide tiles), K with a partial
+    last stage."""
     N, K = shape
     wref = oracle_weight(synth.weight_normal(N, K, seed=N * 5 + K, outlier_frac=0.01))
     x = synth.act_student_t(M, K, seed=M + 2000)

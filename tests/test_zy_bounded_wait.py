@@ -2,7 +2,9 @@
 fault: nvfp4_selftest_wait_timeout launches one thread that waits on an
 mbarrier nothing completes.  The wait must give up after its cycle limit
 (about 1.5 s), record NVFP4_ERR_TIMEOUT in the device status word and leave
-the CUDA context usable.  Collected last: it takes a second or two."""
+the CUDA context usable.  Collected after the parity tests (it takes a
+second or two) and before the no-alloc entry point's test, which comes
+last."""
 import time
 
 import numpy as np
