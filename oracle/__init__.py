@@ -99,6 +99,8 @@ def _load():
         lib.oracle_dequant_bf16.argtypes = [u8p, u8p, ctypes.c_float, i64, i64, u16p]
         lib.oracle_dequant_bf16.restype = ctypes.c_int
         lib.oracle_gptq_fos.argtypes = [u16p, i64, i64, f32p, ctypes.c_float, i64, u8p, u8p, f32p, f32p]
+        lib.oracle_gptq_fos_ref64.argtypes = [u16p, i64, i64, f32p, ctypes.c_double, u8p, ctypes.c_float, u8p,
+                                              ctypes.c_double, u8p, u8p]
         lib.oracle_gptq_fos.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -352,3 +354,28 @@ def gptq_fos(w_bits: np.ndarray, H: np.ndarray, damp: float = 0.01, block: int =
     if want_u:
         out["U"] = U
     return out
+
+
+def gptq_fos_ref64(w_bits: np.ndarray, H: np.ndarray, scales: np.ndarray, ts: float, damp: float = 0.01,
+                   follow: np.ndarray | None = None, delta: float = 1e-3) -> dict:
+    """The same GPTQ written plainly in binary64, unblocked (nvfp4_oracle.c,
+    oracle_gptq_fos_ref64), on given FourOverSix scales and tensor scale.
+    With `follow` (another run's codes), elements whose quotient lies within
+    `delta` of an E2M1 rounding midpoint take the followed code and are
+    flagged in "near"; a followed code that is not one of the two values
+    either side of that midpoint raises."""
+    w_bits = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    N, K = w_bits.shape
+    H = np.ascontiguousarray(H, dtype=np.float32)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    assert H.shape == (K, K) and scales.shape == (N, K // 16)
+    codes = np.zeros((N, K // 2), np.uint8)
+    near = np.zeros((N, K), np.uint8)
+    fol = None if follow is None else np.ascontiguousarray(follow, dtype=np.uint8)
+    st = _load().oracle_gptq_fos_ref64(_ptr(w_bits, ctypes.c_uint16), N, K, _ptr(H, ctypes.c_float), damp,
+                                       _ptr(scales, ctypes.c_uint8), ts,
+                                       None if fol is None else _ptr(fol, ctypes.c_uint8), delta,
+                                       _ptr(codes, ctypes.c_uint8), _ptr(near, ctypes.c_uint8))
+    if st:
+        raise OracleError(st)
+    return {"codes": codes, "near": near.astype(bool)}

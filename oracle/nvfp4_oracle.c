@@ -507,3 +507,136 @@ int oracle_gptq_fos(const uint16_t* W, int64_t N, int64_t K, const float* H, flo
   free(E);
   return st;
 }
+
+/* ------------------------------------------------------------------------ */
+/* GPTQ with FourOverSix scales, plain binary64 form                        */
+/* ------------------------------------------------------------------------ */
+
+/* Lower Cholesky factor of the symmetric positive definite A [K, K] (binary64,
+ * textbook column form), in place in the lower triangle; 0 on success. */
+static int chol64(double* A, int64_t K) {
+  for (int64_t j = 0; j < K; ++j) {
+    double d = A[j * K + j];
+    for (int64_t k = 0; k < j; ++k) d -= A[j * K + k] * A[j * K + k];
+    if (!(d > 0.0)) return -1;
+    d = sqrt(d);
+    A[j * K + j] = d;
+    for (int64_t i = j + 1; i < K; ++i) {
+      double s = A[i * K + j];
+      for (int64_t k = 0; k < j; ++k) s -= A[i * K + k] * A[j * K + k];
+      A[i * K + j] = s / d;
+    }
+  }
+  return 0;
+}
+
+/* The same GPTQ as oracle_gptq_fos, written from its definition with none of
+ * that function's binary32 order: every quantity in binary64, no blocking.
+ *   Hd    = H + d I, d = damp * mean(diag H);
+ *   Hinv  = Hd^-1 (Cholesky of Hd, then its inverse);
+ *   U     = the upper-triangular factor with Hinv = U^T U (Cholesky of Hinv,
+ *           transposed);
+ *   for each row, columns j in order: q = nearest E2M1 value of w[j] / eff
+ *   (ties to even, saturating at 6; eff = value(scale) * ts of the given
+ *   FourOverSix scales), e = (w[j] - value(q) eff) / U[j][j], and every later
+ *   column c gets w[c] -= e U[j][c] at once.
+ * follow (nullable): the codes of another GPTQ run over the same W, H and
+ * scales.  Where this run's |w[j] / eff| lies within `delta` of an E2M1
+ * rounding midpoint the followed code is taken instead (so both runs go on
+ * from the same decision), near[n * K + j] is set to 1, and the followed
+ * value must be one of the two grid values either side of that midpoint
+ * (else OR_ERR_SHAPE).  codes receives the decisions (sign of zero from the
+ * quotient).  OR_ERR_NONFINITE if Hd or Hinv is not positive definite. */
+int oracle_gptq_fos_ref64(const uint16_t* W, int64_t N, int64_t K, const float* H, double damp,
+                          const uint8_t* scales, float ts, const uint8_t* follow, double delta, uint8_t* codes,
+                          uint8_t* near) {
+  static const double grid[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+  if (N <= 0 || K <= 0 || K % 16 != 0) return OR_ERR_SHAPE;
+  double* A = (double*)malloc(sizeof(double) * K * K);
+  double* Inv = (double*)malloc(sizeof(double) * K * K);
+  double* w = (double*)malloc(sizeof(double) * K);
+  if (!A || !Inv || !w) {
+    free(A); free(Inv); free(w);
+    return OR_ERR_SHAPE;
+  }
+  int st = OR_OK;
+  double dsum = 0.0;
+  for (int64_t k = 0; k < K; ++k) dsum += (double)H[k * K + k];
+  const double dval = damp * (dsum / (double)K);
+  for (int64_t i = 0; i < K * K; ++i) A[i] = (double)H[i];
+  for (int64_t k = 0; k < K; ++k) A[k * K + k] += dval;
+  if (chol64(A, K) != 0) st = OR_ERR_NONFINITE;
+  if (st == OR_OK) {
+    /* Hd^-1 = L^-T L^-1: solve L Y = I column by column, then L^T Z = Y */
+    for (int64_t c = 0; c < K; ++c) {
+      for (int64_t i = 0; i < K; ++i) { /* forward */
+        double s = (i == c) ? 1.0 : 0.0;
+        for (int64_t k = 0; k < i; ++k) s -= A[i * K + k] * Inv[k * K + c];
+        Inv[i * K + c] = s / A[i * K + i];
+      }
+      for (int64_t i = K - 1; i >= 0; --i) { /* backward */
+        double s = Inv[i * K + c];
+        for (int64_t k = i + 1; k < K; ++k) s -= A[k * K + i] * Inv[k * K + c];
+        Inv[i * K + c] = s / A[i * K + i];
+      }
+    }
+    /* symmetrise (the two triangles agree up to rounding), then factor */
+    for (int64_t i = 0; i < K; ++i)
+      for (int64_t j = 0; j < i; ++j) {
+        const double v = 0.5 * (Inv[i * K + j] + Inv[j * K + i]);
+        Inv[i * K + j] = Inv[j * K + i] = v;
+      }
+    if (chol64(Inv, K) != 0) st = OR_ERR_NONFINITE; /* lower C, Hinv = C C^T, U = C^T */
+  }
+#define U64(i, j) Inv[(j) * K + (i)]
+  for (int64_t n = 0; n < N && st == OR_OK; ++n) {
+    for (int64_t k = 0; k < K; ++k) w[k] = (double)oracle_bf16_value(W[n * K + k]);
+    for (int64_t j = 0; j < K && st == OR_OK; ++j) {
+      const double eff = oracle_e4m3_value(scales[n * (K / 16) + j / 16]) * (double)ts;
+      uint8_t q, nflag = 0;
+      double d;
+      if (eff == 0.0) {
+        q = signbit(w[j]) ? 8 : 0;
+        d = w[j];
+      } else {
+        const double x = w[j] / eff, ax = fabs(x);
+        int best = 0;
+        for (int g = 1; g < 8; ++g) {
+          const double dg = fabs(ax - grid[g]), db = fabs(ax - grid[best]);
+          if (dg < db || (dg == db && (g & 1) == 0)) best = g; /* ties to the even code */
+        }
+        /* distance to the nearest rounding midpoint */
+        double md = 1e300;
+        for (int g = 0; g < 7; ++g) {
+          const double m = fabs(ax - 0.5 * (grid[g] + grid[g + 1]));
+          if (m < md) md = m;
+        }
+        q = (uint8_t)((x < 0.0 || (x == 0.0 && signbit(x)) ? 8 : 0) | best);
+        if (follow != NULL && md < delta) {
+          const uint8_t byte = follow[n * (K / 2) + j / 2];
+          const uint8_t fq = (j & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+          const int fm = fq & 7;
+          /* the midpoint next to ax, and the grid values either side of it */
+          int lo = 0;
+          for (int g = 0; g < 7; ++g)
+            if (fabs(ax - 0.5 * (grid[g] + grid[g + 1])) == md) lo = g;
+          if (fm != lo && fm != lo + 1) st = OR_ERR_SHAPE;
+          if (fm != 0 && ((fq & 8) != 0) != (x < 0.0)) st = OR_ERR_SHAPE;
+          q = fq;
+          nflag = 1;
+        }
+        d = w[j] - grid[q & 7] * ((q & 8) ? -1.0 : 1.0) * eff;
+      }
+      if (near != NULL) near[n * K + j] = nflag;
+      const double e = d / U64(j, j);
+      for (int64_t c = j + 1; c < K; ++c) w[c] -= e * U64(j, c);
+      uint8_t* byte = codes + n * (K / 2) + j / 2;
+      *byte = (j & 1) ? (uint8_t)((*byte & 15) | (q << 4)) : (uint8_t)((*byte & 0xF0) | q);
+    }
+  }
+#undef U64
+  free(A);
+  free(Inv);
+  free(w);
+  return st;
+}

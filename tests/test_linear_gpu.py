@@ -110,8 +110,8 @@ def _gate_up_refs(x, wref, path_w4a4, m_rows=None):
                         m_rows=m_rows)
     else:
         y = oracle_w4a16(x if m_rows is None else x[m_rows], wref["codes"], wref["scales"], wref["ts"])
-    F = y.shape[1] // 2
-    return y[:, :F], y[:, F:]
+    F = y.y.shape[1] // 2
+    return y.cols(slice(0, F)), y.cols(slice(F, None))
 
 
 @pytest.mark.parametrize("F", [256, 384, 200])

@@ -567,6 +567,72 @@ def test_gptq_lowers_layer_error():
     assert err(g["codes"]) < 0.9 * err(f["codes"])
 
 
+def _code_values(codes):
+    """E2M1 values of packed codes (+0 and -0 both 0)."""
+    e2 = np.array([oracle.e2m1_value(c) for c in range(16)])
+    return e2[np.stack([codes & 15, codes >> 4], axis=-1).reshape(codes.shape[0], -1)]
+
+
+def test_gptq_ref64_pinned_to_definitions():
+    """The plain binary64 GPTQ itself: with H = c I it is round-to-nearest
+    under the FourOverSix scales (except where the binary32 quotient of the
+    quantiser lands exactly on a rounding midpoint that the binary64 one
+    misses by under 1e-6: those follow the quantiser's code), and on a small
+    case each of its codes rounds the binary64 least-squares continuation of
+    its row (the defining property, solved directly), away from midpoints."""
+    w = synth.weight_normal(16, 128, seed=51, outlier_frac=0.02)
+    f = oracle.quantize_fos(w)
+    r = oracle.gptq_fos_ref64(w, np.eye(128, dtype=np.float32) * 0.5, f["scales"], f["ts"], follow=f["codes"],
+                              delta=1e-6)
+    assert np.array_equal(_code_values(r["codes"]), _code_values(f["codes"]))
+    assert 0 < r["near"].sum() <= 0.01 * r["near"].size  # exact midpoints, and one the binary32 quotient hits
+    free = oracle.gptq_fos_ref64(w, np.eye(128, dtype=np.float32) * 0.5, f["scales"], f["ts"])
+    assert np.array_equal(_code_values(free["codes"])[~r["near"]], _code_values(f["codes"])[~r["near"]])
+    N, K, damp = 4, 48, 0.05
+    w = synth.weight_normal(N, K, seed=52, outlier_frac=0.02)
+    f = oracle.quantize_fos(w)
+    H = _hessian(K, 256, 53)
+    r = oracle.gptq_fos_ref64(w, H, f["scales"], f["ts"], damp=damp)
+    W0 = synth.bf16_bits_to_f32(w).astype(np.float64)
+    H64 = H.astype(np.float64)
+    Hd = H64 + damp * np.mean(np.diag(H64)) * np.eye(K)
+    Q = _dequant64(r["codes"], f["scales"], f["ts"])
+    e4 = np.array([oracle.e4m3_value(b) if (b & 0x7F) != 0x7F else 0.0 for b in range(256)])
+    unit = np.repeat(e4[f["scales"]], 16, axis=1) * f["ts"]
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    checked = 0
+    for n in range(N):
+        for i in range(K):
+            eF = W0[n, :i] - Q[n, :i]
+            u = W0[n, i:] + (np.linalg.solve(Hd[i:, i:], Hd[i:, :i] @ eF) if i else 0.0)
+            x = u[0] / unit[n, i]
+            d = np.sort(np.abs(grid - abs(x)))
+            if d[1] - d[0] < 1e-6:
+                continue
+            assert Q[n, i] / unit[n, i] == np.copysign(grid[np.argmin(np.abs(grid - abs(x)))], x), (n, i, x)
+            checked += 1
+    assert checked >= 0.98 * N * K
+
+
+@pytest.mark.parametrize("N,K,block,damp", [(64, 512, 128, 0.01), (40, 1040, 128, 0.01), (48, 384, 48, 0.1)])
+def test_gptq_binary32_oracle_agrees_with_plain_binary64(N, K, block, damp):
+    """The binary32 GPTQ oracle (the GPU kernel's operation order: index
+    reversal J H J, right-looking Cholesky, lazy 128-column blocks) against
+    the plain unblocked binary64 GPTQ, which shares none of that order: every
+    code agrees, except at elements whose binary64 quotient lies within 1e-3
+    of an E2M1 rounding midpoint, where the binary64 run adopts the binary32
+    code (which must be one of the two values either side) so both go on
+    from the same decision.  A wrong lazy-block update or reversal changes
+    the continuation by far more than rounding and fails here."""
+    w = synth.weight_normal(N, K, seed=N + K, outlier_frac=0.01)
+    H = _hessian(K, 2 * K, N + 7)
+    g = oracle.gptq_fos(w, H, damp=damp, block=block)
+    r = oracle.gptq_fos_ref64(w, H, g["scales"], g["ts"], damp=damp, follow=g["codes"], delta=1e-3)
+    assert np.array_equal(_code_values(r["codes"]), _code_values(g["codes"]))
+    assert r["near"].mean() < 0.01, r["near"].mean()
+    assert not np.array_equal(g["codes"], oracle.quantize_fos(w)["codes"])  # errors were spread
+
+
 def test_silu_mul_reference_closed_forms():
     """The binary64 silu(g) * u of the test utilities at points with closed
     forms: 0 at g = 0, the logistic value at g = 1, the limits g (g >> 0) and
@@ -639,63 +705,142 @@ def test_threaded_oracle_splits_match_single_calls():
         for k in ("codes", "scales", "choice"):
             assert np.array_equal(q[k], ref[k]), (k, threads)
         assert q["m4_count"] == ref["m4_count"]
-        assert np.array_equal(oracle_w4a16(x, ref["codes"], ref["scales"], ref["ts"], threads=threads), y16)
+        assert np.array_equal(oracle_w4a16(x, ref["codes"], ref["scales"], ref["ts"], threads=threads).y, y16)
         assert np.array_equal(oracle_w4a16(x, ref["codes"], ref["scales"], ref["ts"], n_rows=cols,
-                                           threads=threads), y16[:, cols])
+                                           threads=threads).y, y16[:, cols])
         assert np.array_equal(oracle_w4a4(a["codes"], a["scales"], a["ts"], ref["codes"], ref["scales"],
-                                          ref["ts"], threads=threads), y4)
+                                          ref["ts"], threads=threads).y, y4)
         assert np.array_equal(oracle_w4a4(a["codes"], a["scales"], a["ts"], ref["codes"], ref["scales"],
-                                          ref["ts"], m_rows=np.array([12, 3]), n_rows=cols, threads=threads),
+                                          ref["ts"], m_rows=np.array([12, 3]), n_rows=cols, threads=threads).y,
                               y4[np.ix_([12, 3], cols)])
 
 
+def test_gemm_reference_magnitude_sums():
+    """The accumulation allowance's S = sum_k |a_k| |b_k|, which the
+    comparators get from the oracle on sign-cleared operands, equals the
+    binary64 product of the absolute dequantised operands (numpy), for both
+    GEMMs and the straight-through gradients; the W4A16 input-rounding term
+    uses each weight row's sum of |w|."""
+    from nvfp4_testutil import oracle_qat, oracle_w4a16, oracle_w4a4
+    w = synth.weight_normal(40, 256, seed=41, outlier_frac=0.02)
+    ref = oracle.quantize_fos(w)
+    x = synth.act_student_t(9, 256, seed=42)
+    a = oracle.quantize_act(x)
+
+    def deq(codes, scales, ts):
+        vals = np.array([oracle.e2m1_value(c) for c in range(16)])
+        q = np.stack([codes & 15, codes >> 4], axis=-1).reshape(codes.shape[0], -1)
+        sv = np.array([oracle.e4m3_value(b) for b in range(256)])[scales]
+        return vals[q] * np.repeat(sv, 16, axis=1) * ts
+    wd = deq(ref["codes"], ref["scales"], ref["ts"])
+    ad = deq(a["codes"], a["scales"], a["ts"])
+    xd = oracle.bf16_to_f32(x).astype(np.float64)
+    r16 = oracle_w4a16(x, ref["codes"], ref["scales"], ref["ts"])
+    assert np.allclose(r16.s, np.abs(xd) @ np.abs(wd).T, rtol=1e-12, atol=0)
+    assert np.allclose(r16.y, xd @ wd.T, rtol=1e-9, atol=1e-12)
+    assert r16.k == 256
+    assert np.allclose(r16.xin, 2.0 ** -39 * np.max(np.abs(xd), axis=1, keepdims=True) * np.abs(wd).sum(axis=1),
+                       rtol=1e-12, atol=0)
+    r4 = oracle_w4a4(a["codes"], a["scales"], a["ts"], ref["codes"], ref["scales"], ref["ts"])
+    assert np.allclose(r4.s, np.abs(ad) @ np.abs(wd).T, rtol=1e-12, atol=0) and r4.k == 256 and r4.xin is None
+    rng = np.random.default_rng(43)
+    dy = synth.f32_to_bf16_bits(rng.standard_normal((9, 40)).astype(np.float32))
+    w_hat = oracle.dequant_bf16(ref["codes"], ref["scales"], ref["ts"])
+    x_hat = oracle.dequant_bf16(a["codes"], a["scales"], a["ts"])
+    gx, gw = oracle_qat(dy, w_hat, x_hat)
+    dyd = oracle.bf16_to_f32(dy).astype(np.float64)
+    whd, xhd = oracle.bf16_to_f32(w_hat).astype(np.float64), oracle.bf16_to_f32(x_hat).astype(np.float64)
+    assert np.allclose(gx.s, np.abs(dyd) @ np.abs(whd), rtol=1e-12, atol=0) and gx.k == 40
+    assert np.allclose(gw.s, np.abs(dyd).T @ np.abs(xhd), rtol=1e-12, atol=0) and gw.k == 9
+
+
 def test_gemm_tolerance_checker():
-    """The comparator every GEMM parity test uses: per output row,
-    |y - ref| <= GEMM_REL_TOL * max|ref_row| (+ half a bf16 ulp of ref for
-    bf16 outputs), each row on its own scale; non-finite outputs fail."""
-    from nvfp4_testutil import GEMM_REL_TOL, assert_gemm_close, bf16_half_ulp
-    hu = bf16_half_ulp(np.array([1.0, 1.5, 2.0, -3.0, 0.0, 2.0 ** -130, 2.0 ** -126, 3e38]))
-    assert list(hu[:6]) == [2.0 ** -8, 2.0 ** -8, 2.0 ** -7, 2.0 ** -7, 2.0 ** -134, 2.0 ** -134]
-    assert hu[6] == 2.0 ** -134 and hu[7] == 2.0 ** 119
+    """The comparator every GEMM parity test uses (R14): binary32 outputs
+    within 1e-3 of max|ref_row| per row, within 1e-3 (|ref| + rms(ref_row))
+    elementwise and within the accumulation allowance
+    (ceil(k/16) + 8) 2^-23 S; bf16 outputs one of the two bf16 values that
+    bracket ref widened by that allowance; non-finite outputs fail."""
+    from nvfp4_testutil import GemmRef, assert_gemm_close, bf16_bracket
+    # the bf16 bracket, by hand
+    lo, hi = bf16_bracket(np.array([1.0, 1.0 + 2.0 ** -9, -3.1, 0.0, 2.0 ** -130 + 2.0 ** -140, 255.5]))
+    assert list(lo) == [1.0, 1.0, -3.109375, 0.0, 2.0 ** -130, 255.0]  # spacing 2^-6 in [2, 4)
+    assert list(hi) == [1.0, 1.0 + 2.0 ** -7, -3.09375, 0.0, 2.0 ** -130 + 2.0 ** -133, 256.0]
+    # the allowance, by hand
     ref = np.array([[1.0, -0.5, 0.25], [1e-6, -2e-6, 3e-6]])
-    tol = GEMM_REL_TOL * np.max(np.abs(ref), axis=1, keepdims=True)
-    assert_gemm_close(ref + 0.99 * tol, ref, bf16=False)
+    g = GemmRef(ref, np.ones_like(ref), 4096)
+    assert np.all(g.allowance() == 264 * 2.0 ** -23 + 16 * 2.0 ** -149)
+    # binary32: the allowance binds when S is small...
+    small = GemmRef(ref, np.abs(ref) * 10, 64)  # acc = 12 * 2^-23 * 10 |ref|, far inside the R14 bounds
+    acc = small.allowance()
+    assert_gemm_close(ref + 0.99 * acc, small, bf16=False)
+    bump = np.zeros_like(ref)
+    bump[1, 2] = 1.01
     with pytest.raises(AssertionError):
-        assert_gemm_close(ref + 1.01 * tol * np.array([[0, 0, 0], [0, 1, 0]]), ref, bf16=False)  # small row
-    with pytest.raises(AssertionError):
-        assert_gemm_close(ref + 1.01 * tol * np.array([[1, 0, 0], [0, 0, 0]]), ref, bf16=False)
-    half = bf16_half_ulp(ref)
-    assert_gemm_close(ref + 0.99 * tol + 0.9 * half, ref, bf16=True)
-    with pytest.raises(AssertionError):
-        assert_gemm_close(ref + 0.99 * tol + 1.2 * half, ref, bf16=False)
-    with pytest.raises(AssertionError):
-        assert_gemm_close(ref + tol + 1.1 * half, ref, bf16=True)
+        assert_gemm_close(ref + bump * acc, small, bf16=False)
+    # ...and the R14 clauses bind when S is large
+    big = GemmRef(ref, np.full_like(ref, 1e6), 64)
+    rms = np.sqrt(np.mean(ref * ref, axis=1, keepdims=True))
+    elem = 1e-3 * (np.abs(ref) + rms)
+    rowb = 1e-3 * np.max(np.abs(ref), axis=1, keepdims=True)
+    tight = np.minimum(elem, rowb)
+    assert_gemm_close(ref + 0.99 * tight, big, bf16=False)
+    with pytest.raises(AssertionError):  # elementwise clause on a small element of the first row
+        assert_gemm_close(ref + np.array([[0, 0, 1.01], [0, 0, 0]]) * elem, big, bf16=False)
+    with pytest.raises(AssertionError):  # row clause on the small-scale row
+        assert_gemm_close(ref + np.array([[0, 0, 0], [0, 1.01, 0]]) * rowb, big, bf16=False)
     bad = ref.copy()
     bad[0, 1] = np.nan
     with pytest.raises(AssertionError):
-        assert_gemm_close(bad, ref, bf16=False)
+        assert_gemm_close(bad, big, bf16=False)
     with pytest.raises(AssertionError):
-        assert_gemm_close(ref[:, :2], ref, bf16=False)
-    # bf16 rounding of an exact result always passes
+        assert_gemm_close(ref[:, :2], big, bf16=False)
+    with pytest.raises(AssertionError):  # a bare array carries no allowance
+        assert_gemm_close(ref, ref, bf16=False)
+    # bf16: both neighbours of an exact value pass, the next ones fail
     rng = np.random.default_rng(33)
     exact = rng.standard_normal((6, 50)) * np.exp(rng.uniform(-20, 20, (6, 1)))
+    exact_ref = GemmRef(exact, np.abs(exact) * 1e-3, 16)  # allowance far below half a bf16 step
+    lo, hi = bf16_bracket(exact)
+    assert_gemm_close(lo, exact_ref, bf16=True)
+    assert_gemm_close(hi, exact_ref, bf16=True)
     rounded = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(exact.astype(np.float32))).astype(np.float64)
-    assert_gemm_close(rounded, exact, bf16=True)
+    assert_gemm_close(rounded, exact_ref, bf16=True)
+    below, _ = bf16_bracket(np.nextafter(lo, -np.inf))
+    with pytest.raises(AssertionError):
+        assert_gemm_close(np.where(np.arange(50) == 7, below, lo), exact_ref, bf16=True)
+    # a near-zero element: the allowance lets the accumulated value round either way
+    z = np.array([[2.0 ** -40, 1.0]])
+    zr = GemmRef(z, np.array([[1.0, 1.0]]), 16)  # allowance ~ 2^-20 >> 2^-40
+    assert_gemm_close(np.array([[-2.0 ** -22, 1.0]]), zr, bf16=True)
+    with pytest.raises(AssertionError):
+        assert_gemm_close(np.array([[-2.0 ** -15, 1.0]]), zr, bf16=True)
 
 
 def test_silu_mul_tolerance_checker():
     """The gated projection's comparator: |y - silu(g) u| within
-    SILU_MUL_REL_TOL * max|g_row| * max|u_row| (+ half a bf16 ulp)."""
-    from nvfp4_testutil import SILU_MUL_REL_TOL, assert_silu_mul_close, silu_mul_ref
+    1.1 eg (|u| + eu) + |silu(g)| eu + 2^-19 (1 + |g|) |silu(g) u| (eg, eu the
+    GEMM allowances), bf16 in the bracket of that interval; gate and up
+    swapped fail."""
+    from nvfp4_testutil import GemmRef, assert_silu_mul_close, bf16_bracket, silu_mul_allowance, silu_mul_ref
     rng = np.random.default_rng(34)
-    g = rng.standard_normal((3, 40)) * 3
-    u = rng.standard_normal((3, 40))
-    y = silu_mul_ref(g, u)
-    tol = SILU_MUL_REL_TOL * np.max(np.abs(g), axis=1, keepdims=True) * np.max(np.abs(u), axis=1, keepdims=True)
-    assert_silu_mul_close(y + 0.99 * tol, g, u, bf16=False)
+    gy = rng.standard_normal((3, 40)) * 3
+    uy = rng.standard_normal((3, 40))
+    g = GemmRef(gy, np.abs(gy) * 4, 256)
+    u = GemmRef(uy, np.abs(uy) * 4, 256)
+    y = silu_mul_ref(gy, uy)
+    allow = silu_mul_allowance(g, u)
+    eg, eu = g.allowance(), u.allowance()
+    sg = silu_mul_ref(gy, np.ones_like(gy))
+    assert np.allclose(allow, 1.1 * eg * (np.abs(uy) + eu) + np.abs(sg) * eu +
+                       2.0 ** -19 * (1 + np.abs(gy)) * np.abs(y) + 2.0 ** -140, rtol=1e-15, atol=0)
+    assert_silu_mul_close(y + 0.99 * allow, g, u, bf16=False)
     bump = np.zeros_like(y)
     bump[2, 7] = 1.01
     with pytest.raises(AssertionError):
-        assert_silu_mul_close(y + bump * tol, g, u, bf16=False)
+        assert_silu_mul_close(y + bump * allow, g, u, bf16=False)
     with pytest.raises(AssertionError):
-        assert_silu_mul_close(silu_mul_ref(u, g), g, u, bf16=False)  # gate and up swapped
+        assert_silu_mul_close(silu_mul_ref(uy, gy), g, u, bf16=False)  # gate and up swapped
+    lo, hi = bf16_bracket(y)
+    assert_silu_mul_close(lo, g, u, bf16=True)
+    assert_silu_mul_close(hi, g, u, bf16=True)
+
