@@ -44,8 +44,7 @@
  *     (nvfp4_set_act_fos), the weight-prefetch flag
  *     (nvfp4_set_weight_prefetch) and the device status word, besides
  *     host-side lookups made once (the driver's tensor-map encoder, per-kernel
- *     occupancy, per-device attributes, one cuBLAS handle per device for
- *     nvfp4_qat_backward) and the static scratch array of
+ *     occupancy, per-device attributes) and the static scratch array of
  *     nvfp4_linear_noalloc.  Tensor maps are encoded on every call.
  */
 #ifndef NVFP4_H_
@@ -197,8 +196,8 @@ nvfp4_status nvfp4_quantize_act(const void* X, int64_t M, int64_t K, float divis
  *   X      in:  device bf16 [M, K];  M >= 0 (M == 0 launches nothing)
  *   W      in:  quantised weight; K % 64 == 0
  *   Y      out: device [M, N] of out_dtype
- * Three kernels implement it.  For small M (see nvfp4_set_w4a16_sk_max_m): a
- * persistent split-K kernel (one CTA per SM; clusters of up to 8 CTAs each
+ * Three kernels implement it.  For small M (see
+ * nvfp4_set_w4a16_sk_max_m): a persistent split-K kernel (one CTA per SM; clusters of up to 8 CTAs each
  * own a run of 128-row weight tiles, CTA r of a cluster a K slice of every
  * one, the slices of a tile summed through distributed shared memory) that
  * keeps its K slice of X in shared memory as f16 scaled per token by a power
@@ -208,7 +207,7 @@ nvfp4_status nvfp4_quantize_act(const void* X, int64_t M, int64_t K, float divis
  * dequantised into tensor memory for tcgen05 MMAs.  All give the same result
  * up to fp32 summation order, except that the split-K kernel's f16 copy of X
  * rounds elements more than 2^29 below their token's largest magnitude in a
- * K slice (an absolute error below 2^-25 of that magnitude).  The workspace
+ * K slice (an absolute error below 2^-40 of that magnitude).  The workspace
  * arguments are unused (NULL, 0).
  */
 nvfp4_status nvfp4_gemm_w4a16(const void* X, int64_t M, const nvfp4_weight* W, void* Y,
@@ -295,11 +294,12 @@ nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales_mma,
  *   dW = dY^T X_hat   (fp32 [N, K]; skipped if dW is NULL)
  * with W_hat, X_hat the nvfp4_dequantize bf16 values of W and of the
  * quantised activations (a_codes, a_scales_mma, a_tensor_scale from
- * nvfp4_quantize_act or nvfp4_quantize_fos), fp32 accumulation (cuBLAS).
+ * nvfp4_quantize_act or nvfp4_quantize_fos), fp32 accumulation.  Both
+ * products run on this library's tensor-core kernel (tcgen05 kind::f16 on
+ * CTA pairs); W_hat^T, X_hat^T and dY^T are formed in the workspace first
+ * (dequantised or transposed straight into that layout).
  *   dY         in: device bf16 [M, N]
  *   workspace  nvfp4_workspace_bytes(NVFP4_OP_QAT_BACKWARD, M, N, K) bytes
- * Not capturable in a CUDA graph (the library's cuBLAS handle is created on
- * first use and shared, under a lock, by all callers on the device).
  */
 nvfp4_status nvfp4_qat_backward(const void* dY, int64_t M, const nvfp4_weight* W,
                                 const uint8_t* a_codes, const uint8_t* a_scales_mma,

@@ -222,9 +222,9 @@ size_t nvfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
       return nvfp4::gptq_workspace_bytes(N, K) + align256((size_t)N * (size_t)(K / 16)) +
              align256(nvfp4::quant_workspace_bytes());
     case NVFP4_OP_QAT_BACKWARD:
-      // bf16 W_hat [N, K] and X_hat [M, K]
+      // transposed bf16 operands of the two tensor-core GEMMs
       if (M <= 0 || N <= 0) return 0;
-      return align256((size_t)N * (size_t)K * 2) + align256((size_t)M * (size_t)K * 2);
+      return nvfp4::qat_workspace_bytes(M, N, K);
     case NVFP4_OP_LINEAR_SILU_MUL:
       // the linear workspace, then fp32 [min(M, chunk), N] for an unfused silu(G) * U
       if (M <= 0 || N <= 0) return 0;
@@ -473,23 +473,15 @@ nvfp4_status nvfp4_qat_backward(const void* dY, int64_t M, const nvfp4_weight* W
     return fail(NVFP4_ERR_INVALID_ARG, "qat_backward: dY (and the quantised activations for dW) are required");
   if (!aligned(dY, 16) || (dX != nullptr && !aligned(dX, 16)) || (dW != nullptr && !aligned(dW, 16)))
     return fail(NVFP4_ERR_ALIGN, "qat_backward: pointers must be 16-byte aligned");
-  const size_t wbytes = align256((size_t)N * (size_t)K * 2);
   if (workspace == nullptr || !aligned(workspace, 256) ||
       workspace_bytes < nvfp4_workspace_bytes(NVFP4_OP_QAT_BACKWARD, M, N, K))
     return fail(NVFP4_ERR_WORKSPACE, "qat_backward: workspace missing, not 256-byte aligned or too small");
-  uint8_t* w_hat = static_cast<uint8_t*>(workspace);
-  uint8_t* x_hat = w_hat + wbytes;
-  if (dX != nullptr && (st = nvfp4_dequantize(W->codes, W->scales_mma, W->tensor_scale, N, K, w_hat, stream)) !=
-                           NVFP4_OK)
-    return st;
-  if (dW != nullptr &&
-      (st = nvfp4_dequantize(a_codes, a_scales_mma, a_tensor_scale, M, K, x_hat, stream)) != NVFP4_OK)
-    return st;
-  const int bst = nvfp4::qat_backward_gemms(dY, w_hat, x_hat, M, N, K, dX, dW, stream);
-  if (bst != 0) {
-    nvfp4::set_last_error("qat_backward: cuBLAS GEMM failed");
-    return NVFP4_ERR_CUDA;
-  }
+  const DeviceInfo* d = nullptr;
+  if ((st = device_info(&d)) != NVFP4_OK) return st;
+  const cudaError_t err = nvfp4::qat_backward(dY, M, W->codes, W->scales_mma, W->tensor_scale, N, K, a_codes,
+                                              a_scales_mma, a_tensor_scale, dX, dW, workspace, d->status, stream);
+  if (err == cudaErrorNotSupported) return fail(NVFP4_ERR_UNSUPPORTED, "qat_backward: unsupported size");
+  if (err != cudaSuccess) return fail_cuda(err, "qat_backward launch");
   return NVFP4_OK;
 }
 

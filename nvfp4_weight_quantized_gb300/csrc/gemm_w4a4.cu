@@ -453,13 +453,25 @@ constexpr uint32_t kPairSfStageCols = 16 + 32;        // A: 4 MMAs x 4; B: 4 MMA
 static_assert(kPairSfCol + kPairStages * kPairSfStageCols <= kTmemCols, "TMEM budget");
 // kind::mxf4nvf4, E2M1 x E2M1, K-major, N = 256, UE4M3 scales, M = 256
 constexpr uint32_t kPairIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(256 >> 3) << 17) | (2u << 27);
+// kind::f16 (the bf16 mode below): fp32 accumulator (bits 4-5 = 1), A and B
+// bf16 (format 1 in bits 7-9 and 10-12), both K-major, N >> 3 in bits 17-22,
+// M >> 4 in bits 24-28 (M = 256 across the pair), dense
+constexpr uint32_t kPairIdescBf16 =
+    (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(256 >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
 
+// kBF16: the same pipeline as a plain bf16 GEMM, Y = A B^T with A [M, Kb] and
+// B [N, Kb] bf16, both K-major: a 128-byte row of a stage holds 64 bf16 (256
+// FP4 elements in the NVFP4 mode), the MMAs are kind::f16 with K = 16 (32
+// bytes, the same descriptor step), and there are no scale factors (the
+// scale producer and loaders only pass the stage on) and no tensor scales.
+// The caller passes K = 4 * Kb rounded up to 64, so that K / 64 counts the
+// 16-wide MMA steps.
 // kGateUp: W is a gated-MLP input projection [2F, K] (rows [0, F) gate,
 // [F, 2F) up, F % 128 == 0) and the kernel writes Y[m, f] = silu(G) * U for
 // F features: a tile covers 128 features, CTA 0 of the pair staging their
 // gate rows and CTA 1 their up rows, so accumulator column j (< 128) of every
 // row holds G[m, f0 + j] and column 128 + j holds U[m, f0 + j].
-template <bool kF32, bool kGateUp = false>
+template <bool kF32, bool kGateUp = false, bool kBF16 = false>
 __global__ void __launch_bounds__(kPairThreads, 1)
 w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                  const __grid_constant__ CUtensorMap tmap_y, int tma_store, const uint8_t* __restrict__ a_smma,
@@ -517,7 +529,7 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         const bool has_a = arow < M, has_b = brow < N;
         const uint32_t a_bytes = has_a ? kABytes : 0;
         const int64_t sfb_left = b_row_tiles - n0 / 128;
-        const int nsfb = kGateUp ? 2 : sfb_left <= 0 ? 0 : sfb_left < 2 ? (int)sfb_left : 2;
+        const int nsfb = kBF16 ? 0 : kGateUp ? 2 : sfb_left <= 0 ? 0 : sfb_left < 2 ? (int)sfb_left : 2;
         for (int ks = 0; ks < kt; ++ks, ++g) {
           const int s = g % S;
           if (g >= S && !mbar_wait(&sm.empty[s], (uint32_t)(g / S - 1) & 1u)) {
@@ -527,9 +539,9 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
           const int kk_n = min(4, kb64 - 4 * ks);
           const uint32_t sf_bytes = (uint32_t)kk_n * kScaleTileBytes;
           if (warp == kProducerWarp) {
-            mbar_arrive_expect_tx(&sm.full[s], a_bytes + (has_a ? sf_bytes : 0));
+            mbar_arrive_expect_tx(&sm.full[s], a_bytes + (has_a && !kBF16 ? sf_bytes : 0));
             if (has_a) tma_load_2d(sm.a[s], &tmap_a, ks * (BK / 2), (int)arow, &sm.full[s]);
-            if (has_a)
+            if (has_a && !kBF16)
               bulk_load(sm.sfa[s], a_smma + ((arow / 128) * kb64 + 4 * ks) * kScaleTileBytes, sf_bytes,
                         &sm.full[s]);
           } else if (warp == kProdB) {
@@ -578,9 +590,14 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
           const uint32_t sfb_t = sfa_t + 16;
           const uint64_t adesc = smem_desc(smem_addr(sm.a[s]), 0, 1024, 2);
           const uint64_t bdesc = smem_desc(smem_addr(sm.b[s]), 0, 1024, 2);
-          for (int kk = 0; kk < kk_n; ++kk)
-            mma_mxf4nvf4_pair(tmem, adesc + 2ull * kk, bdesc + 2ull * kk, kPairIdesc, sfa_t + 4 * kk,
-                              sfb_t + 8 * kk, (ks | kk) != 0);
+          if (kBF16) {
+            for (int kk = 0; kk < kk_n; ++kk)
+              mma_f16_pair(tmem, adesc + 2ull * kk, bdesc + 2ull * kk, kPairIdescBf16, (ks | kk) != 0);
+          } else {
+            for (int kk = 0; kk < kk_n; ++kk)
+              mma_mxf4nvf4_pair(tmem, adesc + 2ull * kk, bdesc + 2ull * kk, kPairIdesc, sfa_t + 4 * kk,
+                                sfb_t + 8 * kk, (ks | kk) != 0);
+          }
           commit_pair(&sm.empty[s], pair_mask);
         }
         if (!failed) commit_pair(&sm.acc_full, pair_mask);
@@ -601,30 +618,32 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
           break;
         }
         const uint32_t col = tmem + lane_base + kPairSfCol + kPairSfStageCols * s;
-        uint32_t r[16];
+        if (!kBF16) {  // bf16 mode: no scale factors, the stage is only passed on
+          uint32_t r[16];
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint4 v = *reinterpret_cast<const uint4*>(sm.sfa[s] + kk * kScaleTileBytes + lane * 16);
-          r[4 * kk] = v.x;
-          r[4 * kk + 1] = v.y;
-          r[4 * kk + 2] = v.z;
-          r[4 * kk + 3] = v.w;
-        }
-        tmem_st_x16(col, r);
-#pragma unroll
-        for (int h = 0; h < 8; h += 4) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int idx = h + q;  // = 2 kk + rt
-            const int kk = idx >> 1, rt = idx & 1;
-            const uint4 v =
-                *reinterpret_cast<const uint4*>(sm.sfb[s] + rt * kSfaBytes + kk * kScaleTileBytes + lane * 16);
-            r[4 * q] = v.x;
-            r[4 * q + 1] = v.y;
-            r[4 * q + 2] = v.z;
-            r[4 * q + 3] = v.w;
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint4 v = *reinterpret_cast<const uint4*>(sm.sfa[s] + kk * kScaleTileBytes + lane * 16);
+            r[4 * kk] = v.x;
+            r[4 * kk + 1] = v.y;
+            r[4 * kk + 2] = v.z;
+            r[4 * kk + 3] = v.w;
           }
-          tmem_st_x16(col + 16 + 4 * h, r);
+          tmem_st_x16(col, r);
+#pragma unroll
+          for (int h = 0; h < 8; h += 4) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int idx = h + q;  // = 2 kk + rt
+              const int kk = idx >> 1, rt = idx & 1;
+              const uint4 v =
+                  *reinterpret_cast<const uint4*>(sm.sfb[s] + rt * kSfaBytes + kk * kScaleTileBytes + lane * 16);
+              r[4 * q] = v.x;
+              r[4 * q + 1] = v.y;
+              r[4 * q + 2] = v.z;
+              r[4 * q + 3] = v.w;
+            }
+            tmem_st_x16(col + 16 + 4 * h, r);
+          }
         }
         tmem_wait_st();
         fence_before_sync();
@@ -636,7 +655,7 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
   } else {
     // ---------------- epilogue (each CTA; TMEM lane = tile row) ----------------
     griddep_wait();  // the tensor scales may come from the previous kernel in the stream
-    const float alpha = __fmul_rn(*a_ts, *b_ts);
+    const float alpha = kBF16 ? 1.0f : __fmul_rn(*a_ts, *b_ts);
     const bool vec_ok = kF32 ? (N % 4 == 0) : (N % 8 == 0);
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const int r = warp * 32 + lane;
@@ -822,6 +841,21 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_by
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row-major [rows, pitch_bytes] matrix of which the first row_bytes of each
+// row are the tensor (zero fill beyond them and past the last row), boxes of
+// [128 rows, 128 bytes], 128-byte swizzle.
+bool make_map_pitch(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes, uint64_t pitch_bytes) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Y as bf16 [M, N] for TMA stores: boxes of 128 rows x 64 columns (128
 // bytes), 128-byte swizzle.
 bool make_y_map(CUtensorMap* map, void* y, uint64_t M, uint64_t N) {
@@ -927,6 +961,60 @@ cudaError_t launch_pairs(const uint8_t* a_codes, const uint8_t* a_smma, const fl
 }
 
 }  // namespace
+
+cudaError_t launch_gemm_bf16_tn(const void* a, int64_t pitch_a, const void* b, int64_t pitch_b, int64_t rows_a,
+                                int64_t rows_b, int64_t red, void* y, bool out_f32, unsigned int* status,
+                                cudaStream_t stream) {
+  if (rows_a <= 0 || rows_b <= 0) return cudaSuccess;
+  if (red <= 0 || pitch_a < red || pitch_b < red || pitch_a % 8 != 0 || pitch_b % 8 != 0 || rows_a > INT32_MAX ||
+      rows_b > INT32_MAX || red > ((int64_t)1 << 28))
+    return cudaErrorNotSupported;
+  CUtensorMap ma, mb, my;
+  if (!make_map_pitch(&ma, a, (uint64_t)rows_a, (uint64_t)red * 2, (uint64_t)pitch_a * 2) ||
+      !make_map_pitch(&mb, b, (uint64_t)rows_b, (uint64_t)red * 2, (uint64_t)pitch_b * 2))
+    return cudaErrorInvalidValue;
+  int tma_store = (!out_f32 && rows_b % 8 == 0) ? 1 : 0;
+  memset(&my, 0, sizeof my);
+  if (tma_store && !make_y_map(&my, y, (uint64_t)rows_a, (uint64_t)rows_b)) tma_store = 0;
+  const size_t smem = sizeof(PairSmem) + 1024;
+  auto kern = out_f32 ? w4a4_pair_kernel<true, false, true> : w4a4_pair_kernel<false, false, true>;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kPairThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  static int max_clusters[2] = {0, 0};  // per output type (the device is fixed for the process)
+  static std::once_flag once[2];
+  cudaError_t err = cudaSuccess;
+  std::call_once(once[out_f32 ? 1 : 0], [&] {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return;
+    cudaLaunchConfig_t q = cfg;
+    q.gridDim = dim3(2);
+    q.numAttrs = 1;  // the cluster shape only
+    int n = 0;
+    err = cudaOccupancyMaxActiveClusters(&n, kern, &q);
+    max_clusters[out_f32 ? 1 : 0] = err == cudaSuccess ? n : 0;
+  });
+  if (err != cudaSuccess) return err;
+  const int mc = max_clusters[out_f32 ? 1 : 0];
+  if (mc < 1) return cudaErrorNotSupported;
+  const int64_t work = ((rows_a + 255) / 256) * ((rows_b + 255) / 256);
+  cfg.gridDim = dim3((unsigned)(2 * std::min<int64_t>(work, mc)));
+  const int64_t k4 = 4 * ((red + 15) / 16 * 16);  // 16-wide MMA steps, counted as in the NVFP4 mode
+  const uint8_t* no_sf = nullptr;
+  const float* no_ts = nullptr;
+  return cudaLaunchKernelEx(&cfg, kern, ma, mb, my, tma_store, no_sf, no_sf, no_ts, no_ts, rows_a, rows_b, k4, y,
+                            status);
+}
 
 cudaError_t launch_gemm_w4a4_gate_up(const uint8_t* a_codes, const uint8_t* a_scales_mma, const float* a_ts,
                                      int64_t M, const uint8_t* w_codes, const uint8_t* w_scales_mma,

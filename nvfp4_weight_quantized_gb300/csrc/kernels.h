@@ -70,16 +70,29 @@ cudaError_t launch_gemm_w4a4_gate_up(const uint8_t* a_codes, const uint8_t* a_sc
                                      int64_t M, const uint8_t* w_codes, const uint8_t* w_scales_mma,
                                      const float* w_ts, int64_t N, int64_t K, void* y, unsigned int* status,
                                      cudaStream_t stream);
+// Y [rows_a, rows_b] (bf16, or fp32 when out_f32) = A B^T for bf16 A
+// [rows_a, red] and B [rows_b, red] whose rows are pitch_a / pitch_b elements
+// apart (multiples of 8), on the CTA-pair tensor-core kernel (tcgen05
+// kind::f16, fp32 accumulation).  cudaErrorNotSupported for a bad pitch or
+// when no pair can be resident.
+cudaError_t launch_gemm_bf16_tn(const void* a, int64_t pitch_a, const void* b, int64_t pitch_b, int64_t rows_a,
+                                int64_t rows_b, int64_t red, void* y, bool out_f32, unsigned int* status,
+                                cudaStream_t stream);
 // Y[m, f] = silu(y2[m, f]) * y2[m, F + f] for y2 fp32 [M, 2F]; Y [M, F].
 cudaError_t launch_silu_mul(const float* y2, int64_t M, int64_t F, void* y, bool out_f32, cudaStream_t stream);
 
 // NVFP4 [R, K] (codes, MMA-tiled scales, device tensor scale) -> bf16 [R, K].
 cudaError_t launch_dequant_bf16(const uint8_t* codes, const uint8_t* scales_mma, const float* ts, int64_t R,
                                 int64_t K, void* out, int num_sms, cudaStream_t stream);
-// dX = dY W_hat (bf16 [M, K], skipped if null) and dW = dY^T X_hat (fp32
-// [N, K], skipped if null) on cuBLAS; 0 or a cublasStatus_t.
-int qat_backward_gemms(const void* dy, const void* w_hat, const void* x_hat, int64_t M, int64_t N, int64_t K,
-                       void* dx, void* dw, cudaStream_t stream);
+// The straight-through backward of Y = X_hat W_hat^T (qat.cu): dX = dY W_hat
+// (bf16 [M, K], skipped if null) and dW = dY^T X_hat (fp32 [N, K], skipped if
+// null) for dY bf16 [M, N], W NVFP4 [N, K] and the quantised activations
+// [M, K]; workspace of qat_workspace_bytes(M, N, K) (transposed bf16
+// operands).
+size_t qat_workspace_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t qat_backward(const void* dy, int64_t M, const uint8_t* w_codes, const uint8_t* w_smma, const float* w_ts,
+                         int64_t N, int64_t K, const uint8_t* a_codes, const uint8_t* a_smma, const float* a_ts,
+                         void* dx, void* dw, void* workspace, unsigned int* status, cudaStream_t stream);
 
 // GPTQ inside FourOverSix scales (see gptq.cu): W bf16 [N, K], H fp32 [K, K],
 // scales logical [N, K/16] and ts from the FourOverSix quantiser on W; codes

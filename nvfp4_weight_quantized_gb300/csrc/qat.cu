@@ -6,12 +6,15 @@
 // FP4 itself (nvfp4_gemm_w4a4 here) and the backward pass sends the
 // gradients straight through the quantisers to the bf16 master weights.  For
 // Y = X_hat W_hat^T that gives dX = dY W_hat and dW = dY^T X_hat, plain bf16
-// GEMMs: the NVFP4 operands are dequantised to bf16 by dequant_bf16_kernel
-// and the two products run on cuBLAS (fp32 accumulation).
-#include <cublas_v2.h>
-
-#include <map>
-#include <mutex>
+// GEMMs with fp32 accumulation.  Both run on this library's CTA-pair
+// tensor-core kernel in its bf16 mode (tcgen05 kind::f16, launch_gemm_bf16_tn),
+// which wants both operands K-major (the reduced index contiguous):
+//   dX [M, K] = dY [M, N] * (W_hat^T [K, N])^T   -- reduced over N;
+//   dW [N, K] = dY^T [N, M] * (X_hat^T [K, M])^T  -- reduced over M;
+// so the NVFP4 operands are dequantised straight into transposed bf16
+// buffers (dequant_bf16_t_kernel) and dY is transposed (transpose_bf16_kernel),
+// rows padded with zeros to a multiple of 16 elements.
+#include <algorithm>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -21,10 +24,18 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kTile = 64;        // transposing kernels: 64 x 64 tiles
+constexpr int kTilePitch = 72;   // bf16 per shared-memory tile row (16-byte aligned, fewer bank conflicts)
 
-// One 16-element block per thread and step: value(code) * value(scale) is
-// exact in binary32 (at most 2 + 4 significant bits), times the tensor scale
-// rounded once, then rounded to bf16; 8 code bytes in, 32 bytes out.
+// value(code) * value(scale) is exact in binary32 (at most 2 + 4 significant
+// bits); times the tensor scale rounded once; then rounded to bf16 (reading
+// R18 of the design notes).
+__device__ __forceinline__ float dequant_value(uint32_t code, float s, float ts) {
+  const float mag = e2m1_mag_to_f32(code & 7u);
+  return __fmul_rn(__fmul_rn(code & 8u ? -mag : mag, s), ts);
+}
+
+// One 16-element block per thread and step: 8 code bytes in, 32 bytes out.
 __global__ void __launch_bounds__(kThreads)
 dequant_bf16_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ smma,
                     const float* __restrict__ ts_ptr, int64_t R, int64_t K, __nv_bfloat16* __restrict__ out) {
@@ -39,14 +50,7 @@ dequant_bf16_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const uint32_t byte = ((j < 4 ? cw.x : cw.y) >> (8 * (j & 3))) & 0xFFu;
-      float q[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t code = (byte >> (4 * h)) & 15u;
-        const float mag = e2m1_mag_to_f32(code & 7u);
-        q[h] = __fmul_rn(__fmul_rn(code & 8u ? -mag : mag, s), ts);
-      }
-      __nv_bfloat162 p = __floats2bfloat162_rn(q[0], q[1]);
+      __nv_bfloat162 p = __floats2bfloat162_rn(dequant_value(byte & 15u, s, ts), dequant_value(byte >> 4, s, ts));
       o[j] = *reinterpret_cast<uint32_t*>(&p);
     }
     uint4* dst = reinterpret_cast<uint4*>(out + r * K + 16 * c);
@@ -55,21 +59,91 @@ dequant_bf16_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict
   }
 }
 
-std::mutex g_blas_mu;
-std::map<int, cublasHandle_t> g_blas;  // per device, created on first use
-
-cublasStatus_t blas_handle(cublasHandle_t* h) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return CUBLAS_STATUS_NOT_INITIALIZED;
-  auto it = g_blas.find(dev);
-  if (it != g_blas.end()) {
-    *h = it->second;
-    return CUBLAS_STATUS_SUCCESS;
+// NVFP4 [R, K] -> bf16 out^T [K, Rp] (out[k * Rp + r]), columns R .. Rp - 1
+// zero; Rp % 8 == 0.  A CTA dequantises a 64 x 64 tile (one 16-element block
+// per thread), transposes it in shared memory and writes 64 rows of 128 bytes.
+__global__ void __launch_bounds__(kThreads)
+dequant_bf16_t_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ smma,
+                      const float* __restrict__ ts_ptr, int64_t R, int64_t K, int64_t Rp,
+                      __nv_bfloat16* __restrict__ out) {
+  __shared__ __align__(16) __nv_bfloat16 tile[kTile][kTilePitch];
+  griddep_wait();
+  const float ts = *ts_ptr;
+  const int64_t kb = K / 16, ct = (kb + 3) / 4;
+  const int64_t r0 = (int64_t)blockIdx.x * kTile, k0 = (int64_t)blockIdx.y * kTile;
+  {
+    const int rl = threadIdx.x & 63, cl = threadIdx.x >> 6;  // row, 16-block of the tile
+    const int64_t r = r0 + rl, c = k0 / 16 + cl;
+    __nv_bfloat16 v[16];
+    if (r < R && c < kb) {
+      const uint2 cw = *reinterpret_cast<const uint2*>(codes + r * (K / 2) + 8 * c);
+      const float s = e4m3_to_f32(smma[scale_mma_offset(r, c, ct)]);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        v[j] = __float2bfloat16_rn(dequant_value(((j < 8 ? cw.x : cw.y) >> (4 * (j & 7))) & 15u, s, ts));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = __float2bfloat16_rn(0.0f);
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) tile[16 * cl + j][rl] = v[j];
   }
-  cublasStatus_t st = cublasCreate(h);
-  if (st == CUBLAS_STATUS_SUCCESS) g_blas[dev] = *h;
-  return st;
+  __syncthreads();
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const int kl = (threadIdx.x >> 3) + 32 * pass, v8 = threadIdx.x & 7;
+    const int64_t k = k0 + kl, r = r0 + 8 * v8;
+    if (k < K && r < Rp)
+      *reinterpret_cast<uint4*>(out + k * Rp + r) = *reinterpret_cast<const uint4*>(&tile[kl][8 * v8]);
+  }
 }
+
+// bf16 [rows, cols] (row pitch `spitch`) -> dst, zero-padded: kTranspose:
+// dst^T [cols, rows_p] (dst[c * rows_p + r]); else a copy [rows, cols_p].
+// rows_p / cols_p % 8 == 0.  64 x 64 tiles through shared memory.
+template <bool kTranspose>
+__global__ void __launch_bounds__(kThreads)
+transpose_bf16_kernel(const __nv_bfloat16* __restrict__ src, int64_t rows, int64_t cols, int64_t spitch,
+                      __nv_bfloat16* __restrict__ dst, int64_t dpad) {
+  __shared__ __align__(16) __nv_bfloat16 tile[kTile][kTilePitch];
+  griddep_wait();
+  const int64_t r0 = (int64_t)blockIdx.x * kTile, c0 = (int64_t)blockIdx.y * kTile;
+  const __nv_bfloat16 zero = __float2bfloat16_rn(0.0f);
+  for (int i = threadIdx.x; i < kTile * kTile; i += kThreads) {  // coalesced along the source row
+    const int rl = i >> 6, cl = i & 63;
+    const int64_t r = r0 + rl, c = c0 + cl;
+    const __nv_bfloat16 v = (r < rows && c < cols) ? src[r * spitch + c] : zero;
+    if (kTranspose) tile[cl][rl] = v;
+    else tile[rl][cl] = v;
+  }
+  __syncthreads();
+  // 64 destination rows of 8 16-byte pieces
+  const int64_t d_rows = kTranspose ? cols : rows, d_cols = dpad;
+  const int64_t dr0 = kTranspose ? c0 : r0, dc0 = kTranspose ? r0 : c0;
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const int rl = (threadIdx.x >> 3) + 32 * pass, v8 = threadIdx.x & 7;
+    const int64_t r = dr0 + rl, c = dc0 + 8 * v8;
+    if (r < d_rows && c < d_cols)
+      *reinterpret_cast<uint4*>(dst + r * d_cols + c) = *reinterpret_cast<const uint4*>(&tile[rl][8 * v8]);
+  }
+}
+
+cudaLaunchConfig_t pdl_config(dim3 grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+int64_t round16(int64_t v) { return (v + 15) / 16 * 16; }
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 }  // namespace
 
@@ -78,41 +152,62 @@ cudaError_t launch_dequant_bf16(const uint8_t* codes, const uint8_t* scales_mma,
   if (R <= 0) return cudaSuccess;
   const int64_t nblk = R * (K / 16);
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)std::min<int64_t>((nblk + kThreads - 1) / kThreads, (int64_t)num_sms * 8));
-  cfg.blockDim = dim3(kThreads);
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cudaLaunchConfig_t cfg = pdl_config(
+      dim3((unsigned)std::min<int64_t>((nblk + kThreads - 1) / kThreads, (int64_t)num_sms * 8)), stream, attr);
   return cudaLaunchKernelEx(&cfg, dequant_bf16_kernel, codes, scales_mma, ts, R, K,
                             static_cast<__nv_bfloat16*>(out));
 }
 
-// Row-major operands seen by column-major cuBLAS: a row-major [r, c] matrix is
-// a column-major [c, r] one with leading dimension c.
-//   dX [M, K] = dY [M, N] W_hat [N, K]:  dX^T = W_hat^T dY^T  -> C[K, M] = A[K, N] B[N, M]
-//   dW [N, K] = dY^T [N, M] X_hat [M, K]: dW^T = X_hat^T dY   -> C[K, N] = A[K, M] B^T, B = dY^T as [N, M]
-int qat_backward_gemms(const void* dy, const void* w_hat, const void* x_hat, int64_t M, int64_t N, int64_t K,
-                       void* dx, void* dw, cudaStream_t stream) {
-  std::lock_guard<std::mutex> lk(g_blas_mu);
-  cublasHandle_t h = nullptr;
-  cublasStatus_t st = blas_handle(&h);
-  if (st != CUBLAS_STATUS_SUCCESS) return (int)st;
-  if ((st = cublasSetStream(h, stream)) != CUBLAS_STATUS_SUCCESS) return (int)st;
-  const float one = 1.0f, zero = 0.0f;
+size_t qat_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  // W_hat^T [K, Np], X_hat^T [K, Mp], dY^T [N, Mp], and a padded dY [M, Np]
+  // when its rows are not 16-byte aligned
+  const size_t Mp = (size_t)round16(M), Np = (size_t)round16(N), k = (size_t)K, m = (size_t)M;
+  return align256(k * Np * 2) + align256(k * Mp * 2) + align256((size_t)N * Mp * 2) +
+         (N % 8 != 0 ? align256(m * Np * 2) : 0);
+}
+
+cudaError_t qat_backward(const void* dy, int64_t M, const uint8_t* w_codes, const uint8_t* w_smma, const float* w_ts,
+                         int64_t N, int64_t K, const uint8_t* a_codes, const uint8_t* a_smma, const float* a_ts,
+                         void* dx, void* dw, void* workspace, unsigned int* status, cudaStream_t stream) {
+  if (M <= 0 || (dx == nullptr && dw == nullptr)) return cudaSuccess;
+  const int64_t Mp = round16(M), Np = round16(N);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto* wt = reinterpret_cast<__nv_bfloat16*>(ws);                          // W_hat^T [K, Np]
+  auto* xt = reinterpret_cast<__nv_bfloat16*>(ws + align256((size_t)K * Np * 2));  // X_hat^T [K, Mp]
+  auto* dyt = reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<uint8_t*>(xt) + align256((size_t)K * Mp * 2));
+  auto* dyp = reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<uint8_t*>(dyt) + align256((size_t)N * Mp * 2));
+  const auto* dyb = static_cast<const __nv_bfloat16*>(dy);
+  cudaLaunchAttribute attr[1];
+  cudaError_t err;
   if (dx != nullptr) {
-    st = cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_N, (int)K, (int)M, (int)N, &one, w_hat, CUDA_R_16BF, (int)K, dy,
-                      CUDA_R_16BF, (int)N, &zero, dx, CUDA_R_16BF, (int)K, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-    if (st != CUBLAS_STATUS_SUCCESS) return (int)st;
+    // dX [M, K] = dY [M, N] . W_hat^T [K, N]: reduced over N
+    cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)((N + kTile - 1) / kTile), (unsigned)((K + kTile - 1) / kTile)),
+                                        stream, attr);
+    if ((err = cudaLaunchKernelEx(&cfg, dequant_bf16_t_kernel, w_codes, w_smma, w_ts, N, K, Np, wt)) != cudaSuccess)
+      return err;
+    const __nv_bfloat16* a = dyb;
+    int64_t pitch = N;
+    if (N % 8 != 0) {  // rows of dY are not 16-byte aligned: a zero-padded copy [M, Np]
+      cfg = pdl_config(dim3((unsigned)((M + kTile - 1) / kTile), (unsigned)((N + kTile - 1) / kTile)), stream, attr);
+      if ((err = cudaLaunchKernelEx(&cfg, transpose_bf16_kernel<false>, dyb, M, N, N, dyp, Np)) != cudaSuccess)
+        return err;
+      a = dyp;
+      pitch = Np;
+    }
+    if ((err = launch_gemm_bf16_tn(a, pitch, wt, Np, M, K, N, dx, false, status, stream)) != cudaSuccess) return err;
   }
   if (dw != nullptr) {
-    st = cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_T, (int)K, (int)N, (int)M, &one, x_hat, CUDA_R_16BF, (int)K, dy,
-                      CUDA_R_16BF, (int)N, &zero, dw, CUDA_R_32F, (int)K, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-    if (st != CUBLAS_STATUS_SUCCESS) return (int)st;
+    // dW [N, K] = dY^T [N, Mp] . X_hat^T [K, Mp]: reduced over M
+    cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)((M + kTile - 1) / kTile), (unsigned)((K + kTile - 1) / kTile)),
+                                        stream, attr);
+    if ((err = cudaLaunchKernelEx(&cfg, dequant_bf16_t_kernel, a_codes, a_smma, a_ts, M, K, Mp, xt)) != cudaSuccess)
+      return err;
+    cfg = pdl_config(dim3((unsigned)((M + kTile - 1) / kTile), (unsigned)((N + kTile - 1) / kTile)), stream, attr);
+    if ((err = cudaLaunchKernelEx(&cfg, transpose_bf16_kernel<true>, dyb, M, N, N, dyt, Mp)) != cudaSuccess)
+      return err;
+    if ((err = launch_gemm_bf16_tn(dyt, Mp, xt, Mp, N, K, M, dw, true, status, stream)) != cudaSuccess) return err;
   }
-  return 0;
+  return cudaSuccess;
 }
 
 }  // namespace nvfp4

@@ -175,6 +175,18 @@ __device__ __forceinline__ void mma_mxf4nvf4_pair(uint32_t d_tmem, uint64_t ades
       : "memory");
 }
 
+// The pair form of a plain dense MMA, kind::f16 (bf16 or f16 operands from
+// shared memory, K = 16 per call, fp32 accumulator in each CTA's TMEM).
+// Issued by one thread of the even CTA.
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets lane
 // (warp's sub-partition base + i), columns [col, col + 32).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {

@@ -44,8 +44,12 @@ def test_workspace_bytes(L):
     assert nv.nvfp4_workspace_bytes(nv.OP_LINEAR_SILU_MUL, 300, 2 * 11008, 4096) == lin300 + 300 * 2 * 11008 * 4
     big = nv.nvfp4_workspace_bytes(nv.OP_LINEAR_SILU_MUL, 5000, 2 * 11008, 4096)
     assert big == nv.nvfp4_workspace_bytes(nv.OP_LINEAR, 5000, 2 * 11008, 4096) + 1024 * 2 * 11008 * 4
-    # QAT backward: bf16 W_hat [N, K] and X_hat [M, K], each 256-byte aligned
-    assert nv.nvfp4_workspace_bytes(nv.OP_QAT_BACKWARD, 37, 200, 320) == 128000 + 23808
+    # QAT backward: bf16 W_hat^T [K, Np], X_hat^T [K, Mp], dY^T [N, Mp] (rows padded to 16),
+    # each 256-byte aligned, plus a padded dY [M, Np] when N % 8 != 0
+    assert nv.nvfp4_workspace_bytes(nv.OP_QAT_BACKWARD, 37, 200, 320) == 320 * 208 * 2 + 320 * 48 * 2 + 200 * 48 * 2
+    a256 = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    assert nv.nvfp4_workspace_bytes(nv.OP_QAT_BACKWARD, 37, 201, 320) == \
+        320 * 208 * 2 + 320 * 48 * 2 + a256(201 * 48 * 2) + a256(37 * 208 * 2)
 
 
 def test_crossover_table(L):

@@ -36,10 +36,13 @@ def test_dequantize_bit_exact(shape):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("MNK", [(1, 64, 64), (37, 200, 320), (300, 512, 1024)])
+@pytest.mark.parametrize("MNK", [(1, 64, 64), (37, 200, 320), (20, 100, 192), (300, 512, 1024), (260, 520, 576)])
 def test_qat_backward(MNK):
     """dX = dY W_hat (bf16) and dW = dY^T X_hat (fp32) against the binary64
-    oracle on the same bf16 operands (GEMM tolerance: fp32 accumulation)."""
+    oracle on the same bf16 operands (GEMM tolerance: fp32 accumulation).
+    The shapes cover rows padded to 16 (M = 1, 37, 20, 260), dY rows that are
+    not 16-byte aligned (N = 100: a padded copy), more than one 256 x 256
+    output tile each way and a ragged last one."""
     M, N, K = MNK
     w = synth.weight_normal(N, K, seed=N + 3 * K, outlier_frac=0.01)
     x = synth.act_student_t(M, K, seed=M + 5)
