@@ -328,6 +328,9 @@ def run_ours(args):
         launches = 2
 
     detail = {
+        # the metric's W4A16 half on its own: the decode GEMMs' algorithmic bytes over their time
+        "w4a16_gbs": round(w16_bytes / w16_time / 1e9, 1) if w16_time > 0 else None,
+        "w4a16_frac_hbm": round(w16_bytes / w16_time / 1e9 / hbm_peak, 4) if w16_time > 0 else None,
         "quantize_fos_us": round(q_avg * 1e6, 2),
         "quantize_fos_gbs": round(q_bytes(N, K) / q_avg / 1e9, 1),
         "m4_block_fraction": round(m4_fraction, 4),
@@ -342,7 +345,12 @@ def run_ours(args):
     }
     if not args.no_prefill and rank == 0:
         # each detail runs guarded: an exception is reported in the line
-        for key, fn in (("w4a4_prefill", prefill_sweep), ("model_quantizer", model_quantizer),
+        fp4_peak = guarded(lambda nv_, dev_, stream_: fp4_peak_measured(nv_), nv, dev, stream)
+        if not isinstance(fp4_peak, dict) or "tflops" not in fp4_peak:
+            detail["fp4_peak"], fp4_peak = fp4_peak, None
+        detail["w4a4_prefill"] = guarded(lambda nv_, dev_, stream_: prefill_sweep(nv_, dev_, stream_, fp4_peak),
+                                         nv, dev, stream)
+        for key, fn in (("crossover", crossover_sweep), ("model_quantizer", model_quantizer),
                         ("act_fos", act_fos_compare), ("gate_up_silu_mul", gate_up_bench),
                         ("qat_step", qat_bench), ("gptq_fos", gptq_bench), ("mlp_decode", mlp_decode_bench)):
             detail[key] = guarded(fn, nv, dev, stream)
@@ -380,19 +388,36 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def prefill_sweep(nv, dev, stream):
-    """W4A4 GEMM TFLOPS on the prefill workload (graph of 5 launches each)."""
+def fp4_peak_measured(nv):
+    """The block-scaled FP4 MMA rate of this GPU from the library's own MMA
+    stream (nvfp4_measure_fp4_mma: one CTA pair per two SMs, operands in
+    shared memory, no memory traffic): the best of three runs after a
+    warm-up, with the clock it ran at."""
+    nv.nvfp4_measure_fp4_mma(2000)
+    runs = [nv.nvfp4_measure_fp4_mma(20000) for _ in range(3)]
+    best = max(runs, key=lambda r: r["tflops"])
+    return {"tflops": round(best["tflops"], 1), "pairs": best["pairs"], "sm_mhz": round(best["sm_mhz"]),
+            "runs_tflops": [round(r["tflops"], 1) for r in runs],
+            "source": "measured: nvfp4_measure_fp4_mma, 20000 x 4 MMAs of 256x256x64 per CTA pair, "
+                      "no memory traffic (best of 3)"}
+
+
+def prefill_sweep(nv, dev, stream, fp4_peak=None):
+    """W4A4 GEMM TFLOPS on the prefill workload (graph of 5 launches each),
+    as a fraction of the measured FP4 MMA rate (and, as context, of the
+    measured bf16 peaks times the nominal FP4 : bf16 ratio)."""
     import torch
     N, K = 11008, 4096
     wp = torch.from_numpy(synth.prefill_weight().view(np.int16)).view(torch.bfloat16).to(dev)
     qp = nv.nvfp4_quantize_fos(wp, logical_scales=False, choice=False)
     res = {}
-    for M in (1024, 4096, 16384):
+    burst, sustained, src = fp4_peaks()
+    for M in synth.PREFILL_M:
         X = torch.from_numpy(synth.prefill_act(M).view(np.int16)).view(torch.bfloat16).to(dev)
         a = nv.nvfp4_quantize_act(X)
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         torch.cuda.synchronize()  # made on the default stream, used on `stream`
-        reps = 5
+        reps = 5 if M >= 1024 else 20
         with torch.cuda.stream(stream):
             for _ in range(2):
                 nv.nvfp4_gemm_w4a4(a, qp, out=Y, stream=stream)
@@ -410,12 +435,35 @@ def prefill_sweep(nv, dev, stream):
         e1.synchronize()
         t = e0.elapsed_time(e1) * 1e-3 / reps
         tf = 2 * M * N * K / t / 1e12
-        burst, sustained, _ = fp4_peaks()
-        res[str(M)] = {"gemm_us": round(t * 1e6, 1), "tflops": round(tf, 1),
-                       "frac_fp4_burst": round(tf / burst, 3), "frac_fp4_sustained": round(tf / sustained, 3)}
-    res["fp4_peak_tflops"] = {"burst": round(fp4_peaks()[0], 1), "sustained": round(fp4_peaks()[1], 1),
-                              "source": fp4_peaks()[2]}
+        row = {"gemm_us": round(t * 1e6, 1), "tflops": round(tf, 1),
+               "frac_fp4_burst_x6": round(tf / burst, 3), "frac_fp4_sustained_x6": round(tf / sustained, 3)}
+        if fp4_peak:
+            row["frac_fp4_measured"] = round(tf / fp4_peak["tflops"], 3)
+        res[str(M)] = row
+    res["fp4_peak_tflops"] = {"measured": fp4_peak, "burst_x6": round(burst, 1), "sustained_x6": round(sustained, 1),
+                              "x6_source": src}
     return res
+
+
+def crossover_sweep(nv, dev, stream):
+    """The W4A16 / W4A4 crossover of nvfp4_linear on this GPU: both paths
+    graph-timed over M = 1 .. 256 on the decode, prefill and MLP weight
+    shapes (cold weights, weight prefetch on), the largest M where W4A16 is
+    still faster, and the built-in table's entry beside it."""
+    from nvfp4_weight_quantized_gb300 import tune
+    out = {}
+    saved = nv.nvfp4_get_weight_prefetch()
+    nv.nvfp4_set_weight_prefetch(True)
+    try:
+        for N, K in ((4096, 4096), (11008, 4096), (22016, 4096), (4096, 11008)):
+            times = tune.measure(N, K)
+            out[f"{N}x{K}"] = {
+                "measured_crossover_m": tune.crossover_from(times), "table_crossover_m": nv.nvfp4_get_crossover(N, K),
+                "us": {str(M): [round(t16 * 1e6, 2), round(t4 * 1e6, 2)] for M, (t16, t4) in sorted(times.items())},
+                "us_columns": ["w4a16", "act quant + w4a4"]}
+    finally:
+        nv.nvfp4_set_weight_prefetch(bool(saved))
+    return out
 
 
 def act_fos_compare(nv, dev, stream, M=1024):

@@ -397,6 +397,25 @@ int nvfp4_get_w4a4_cluster(void);
  * current device: NVFP4_OK, NVFP4_ERR_NONFINITE or NVFP4_ERR_TIMEOUT. */
 nvfp4_status nvfp4_get_device_status(cudaStream_t stream);
 
+/*
+ * The dense block-scaled FP4 tensor-core rate of this GPU, measured with this
+ * library's own instruction stream and no memory traffic: the denominator of
+ * the W4A4 roofline fraction (the pages give no FP4 rate; "SOAR 2026 Recap
+ * ...", section "1. Quantization and GEMM dispatch", names the NVFP4 MMA as
+ * the W4A4 engine).  Launches up to max_pairs CTA pairs (one CTA per SM);
+ * each pair issues iters x 4 tcgen05.mma.cta_group::2.kind::mxf4nvf4 of
+ * 256 x 256 x 64 (2 * 256 * 256 * 64 flops each) back to back.
+ *   iters      1 ..= 2^24
+ *   cycles     out: device array of max_pairs; cycles[p] = SM clock cycles
+ *              pair p spent issuing and completing its MMAs
+ *   pairs      out (host): how many pairs were launched (set before return)
+ * Asynchronous on `stream`: time it with events on that stream; flops =
+ * pairs * iters * 4 * 2 * 256 * 256 * 64.  NVFP4_ERR_INVALID_ARG for bad
+ * arguments, NVFP4_ERR_UNSUPPORTED if no pair fits.
+ */
+nvfp4_status nvfp4_measure_fp4_mma(int iters, unsigned long long* cycles, int max_pairs, int* pairs,
+                                    cudaStream_t stream);
+
 /* Self-test of the bounded device-side wait (the failure path of every
  * pipeline wait in the GEMM kernels): launches one thread that waits on an
  * mbarrier nothing completes.  The wait gives up after its cycle limit (about

@@ -26,7 +26,7 @@ __all__ = [
     "nvfp4_dequantize", "nvfp4_qat_backward", "nvfp4_gptq_fos", "nvfp4_set_crossover",
     "nvfp4_get_crossover", "nvfp4_set_w4a16_rf_max_m", "nvfp4_get_w4a16_rf_max_m",
     "nvfp4_set_w4a16_sk_max_m", "nvfp4_get_w4a16_sk_max_m", "nvfp4_set_weight_prefetch",
-    "nvfp4_get_weight_prefetch", "nvfp4_set_w4a4_cluster", "nvfp4_get_w4a4_cluster", "nvfp4_set_act_fos", "nvfp4_get_act_fos", "nvfp4_get_device_status",
+    "nvfp4_get_weight_prefetch", "nvfp4_set_w4a4_cluster", "nvfp4_get_w4a4_cluster", "nvfp4_set_act_fos", "nvfp4_get_act_fos", "nvfp4_get_device_status", "nvfp4_measure_fp4_mma",
     "nvfp4_selftest_wait_timeout",
     "nvfp4_status_string",
 ]
@@ -96,6 +96,7 @@ def lib() -> ctypes.CDLL:
             "nvfp4_get_w4a4_cluster": (ctypes.c_int, []),
             "nvfp4_get_device_status": (st, [vp]),
             "nvfp4_selftest_wait_timeout": (st, [vp]),
+            "nvfp4_measure_fp4_mma": (st, [ctypes.c_int, vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int), vp]),
             "nvfp4_status_string": (ctypes.c_char_p, [st]),
             "nvfp4_last_error": (ctypes.c_char_p, []),
         }
@@ -209,6 +210,28 @@ def nvfp4_selftest_wait_timeout(stream=None) -> None:
     """Launch the bounded-wait self-test (nvfp4_selftest_wait_timeout); the
     next nvfp4_get_device_status() returns ERR_TIMEOUT."""
     _check(lib().nvfp4_selftest_wait_timeout(_stream(stream)), "nvfp4_selftest_wait_timeout")
+
+
+def nvfp4_measure_fp4_mma(iters: int = 20000, stream=None) -> dict:
+    """Time the block-scaled FP4 MMA stream (nvfp4_measure_fp4_mma): one
+    CTA pair per two SMs, iters x 4 MMAs of 256 x 256 x 64 each; returns the
+    rate in TFLOP/s, the pairs launched and the median SM clock it implies."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    max_pairs = torch.cuda.get_device_properties(dev).multi_processor_count
+    cycles = torch.zeros(max_pairs, dtype=torch.int64, device=dev)
+    pairs = ctypes.c_int(0)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    _check(lib().nvfp4_measure_fp4_mma(iters, cycles.data_ptr(), max_pairs, ctypes.byref(pairs), s.cuda_stream),
+           "nvfp4_measure_fp4_mma")
+    e1.record(s)
+    e1.synchronize()
+    t = e0.elapsed_time(e1) * 1e-3
+    flops = pairs.value * iters * 4 * 2.0 * 256 * 256 * 64
+    cyc = cycles[: pairs.value].cpu().double()
+    return {"tflops": flops / t / 1e12, "pairs": pairs.value, "seconds": t,
+            "sm_mhz": float(cyc.median()) / t / 1e6 if pairs.value else 0.0}
 
 
 @dataclasses.dataclass

@@ -536,6 +536,20 @@ int64_t nvfp4_get_crossover(int64_t N, int64_t K) {
   return it == g_crossover.end() ? g_default_crossover : it->second;
 }
 
+nvfp4_status nvfp4_measure_fp4_mma(int iters, unsigned long long* cycles, int max_pairs, int* pairs,
+                                    cudaStream_t stream) {
+  if (pairs == nullptr || cycles == nullptr || iters <= 0 || iters > (1 << 24) || max_pairs <= 0)
+    return fail(NVFP4_ERR_INVALID_ARG, "measure_fp4_mma: need cycles, pairs, 0 < iters <= 2^24, max_pairs > 0");
+  *pairs = 0;
+  const DeviceInfo* d = nullptr;
+  const nvfp4_status st = device_info(&d);
+  if (st != NVFP4_OK) return st;
+  const cudaError_t err = nvfp4::launch_fp4_mma_rate(iters, cycles, max_pairs, pairs, d->status, stream);
+  if (err == cudaErrorNotSupported) return fail(NVFP4_ERR_UNSUPPORTED, "measure_fp4_mma: no CTA pair fits");
+  if (err != cudaSuccess) return fail_cuda(err, "measure_fp4_mma launch");
+  return NVFP4_OK;
+}
+
 nvfp4_status nvfp4_selftest_wait_timeout(cudaStream_t stream) {
   const DeviceInfo* d = nullptr;
   const nvfp4_status st = device_info(&d);

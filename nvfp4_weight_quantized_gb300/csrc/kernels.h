@@ -109,6 +109,12 @@ cudaError_t launch_gptq(const void* W, int64_t N, int64_t K, const float* H, flo
 bool w4a4_set_cluster_ctas(int ctas);
 int w4a4_get_cluster_ctas();
 
+// The block-scaled FP4 MMA rate (fp4_rate.cu): up to max_pairs CTA pairs,
+// one per two SMs, each issuing iters x 4 MMAs of 256 x 256 x 64; cycles[p]
+// receives pair p's clock cycles; *pairs how many ran.
+cudaError_t launch_fp4_mma_rate(int iters, unsigned long long* cycles, int max_pairs, int* pairs,
+                                unsigned int* status, cudaStream_t stream);
+
 // One thread waits on an mbarrier nothing completes; when the bounded wait
 // gives up it sets the timeout bit of `status` (selftest.cu).
 cudaError_t launch_wait_timeout_selftest(unsigned int* status, cudaStream_t stream);

@@ -251,3 +251,14 @@ def test_binding_declares_every_signature(L):
     the binding (an unset signature would pass 64-bit sizes as C ints)."""
     for n in nv.declared_functions():
         assert getattr(L, n).argtypes is not None, f"{n}: no ctypes signature in the binding"
+
+
+def test_measure_fp4_mma_argument_errors(L):
+    """nvfp4_measure_fp4_mma rejects bad arguments before touching a device."""
+    import ctypes
+    pairs = ctypes.c_int(7)
+    fn = L.nvfp4_measure_fp4_mma
+    assert fn(0, ctypes.c_void_p(16), 4, ctypes.byref(pairs), None) == nv.ERR_INVALID_ARG
+    assert fn(10, None, 4, ctypes.byref(pairs), None) == nv.ERR_INVALID_ARG
+    assert fn(10, ctypes.c_void_p(16), 0, ctypes.byref(pairs), None) == nv.ERR_INVALID_ARG
+    assert fn(10, ctypes.c_void_p(16), 4, None, None) == nv.ERR_INVALID_ARG

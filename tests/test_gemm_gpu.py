@@ -271,3 +271,13 @@ def test_w4a4_prefill_shapes():
         rows = None if M <= 256 else sample_rows(M, 64, M)
         worst = run_w4a4(x, wref, 4096, nv.OUT_BF16, m_rows=rows, n_rows=cols)
         print(f"prefill M={M}: worst normwise rel err {worst:.2e}")
+
+
+def test_fp4_mma_rate_measurement():
+    """The FP4 MMA-rate measurement behind the W4A4 roofline denominator runs
+    to completion on every CTA pair (no bounded wait runs out) and reports a
+    plausible rate and clock."""
+    r = nv.nvfp4_measure_fp4_mma(500)
+    assert nv.nvfp4_get_device_status() == nv.OK
+    assert r["pairs"] >= 1 and r["tflops"] > 0, r
+    assert 300 < r["sm_mhz"] < 3000, r
