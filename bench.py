@@ -509,8 +509,17 @@ def act_fos_compare(nv, dev, stream, M=1024):
 
     t6 = timed(lambda: nv.nvfp4_quantize_act(X, stream=stream))
     t4 = timed(lambda: nv.nvfp4_quantize_fos(X, logical_scales=False, choice=False, stream=stream))
+    # the same two quantisers as one cooperative launch each (read once, grid barrier)
+    saved = nv.nvfp4_get_single_launch_quantizer()
+    nv.nvfp4_set_single_launch_quantizer(True)
+    try:
+        t6s = timed(lambda: nv.nvfp4_quantize_act(X, stream=stream))
+        t4s = timed(lambda: nv.nvfp4_quantize_fos(X, logical_scales=False, choice=False, stream=stream))
+    finally:
+        nv.nvfp4_set_single_launch_quantizer(saved)
     return {"M": M, "rel_err_m6": round(err6, 5), "rel_err_fos": round(err4, 5), "m4_block_fraction": round(m4, 4),
             "quant_us_m6": round(t6 * 1e6, 2), "quant_us_fos": round(t4 * 1e6, 2),
+            "quant_us_m6_single_launch": round(t6s * 1e6, 2), "quant_us_fos_single_launch": round(t4s * 1e6, 2),
             "error": "||Y_w4a4 - Y_w4a16||_F / ||Y_w4a16||_F, same quantised weight"}
 
 

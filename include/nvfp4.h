@@ -40,7 +40,8 @@
  *   - The library keeps no state between calls except the crossover table
  *     (nvfp4_set_crossover), the W4A16 kernel knob
  *     (nvfp4_set_w4a16_rf_max_m, nvfp4_set_w4a16_sk_max_m), the W4A4 kernel
- *     knob (nvfp4_set_w4a4_cluster), the activation FourOverSix flag
+ *     knob (nvfp4_set_w4a4_cluster), the quantiser launch form
+ *     (nvfp4_set_single_launch_quantizer), the activation FourOverSix flag
  *     (nvfp4_set_act_fos), the weight-prefetch flag
  *     (nvfp4_set_weight_prefetch) and the device status word, besides
  *     host-side lookups made once (the driver's tensor-map encoder, per-kernel
@@ -381,6 +382,19 @@ int nvfp4_get_weight_prefetch(void);
  * Thread-safe. */
 nvfp4_status nvfp4_set_act_fos(int enable);
 int nvfp4_get_act_fos(void);
+
+/* Quantiser launch form (default off).  On: nvfp4_quantize_fos,
+ * nvfp4_quantize_act and the W4A4 branch of the linear calls run one
+ * cooperative launch per tensor -- every CTA reads its tiles once, keeping
+ * them in shared memory (up to 96 KB per CTA; the rest is read again, from
+ * L2 when it fits), a grid-wide barrier forms the tensor amax, then the
+ * tiles are quantised.  Off: two launches (an amax pass, then the
+ * quantisation pass reading the tensor again).  Both give identical bits;
+ * where no cooperative grid can be formed the two-launch form runs.  On GB300
+ * the two-launch form measured faster (the arithmetic dominates, and two
+ * launches overlap reads with it), hence the default.  Thread-safe. */
+nvfp4_status nvfp4_set_single_launch_quantizer(int enable);
+int nvfp4_get_single_launch_quantizer(void);
 
 /* W4A4 kernel for M > 128: CTAs per thread-block cluster (default 2).
  *   2: a pair of CTAs shares each 256 x 256 output tile through cta_group::2

@@ -27,6 +27,7 @@ __all__ = [
     "nvfp4_get_crossover", "nvfp4_set_w4a16_rf_max_m", "nvfp4_get_w4a16_rf_max_m",
     "nvfp4_set_w4a16_sk_max_m", "nvfp4_get_w4a16_sk_max_m", "nvfp4_set_weight_prefetch",
     "nvfp4_get_weight_prefetch", "nvfp4_set_w4a4_cluster", "nvfp4_get_w4a4_cluster", "nvfp4_set_act_fos", "nvfp4_get_act_fos", "nvfp4_get_device_status", "nvfp4_measure_fp4_mma",
+    "nvfp4_set_single_launch_quantizer", "nvfp4_get_single_launch_quantizer",
     "nvfp4_selftest_wait_timeout",
     "nvfp4_status_string",
 ]
@@ -94,6 +95,8 @@ def lib() -> ctypes.CDLL:
             "nvfp4_set_act_fos": (st, [ctypes.c_int]),
             "nvfp4_get_act_fos": (ctypes.c_int, []),
             "nvfp4_get_w4a4_cluster": (ctypes.c_int, []),
+            "nvfp4_set_single_launch_quantizer": (st, [ctypes.c_int]),
+            "nvfp4_get_single_launch_quantizer": (ctypes.c_int, []),
             "nvfp4_get_device_status": (st, [vp]),
             "nvfp4_selftest_wait_timeout": (st, [vp]),
             "nvfp4_measure_fp4_mma": (st, [ctypes.c_int, vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int), vp]),
@@ -210,6 +213,15 @@ def nvfp4_selftest_wait_timeout(stream=None) -> None:
     """Launch the bounded-wait self-test (nvfp4_selftest_wait_timeout); the
     next nvfp4_get_device_status() returns ERR_TIMEOUT."""
     _check(lib().nvfp4_selftest_wait_timeout(_stream(stream)), "nvfp4_selftest_wait_timeout")
+
+
+def nvfp4_set_single_launch_quantizer(enable: bool) -> None:
+    """One cooperative launch per quantised tensor (True) or two launches."""
+    _check(lib().nvfp4_set_single_launch_quantizer(1 if enable else 0), "nvfp4_set_single_launch_quantizer")
+
+
+def nvfp4_get_single_launch_quantizer() -> bool:
+    return bool(lib().nvfp4_get_single_launch_quantizer())
 
 
 def nvfp4_measure_fp4_mma(iters: int = 20000, stream=None) -> dict:

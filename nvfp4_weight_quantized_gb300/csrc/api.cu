@@ -523,6 +523,13 @@ nvfp4_status nvfp4_set_weight_prefetch(int enable) {
 
 int nvfp4_get_weight_prefetch(void) { return g_weight_prefetch.load(std::memory_order_relaxed) ? 1 : 0; }
 
+nvfp4_status nvfp4_set_single_launch_quantizer(int enable) {
+  nvfp4::quantize_set_single_launch(enable != 0);
+  return NVFP4_OK;
+}
+
+int nvfp4_get_single_launch_quantizer(void) { return nvfp4::quantize_get_single_launch() ? 1 : 0; }
+
 nvfp4_status nvfp4_set_act_fos(int enable) {
   g_act_fos.store(enable != 0, std::memory_order_relaxed);
   return NVFP4_OK;

@@ -14,6 +14,9 @@ namespace nvfp4 {
 constexpr int kMaxAmaxPartials = 1024;
 
 size_t quant_workspace_bytes();
+// Whether launch_quantize uses the single-launch (cooperative) quantiser.
+void quantize_set_single_launch(bool on);
+bool quantize_get_single_launch();
 
 // Records the text nvfp4_last_error() returns on this thread.
 void set_last_error(const char* what);

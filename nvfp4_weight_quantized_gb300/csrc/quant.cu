@@ -6,7 +6,9 @@
 // the smaller block MSE is kept (M=4 only when strictly smaller).  Section
 // "01 Background" gives the E2M1 grid and the M=6 normalisation to [-6, 6].
 //
-// Two launches per tensor:
+// Two launches per tensor by default (below); optionally one cooperative
+// launch (quant_fused_kernel: read once, a grid-wide barrier for the tensor
+// scale, quantise from shared memory; nvfp4_set_single_launch_quantizer):
 //   1. amax_partial_kernel: a grid-stride max of |x| over the tensor, one
 //      partial per CTA in the workspace (bf16 magnitude bits: the unsigned
 //      order of those bits is the order of the values, and Inf/NaN sort
@@ -18,6 +20,11 @@
 // Every binary32 step uses the explicit round-to-nearest intrinsics, so the
 // compiler cannot contract multiply-adds and the result is bit-identical to
 // the order of operations stated in nvfp4.h.
+#include <cooperative_groups.h>
+
+#include <algorithm>
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -220,6 +227,95 @@ __device__ __forceinline__ float cand(const f2 (&x2)[8], float bmax, float eff, 
   return __fadd_rn(c0, c1);
 }
 
+// One tile of the MMA scale layout (128 rows x 4 blocks of 16): thread i
+// quantises blocks (i/4, i%4) and (i/4 + 64, i%4) from their 16 bf16 values
+// v[h] (h = 0, 1; ok[h] false for padding), writes codes, logical scales and
+// choices, stages the tile's 512 scale bytes in `stage` and writes them with
+// one coalesced store (padding rows and columns become 0 there).  All threads
+// of the CTA call it (it synchronises the CTA when scales_mma is written).
+template <bool kFos>
+__device__ __forceinline__ void quantize_tile(const uint4 (&v)[2][2], const bool (&ok)[2], const int64_t (&rr)[2],
+                                              int64_t t, int c, int ri, int ci, int kb, float ts, bool fast6,
+                                              float inv6ts, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                              uint8_t* __restrict__ scales_mma, uint8_t* __restrict__ choice,
+                                              uint8_t* stage, uint32_t& n_m4) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t s = 0;
+    if (ok[h]) {
+      const uint32_t w[8] = {v[h][0].x, v[h][0].y, v[h][0].z, v[h][0].w,
+                             v[h][1].x, v[h][1].y, v[h][1].z, v[h][1].w};
+      f2 x2[8];  // magnitudes, elements (2j, 2j+1)
+      uint32_t m2 = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t a = w[j] & 0x7FFF7FFFu;
+        x2[j] = pk(__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u));
+        m2 = __vmaxu2(m2, a);
+      }
+      // sign bits of the 16 codes: byte j of sgn[q] gets the signs of elements
+      // 8q+2j (bit 3) and 8q+2j+1 (bit 7), i.e. bit 15 and bit 31 of word 4q+j
+      uint32_t sgn[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const uint32_t g1 = __byte_perm(__byte_perm(w[4 * q], w[4 * q + 1], 0x0051u),
+                                        __byte_perm(w[4 * q + 2], w[4 * q + 3], 0x0051u), 0x5410u);
+        const uint32_t g3 = __byte_perm(__byte_perm(w[4 * q], w[4 * q + 1], 0x0073u),
+                                        __byte_perm(w[4 * q + 2], w[4 * q + 3], 0x0073u), 0x5410u);
+        sgn[q] = ((g1 >> 4) & 0x08080808u) | (g3 & 0x80808080u);
+      }
+      const float bmax = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
+      // s6 = E4M3((amax_block / 6) / ts).  bmax * inv6ts is within 2^-21 of
+      // the twice-rounded quotient (relative; tiny quotients are far below
+      // the smallest E4M3 step either way), so the two ends of a 2^-20
+      // bracket convert to the same E4M3 code unless the quotient is within
+      // ~2^-20 of a rounding midpoint -- then it is formed as written.
+      uint32_t s6;
+      {
+        const float q = __fmul_rn(bmax, inv6ts);
+        const uint32_t c2 =
+            cvt_e4m3x2(__fmul_rn(q, 1.00000095367431640625f), __fmul_rn(q, 0.99999904632568359375f));
+        s6 = c2 & 0xFFu;
+        if (__builtin_expect(!fast6 || s6 != (c2 >> 8), 0))
+          s6 = cvt_e4m3x2(0.0f, __fdiv_rn(__fdiv_rn(bmax, 6.0f), ts)) & 0xFFu;
+      }
+      const float s6v = e4m3_to_f32(s6);
+      uint32_t cw[2];
+      const float sse6 = cand(x2, bmax, __fmul_rn(s6v, ts), cw);
+      s = s6;
+      const int64_t blk = rr[h] * kb + c;
+      if (kFos) {
+        const uint32_t s4 = cvt_e4m3x2(0.0f, __fmul_rn(s6v, 1.5f)) & 0xFFu;
+        bool m4 = false;
+        if (s4 != s6) {  // equal scales tie, and a tie keeps M=6
+          uint32_t cw4[2];
+          const float sse4 = cand(x2, bmax, __fmul_rn(e4m3_to_f32(s4), ts), cw4);
+          m4 = sse4 < sse6;
+          if (m4) {
+            cw[0] = cw4[0];
+            cw[1] = cw4[1];
+            s = s4;
+            ++n_m4;
+          }
+        }
+        if (choice != nullptr) choice[blk] = m4 ? 1 : 0;
+      }
+      *reinterpret_cast<uint2*>(codes + 8 * blk) = make_uint2(cw[0] | sgn[0], cw[1] | sgn[1]);
+      if (scales != nullptr) scales[blk] = (uint8_t)s;
+    }
+    if (scales_mma != nullptr) {
+      const int r = ri + 64 * h;  // row inside the tile
+      stage[(r & 31) * 16 + (r >> 5) * 4 + ci] = (uint8_t)s;
+    }
+  }
+  if (scales_mma != nullptr) {
+    __syncthreads();
+    if (threadIdx.x < kScaleTileBytes / 16)
+      reinterpret_cast<uint4*>(scales_mma + t * kScaleTileBytes)[threadIdx.x] =
+          reinterpret_cast<const uint4*>(stage)[threadIdx.x];
+  }
+}
+
 template <bool kFos>
 __global__ void __launch_bounds__(kThreads, 3)
 quant_kernel(const uint4* __restrict__ x, int64_t rows, int64_t K, const uint32_t* __restrict__ partial,
@@ -273,81 +369,8 @@ quant_kernel(const uint4* __restrict__ x, int64_t rows, int64_t K, const uint32_
         v[h][1] = ld_u4_policy(p + 1, pol);
       }
     }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t s = 0;
-      if (ok[h]) {
-        const uint32_t w[8] = {v[h][0].x, v[h][0].y, v[h][0].z, v[h][0].w,
-                               v[h][1].x, v[h][1].y, v[h][1].z, v[h][1].w};
-        f2 x2[8];  // magnitudes, elements (2j, 2j+1)
-        uint32_t m2 = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t a = w[j] & 0x7FFF7FFFu;
-          x2[j] = pk(__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u));
-          m2 = __vmaxu2(m2, a);
-        }
-        // sign bits of the 16 codes: byte j of sgn[q] gets the signs of elements
-        // 8q+2j (bit 3) and 8q+2j+1 (bit 7), i.e. bit 15 and bit 31 of word 4q+j
-        uint32_t sgn[2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const uint32_t g1 = __byte_perm(__byte_perm(w[4 * q], w[4 * q + 1], 0x0051u),
-                                          __byte_perm(w[4 * q + 2], w[4 * q + 3], 0x0051u), 0x5410u);
-          const uint32_t g3 = __byte_perm(__byte_perm(w[4 * q], w[4 * q + 1], 0x0073u),
-                                          __byte_perm(w[4 * q + 2], w[4 * q + 3], 0x0073u), 0x5410u);
-          sgn[q] = ((g1 >> 4) & 0x08080808u) | (g3 & 0x80808080u);
-        }
-        const float bmax = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
-        // s6 = E4M3((amax_block / 6) / ts).  bmax * inv6ts is within 2^-21 of
-        // the twice-rounded quotient (relative; tiny quotients are far below
-        // the smallest E4M3 step either way), so the two ends of a 2^-20
-        // bracket convert to the same E4M3 code unless the quotient is within
-        // ~2^-20 of a rounding midpoint -- then it is formed as written.
-        uint32_t s6;
-        {
-          const float q = __fmul_rn(bmax, inv6ts);
-          const uint32_t c2 =
-              cvt_e4m3x2(__fmul_rn(q, 1.00000095367431640625f), __fmul_rn(q, 0.99999904632568359375f));
-          s6 = c2 & 0xFFu;
-          if (__builtin_expect(!fast6 || s6 != (c2 >> 8), 0))
-            s6 = cvt_e4m3x2(0.0f, __fdiv_rn(__fdiv_rn(bmax, 6.0f), ts)) & 0xFFu;
-        }
-        const float s6v = e4m3_to_f32(s6);
-        uint32_t cw[2];
-        const float sse6 = cand(x2, bmax, __fmul_rn(s6v, ts), cw);
-        s = s6;
-        const int64_t blk = rr[h] * kb + c;
-        if (kFos) {
-          const uint32_t s4 = cvt_e4m3x2(0.0f, __fmul_rn(s6v, 1.5f)) & 0xFFu;
-          bool m4 = false;
-          if (s4 != s6) {  // equal scales tie, and a tie keeps M=6
-            uint32_t cw4[2];
-            const float sse4 = cand(x2, bmax, __fmul_rn(e4m3_to_f32(s4), ts), cw4);
-            m4 = sse4 < sse6;
-            if (m4) {
-              cw[0] = cw4[0];
-              cw[1] = cw4[1];
-              s = s4;
-              ++n_m4;
-            }
-          }
-          if (choice != nullptr) choice[blk] = m4 ? 1 : 0;
-        }
-        *reinterpret_cast<uint2*>(codes + 8 * blk) = make_uint2(cw[0] | sgn[0], cw[1] | sgn[1]);
-        if (scales != nullptr) scales[blk] = (uint8_t)s;
-      }
-      if (scales_mma != nullptr) {
-        const int r = ri + 64 * h;  // row inside the tile
-        stage[buf][(r & 31) * 16 + (r >> 5) * 4 + ci] = (uint8_t)s;
-      }
-    }
-    if (scales_mma != nullptr) {
-      __syncthreads();
-      if (threadIdx.x < kScaleTileBytes / 16)
-        reinterpret_cast<uint4*>(scales_mma + t * kScaleTileBytes)[threadIdx.x] =
-            reinterpret_cast<const uint4*>(stage[buf])[threadIdx.x];
-    }
+quantize_tile<kFos>(v, ok, rr, t, c, ri, ci, kb, ts, fast6, inv6ts, codes, scales, scales_mma, choice, stage[buf],
+                        n_m4);
   }
   griddep_launch_dependents();
   if (kFos && m4_count != nullptr) {
@@ -356,14 +379,170 @@ quant_kernel(const uint4* __restrict__ x, int64_t rows, int64_t K, const uint32_
   }
 }
 
+// The single-launch form, for a cooperative launch (every CTA resident at
+// once): each CTA reads its tiles once -- keeping the first `resident` of
+// them in shared memory -- and publishes its partial maximum; after one
+// grid-wide barrier every CTA folds the partials into the tensor scale and
+// quantises its tiles, the resident ones straight from shared memory.  Same
+// arithmetic and results as amax_partial_kernel + quant_kernel.
+template <bool kFos>
+__global__ void __launch_bounds__(kThreads, 3)
+quant_fused_kernel(const uint4* __restrict__ x, int64_t rows, int64_t K, uint32_t* __restrict__ partial,
+                   float divisor, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                   uint8_t* __restrict__ scales_mma, float* __restrict__ ts_out, uint8_t* __restrict__ choice,
+                   unsigned long long* __restrict__ m4_count, int resident, unsigned int* __restrict__ status) {
+  extern __shared__ uint4 xs[];  // [resident][2 blocks][2 pieces][kThreads]
+  __shared__ uint32_t red[kThreads / 32];
+  __shared__ __align__(16) uint8_t stage[2][kScaleTileBytes];
+  const int kb = (int)(K >> 4);
+  const int ct = (kb + 3) >> 2;
+  const int64_t ntiles = ((rows + 127) >> 7) * ct;
+  const int ri = threadIdx.x >> 2, ci = threadIdx.x & 3;
+  auto tile_at = [&](int64_t t, int& c, int64_t (&rr)[2], bool (&ok)[2]) {
+    const int64_t tr = t / ct;
+    c = (int)(t - tr * ct) * 4 + ci;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      rr[h] = tr * 128 + ri + 64 * h;
+      ok[h] = rr[h] < rows && c < kb;
+    }
+  };
+  // ---- phase 1: read every tile once, the largest |x| of this CTA's ----
+  const uint64_t keep = l2_policy_evict_last();  // tiles read again in phase 2 should hit L2
+  uint32_t m2 = 0;
+  int slot = 0;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++slot) {
+    int c;
+    int64_t rr[2];
+    bool ok[2];
+    tile_at(t, c, rr, ok);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint4 v[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+      if (ok[h]) {
+        const uint4* p = x + rr[h] * (K >> 3) + 2 * c;
+        v[0] = ld_u4_policy(p, keep);
+        v[1] = ld_u4_policy(p + 1, keep);
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          m2 = __vmaxu2(__vmaxu2(m2, v[j].x & 0x7FFF7FFFu),
+                        __vmaxu2(__vmaxu2(v[j].y & 0x7FFF7FFFu, v[j].z & 0x7FFF7FFFu), v[j].w & 0x7FFF7FFFu));
+      }
+      if (slot < resident) {
+        xs[((slot * 2 + h) * 2 + 0) * kThreads + threadIdx.x] = v[0];
+        xs[((slot * 2 + h) * 2 + 1) * kThreads + threadIdx.x] = v[1];
+      }
+    }
+  }
+  uint32_t am = block_reduce_max(max(m2 & 0xFFFFu, m2 >> 16), red);
+  if (threadIdx.x == 0) {
+    partial[blockIdx.x] = am;
+    if (kFos && m4_count != nullptr && blockIdx.x == 0) *m4_count = 0ull;
+  }
+  cooperative_groups::this_grid().sync();  // every partial is in (and m4_count cleared)
+  // ---- phase 2: the tensor scale, then the tiles ----
+  am = 0;
+  for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x) am = max(am, partial[i]);
+  am = block_reduce_max(am, red);
+  if (am >= 0x7F80u) {  // Inf or NaN somewhere in the tensor
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, kStatusNonfinite);
+    return;
+  }
+  const float amax = __uint_as_float(am << 16);
+  const float ts = amax == 0.0f ? 1.0f : __fdiv_rn(amax, divisor);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *ts_out = ts;
+  const bool fast6 = __fmul_rn(6.0f, ts) >= 0x1p-126f;
+  const float inv6ts = fast6 ? __frcp_rn(__fmul_rn(6.0f, ts)) : 0.0f;
+  const uint64_t once = l2_policy_evict_first();
+  uint32_t n_m4 = 0;
+  int buf = 0;
+  slot = 0;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++slot, buf ^= 1) {
+    int c;
+    int64_t rr[2];
+    bool ok[2];
+    tile_at(t, c, rr, ok);
+    uint4 v[2][2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (slot < resident) {
+        v[h][0] = xs[((slot * 2 + h) * 2 + 0) * kThreads + threadIdx.x];
+        v[h][1] = xs[((slot * 2 + h) * 2 + 1) * kThreads + threadIdx.x];
+      } else if (ok[h]) {
+        const uint4* p = x + rr[h] * (K >> 3) + 2 * c;
+        v[h][0] = ld_u4_policy(p, once);
+        v[h][1] = ld_u4_policy(p + 1, once);
+      }
+    }
+    quantize_tile<kFos>(v, ok, rr, t, c, ri, ci, kb, ts, fast6, inv6ts, codes, scales, scales_mma, choice, stage[buf],
+                        n_m4);
+  }
+  if (kFos && m4_count != nullptr) {
+    n_m4 = __reduce_add_sync(0xffffffffu, n_m4);
+    if ((threadIdx.x & 31) == 0 && n_m4) atomicAdd(m4_count, (unsigned long long)n_m4);
+  }
+}
+
+constexpr int kTileBytes = 2 * 2 * kThreads * 16;  // one tile's bf16 values in shared memory (16 KB)
+constexpr int kMaxResident = 4;                      // tiles per CTA kept in shared memory (64 KB)
+
+// Off by default: on GB300 the two-launch form measured faster (the
+// quantiser is arithmetic-bound, and the single launch serialises the read,
+// the grid barrier and the arithmetic that two launches overlap).
+std::atomic<bool> g_single_launch{false};
+
 }  // namespace
 
 size_t quant_workspace_bytes() { return kMaxAmaxPartials * sizeof(uint32_t); }
+
+void quantize_set_single_launch(bool on) { g_single_launch.store(on, std::memory_order_relaxed); }
+bool quantize_get_single_launch() { return g_single_launch.load(std::memory_order_relaxed); }
+
+namespace {
+
+// The single-launch quantiser: cudaErrorNotSupported when no cooperative
+// grid can be formed (the caller then uses the two-launch form).
+cudaError_t launch_quantize_fused(const void* x, int64_t rows, int64_t K, float divisor, bool fos, uint8_t* codes,
+                                  uint8_t* scales, uint8_t* scales_mma, float* ts, uint8_t* choice,
+                                  unsigned long long* m4_count, uint32_t* partial, unsigned int* status, int num_sms,
+                                  cudaStream_t stream) {
+  const int64_t ntiles = ((rows + 127) / 128) * ((K / 16 + 3) / 4);
+  int resident = (int)std::min<int64_t>(kMaxResident, (ntiles + 3 * num_sms - 1) / (3 * (int64_t)num_sms));
+  resident = std::max(resident, 1);
+  const size_t smem = (size_t)resident * kTileBytes;
+  auto kern = fos ? quant_fused_kernel<true> : quant_fused_kernel<false>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  int per_sm = 0;
+  if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem)) != cudaSuccess) return err;
+  if (per_sm < 1) return cudaErrorNotSupported;
+  const int grid = (int)std::min<int64_t>({ntiles, (int64_t)per_sm * num_sms, (int64_t)kMaxAmaxPartials});
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::max(grid, 1));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint4*>(x), rows, K, partial, divisor, codes, scales,
+                            scales_mma, ts, choice, fos ? m4_count : (unsigned long long*)nullptr, resident, status);
+}
+
+}  // namespace
 
 cudaError_t launch_quantize(const void* x, int64_t rows, int64_t K, float divisor, bool fos,
                             uint8_t* codes, uint8_t* scales, uint8_t* scales_mma, float* ts,
                             uint8_t* choice, unsigned long long* m4_count, void* workspace,
                             unsigned int* status, int num_sms, cudaStream_t stream) {
+  if (quantize_get_single_launch()) {
+    const cudaError_t err = launch_quantize_fused(x, rows, K, divisor, fos, codes, scales, scales_mma, ts, choice,
+                                                  m4_count, static_cast<uint32_t*>(workspace), status, num_sms,
+                                                  stream);
+    if (err != cudaErrorNotSupported) return err;
+  }
   const int64_t n_vec = rows * K / 8;  // 16-byte vectors of bf16
   int g1 = (int)std::min<int64_t>((n_vec + kThreads * 4 - 1) / (kThreads * 4), (int64_t)num_sms * 4);
   g1 = std::max(1, std::min(g1, kMaxAmaxPartials));

@@ -262,3 +262,11 @@ def test_measure_fp4_mma_argument_errors(L):
     assert fn(10, None, 4, ctypes.byref(pairs), None) == nv.ERR_INVALID_ARG
     assert fn(10, ctypes.c_void_p(16), 0, ctypes.byref(pairs), None) == nv.ERR_INVALID_ARG
     assert fn(10, ctypes.c_void_p(16), 4, None, None) == nv.ERR_INVALID_ARG
+
+
+def test_single_launch_quantizer_knob(L):
+    saved = nv.nvfp4_get_single_launch_quantizer()
+    for v in (False, True):
+        nv.nvfp4_set_single_launch_quantizer(v)
+        assert nv.nvfp4_get_single_launch_quantizer() == v
+    nv.nvfp4_set_single_launch_quantizer(saved)

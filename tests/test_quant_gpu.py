@@ -251,3 +251,32 @@ def test_nonfinite_input_sets_device_status():
 def test_activation_quantiser_prefill_shapes():
     for M in (64, 256, 1024):
         check_act(synth.prefill_act(M))
+
+
+@pytest.mark.parametrize("shape", [(1, 16), (129, 80), (300, 1040), (4096, 4096), (5000, 2048)])
+def test_both_launch_forms(shape):
+    """The single-launch quantiser (tiles kept in shared memory across the
+    grid-wide barrier, the rest read again) and the two-launch form (the
+    default) give the same bits, both against the oracle: small tensors, a tensor with more
+    tiles per CTA than stay resident, a ragged row count; FourOverSix and
+    activations; and the non-finite status in both."""
+    N, K = shape
+    w = synth.weight_normal(N, K, seed=N + 13 * K, outlier_frac=0.01)
+    saved = nv.nvfp4_get_single_launch_quantizer()
+    try:
+        outs = []
+        for single in (True, False):
+            nv.nvfp4_set_single_launch_quantizer(single)
+            check_fos(w)
+            if N * K <= 300 * 1040:
+                check_act(synth.act_student_t(N, K, seed=N + K))
+            q = nv.nvfp4_quantize_fos(to_dev(w))
+            outs.append([to_np_u8(t) for t in (q.codes, q.scales, q.scales_mma, q.choice)] + [q.tensor_scale.item()])
+            bad = w.copy()
+            bad[N // 2, K // 3] = 0x7FC0  # NaN
+            nv.nvfp4_quantize_fos(to_dev(bad))
+            assert nv.nvfp4_get_device_status() == nv.ERR_NONFINITE
+        for a, b in zip(outs[0], outs[1]):
+            assert np.array_equal(a, b)
+    finally:
+        nv.nvfp4_set_single_launch_quantizer(saved)
