@@ -62,7 +62,7 @@ extern "C" {
 typedef enum nvfp4_status {
   NVFP4_OK = 0,
   NVFP4_ERR_INVALID_ARG = 1, /* null pointer where one is required, bad enum */
-  NVFP4_ERR_SHAPE = 2,       /* sizes <= 0 where not allowed, K not a multiple of 16 (64 for GEMMs) */
+  NVFP4_ERR_SHAPE = 2,       /* sizes <= 0 where not allowed, K not a multiple of 16 (64 for the FP4 MMA) */
   NVFP4_ERR_ALIGN = 3,       /* a tensor pointer not 16-byte aligned */
   NVFP4_ERR_WORKSPACE = 4,   /* workspace too small */
   NVFP4_ERR_NONFINITE = 5,   /* an input held Inf or NaN (device-detected) */
@@ -195,9 +195,13 @@ nvfp4_status nvfp4_quantize_act(const void* X, int64_t M, int64_t K, float divis
  * bf16 activations, weights dequantised exactly (value(code) * value(scale)
  * has at most 6 significant bits), fp32 accumulation.
  *   X      in:  device bf16 [M, K];  M >= 0 (M == 0 launches nothing)
- *   W      in:  quantised weight; K % 64 == 0
+ *   W      in:  quantised weight; K % 16 == 0
  *   Y      out: device [M, N] of out_dtype
- * Three kernels implement it.  For small M (see
+ * For K % 64 != 0 a plain kernel runs (a warp per weight row and 8 tokens,
+ * exact binary32 dequantisation, fp32 fma accumulation per lane, a shuffle
+ * tree across lanes): the tensor-core kernels stream 64-wide chunks whose
+ * rows the TMA can only describe when K % 32 == 0.  For K % 64 == 0 three
+ * tensor-core kernels implement it.  For small M (see
  * nvfp4_set_w4a16_sk_max_m): a persistent split-K kernel (one CTA per SM; clusters of up to 8 CTAs each
  * own a run of 128-row weight tiles, CTA r of a cluster a K slice of every
  * one, the slices of a tile summed through distributed shared memory) that
@@ -224,7 +228,8 @@ nvfp4_status nvfp4_gemm_w4a16(const void* X, int64_t M, const nvfp4_weight* W, v
  *   a_scales_mma in: device, nvfp4_scales_mma_bytes(M, K) bytes
  *   a_tensor_scale in: device, 1 float
  *   M            >= 0 (M == 0 launches nothing)
- *   W            in: quantised weight; K % 64 == 0
+ *   W            in: quantised weight; K % 64 == 0 (the MMA's K step;
+ *                NVFP4_ERR_SHAPE otherwise)
  *   Y            out: device [M, N] of out_dtype
  * Above 128 tokens the kernel runs on CTA pairs (nvfp4_set_w4a4_cluster).
  * NVFP4_ERR_UNSUPPORTED if no kernel configuration fits the size.  The
@@ -239,7 +244,7 @@ nvfp4_status nvfp4_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma
  * NVFP4 linear layer with M-based dispatch (same section: small token counts
  * take W4A16, larger ones W4A4, the two latency curves crossing near M = 48
  * on the pages' GPU, and the faster path is chosen per call).  M <=
- * crossover(N, K) runs nvfp4_gemm_w4a16; otherwise
+ * crossover(N, K), K < 256 or K % 64 != 0 runs nvfp4_gemm_w4a16; otherwise
  * nvfp4_quantize_act (into the workspace) then nvfp4_gemm_w4a4 -- or, with
  * nvfp4_set_act_fos(1), the FourOverSix quantiser on the activations.
  *   workspace  nvfp4_workspace_bytes(NVFP4_OP_LINEAR, M, N, K) bytes

@@ -107,10 +107,14 @@ bool weight_ok(const nvfp4_weight* W) {
   return W != nullptr && W->codes != nullptr && W->scales_mma != nullptr && W->tensor_scale != nullptr;
 }
 
-nvfp4_status check_weight(const nvfp4_weight* W) {
+// A weight descriptor: K a multiple of 16 (one NVFP4 block); the FP4 tensor-core
+// paths (W4A4, and the QAT forward it serves) need K % 64 == 0 as well.
+nvfp4_status check_weight(const nvfp4_weight* W, int k_multiple = 16) {
   if (!weight_ok(W)) return fail(NVFP4_ERR_INVALID_ARG, "weight descriptor or one of its pointers is null");
-  if (W->N <= 0 || W->K <= 0 || W->K % 64 != 0 || W->N > kMaxElems / W->K)
-    return fail(NVFP4_ERR_SHAPE, "weight needs N >= 1, K >= 64, K % 64 == 0");
+  if (W->N <= 0 || W->K <= 0 || W->K % 16 != 0 || W->N > kMaxElems / W->K)
+    return fail(NVFP4_ERR_SHAPE, "weight needs N >= 1, K >= 16, K % 16 == 0");
+  if (W->K % k_multiple != 0)
+    return fail(NVFP4_ERR_SHAPE, "the FP4 tensor-core path needs K % 64 == 0");
   if (!aligned(W->codes, 16) || !aligned(W->scales_mma, 16) || !aligned(W->tensor_scale, 4))
     return fail(NVFP4_ERR_ALIGN, "weight pointers must be 16-byte aligned");
   return NVFP4_OK;
@@ -262,6 +266,12 @@ nvfp4_status nvfp4_gemm_w4a16(const void* X, int64_t M, const nvfp4_weight* W, v
   const DeviceInfo* d = nullptr;
   if ((st = device_info(&d)) != NVFP4_OK) return st;
   const bool f32 = out_dtype == NVFP4_OUT_F32, pf = g_weight_prefetch.load(std::memory_order_relaxed);
+  if (W->K % 64 != 0) {  // rows the 64-wide tensor-core kernels cannot stream
+    const cudaError_t e = nvfp4::launch_gemm_w4a16_any(X, M, W->codes, W->scales_mma, W->tensor_scale, W->N, W->K,
+                                                       Y, f32, d->num_sms, stream);
+    if (e != cudaSuccess) return fail_cuda(e, "gemm_w4a16 launch");
+    return NVFP4_OK;
+  }
   const int64_t sk_max = g_w4a16_sk_max_m.load(std::memory_order_relaxed);
   const int64_t rf_max = g_w4a16_rf_max_m.load(std::memory_order_relaxed);
   cudaError_t err = cudaErrorNotSupported;
@@ -293,7 +303,7 @@ nvfp4_status nvfp4_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma
                              size_t workspace_bytes, cudaStream_t stream) {
   (void)workspace;
   (void)workspace_bytes;
-  nvfp4_status st = check_weight(W);
+  nvfp4_status st = check_weight(W, 64);
   if (st != NVFP4_OK) return st;
   if ((st = check_out_dtype(out_dtype)) != NVFP4_OK) return st;
   if (M < 0 || M > kMaxElems / W->K || M > kMaxElems / W->N) return fail(NVFP4_ERR_SHAPE, "bad M");
@@ -325,15 +335,16 @@ nvfp4_status nvfp4_linear(const void* X, int64_t M, const nvfp4_weight* W, void*
 namespace nvfp4 {
 
 bool linear_takes_w4a4(int64_t M, int64_t N, int64_t K) {
-  // the tensor-core path needs at least one full 256-wide K stage
-  return !(M <= nvfp4_get_crossover(N, K) || K < 256);
+  // the tensor-core path needs at least one full 256-wide K stage and K % 64 == 0
+  return !(M <= nvfp4_get_crossover(N, K) || K < 256 || K % 64 != 0);
 }
 
 nvfp4_status linear_branch(const void* X, int64_t M, const nvfp4_weight* W, void* Y, int out_dtype,
                            void* workspace, size_t workspace_bytes, cudaStream_t stream, bool w4a4) {
   nvfp4_status st = check_weight(W);
   if (st != NVFP4_OK) return st;
-  if (!w4a4 || W->K < 256) return nvfp4_gemm_w4a16(X, M, W, Y, out_dtype, workspace, workspace_bytes, stream);
+  if (!w4a4 || W->K < 256 || W->K % 64 != 0)
+    return nvfp4_gemm_w4a16(X, M, W, Y, out_dtype, workspace, workspace_bytes, stream);
   if ((st = check_out_dtype(out_dtype)) != NVFP4_OK) return st;
   if (M > kMaxElems / W->K) return fail(NVFP4_ERR_SHAPE, "bad M");
   const LinearWs l = linear_ws_layout(M, W->K);
@@ -376,7 +387,7 @@ nvfp4_status nvfp4_linear_silu_mul(const void* X, int64_t M, const nvfp4_weight*
   const bool f32 = out_dtype == NVFP4_OUT_F32;
   const size_t out_elt = f32 ? 4 : 2;
   cudaError_t err;
-  if (M <= nvfp4_get_crossover(N, K) || K < 256) {
+  if (M <= nvfp4_get_crossover(N, K) || K < 256 || K % 64 != 0) {
     // W4A16 into fp32, then silu(G) * U
     for (int64_t r0 = 0; r0 < M; r0 += kSiluChunkRows) {
       const int64_t mc = std::min(kSiluChunkRows, M - r0);
@@ -463,7 +474,7 @@ nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales_mma, c
 nvfp4_status nvfp4_qat_backward(const void* dY, int64_t M, const nvfp4_weight* W, const uint8_t* a_codes,
                                 const uint8_t* a_scales_mma, const float* a_tensor_scale, void* dX, void* dW,
                                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  nvfp4_status st = check_weight(W);
+  nvfp4_status st = check_weight(W, 64);
   if (st != NVFP4_OK) return st;
   const int64_t N = W->N, K = W->K;
   if (M < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX || M > kMaxElems / K || M > kMaxElems / N)

@@ -61,6 +61,12 @@ cudaError_t launch_gemm_w4a16_sk(const void* x, int64_t M, const uint8_t* codes,
                                  void* y, bool out_f32, bool prefetch_w, unsigned int* status,
                                  int num_sms, cudaStream_t stream);
 
+// W4A16 for K % 16 == 0 with K % 64 != 0 (plain loads, CUDA-core fp32
+// accumulation; the tensor-core kernels need 64-wide chunks).
+cudaError_t launch_gemm_w4a16_any(const void* x, int64_t M, const uint8_t* codes, const uint8_t* scales_mma,
+                                  const float* ts, int64_t N, int64_t K, void* y, bool out_f32, int num_sms,
+                                  cudaStream_t stream);
+
 // W4A4: block-scaled FP4 tensor-core GEMM.
 cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma, const float* a_ts,
                              int64_t M, const uint8_t* w_codes, const uint8_t* w_scales_mma,

@@ -149,7 +149,7 @@ def test_gemm_argument_errors(L):
     g16 = L.nvfp4_gemm_w4a16
     assert g16(FAKE, 4, None, FAKE, 0, None, 0, None) == nv.ERR_INVALID_ARG
     assert g16(FAKE, 4, ctypes.byref(_w(codes=None)), FAKE, 0, None, 0, None) == nv.ERR_INVALID_ARG
-    assert g16(FAKE, 4, ctypes.byref(_w(K=48)), FAKE, 0, None, 0, None) == nv.ERR_SHAPE
+    assert g16(FAKE, 4, ctypes.byref(_w(K=40)), FAKE, 0, None, 0, None) == nv.ERR_SHAPE  # K % 16
     assert g16(FAKE, 4, ctypes.byref(_w(N=0)), FAKE, 0, None, 0, None) == nv.ERR_SHAPE
     assert g16(FAKE, 4, ctypes.byref(_w(codes=FAKE + 1)), FAKE, 0, None, 0, None) == nv.ERR_ALIGN
     assert g16(FAKE, -1, ctypes.byref(_w()), FAKE, 0, None, 0, None) == nv.ERR_SHAPE
@@ -162,6 +162,8 @@ def test_gemm_argument_errors(L):
     assert g4(None, FAKE, FAKE, 4, ctypes.byref(_w()), FAKE, 0, None, 0, None) == nv.ERR_INVALID_ARG
     assert g4(FAKE, FAKE, FAKE + 2, 4, ctypes.byref(_w()), FAKE, 0, None, 0, None) == nv.ERR_ALIGN
     assert g4(FAKE, FAKE, FAKE, 0, ctypes.byref(_w()), None, 0, None, 0, None) == nv.OK
+    # the FP4 MMA's K step: W4A16 takes K = 48, W4A4 does not
+    assert g4(FAKE, FAKE, FAKE, 4, ctypes.byref(_w(K=48)), FAKE, 0, None, 0, None) == nv.ERR_SHAPE
 
 
 def test_linear_workspace_errors(L):
@@ -236,7 +238,7 @@ def test_noalloc_argument_paths(L):
     call (no GPU here)."""
     na = L.nvfp4_linear_noalloc
     assert na(FAKE, 4, None, FAKE, 0, None) == nv.ERR_INVALID_ARG
-    assert na(FAKE, 4, ctypes.byref(_w(K=48)), FAKE, 0, None) == nv.ERR_SHAPE
+    assert na(FAKE, 4, ctypes.byref(_w(K=40)), FAKE, 0, None) == nv.ERR_SHAPE
     assert na(FAKE, -2, ctypes.byref(_w()), FAKE, 0, None) == nv.ERR_SHAPE
     assert na(None, 0, ctypes.byref(_w()), None, 0, None) == nv.OK
     big = _w(N=256, K=4096)

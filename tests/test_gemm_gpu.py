@@ -281,3 +281,21 @@ def test_fp4_mma_rate_measurement():
     assert nv.nvfp4_get_device_status() == nv.OK
     assert r["pairs"] >= 1 and r["tflops"] > 0, r
     assert 300 < r["sm_mhz"] < 3000, r
+
+
+@pytest.mark.parametrize("shape", [(200, 16), (64, 48), (130, 80), (257, 1040), (96, 16 * 129)])
+@pytest.mark.parametrize("M", [1, 7, 9, 64])
+def test_w4a16_k_multiple_of_16(shape, M):
+    """Weights whose K is a multiple of 16 but not of 64 (K = 16 x odd
+    included, rows of 8 x odd code bytes): W4A16 through the plain kernel,
+    both output types, against the oracle; the linear call takes W4A16 for
+    them at any M."""
+    N, K = shape
+    wref = oracle_weight(synth.weight_normal(N, K, seed=N + 5 * K, outlier_frac=0.01))
+    x = synth.act_normal(M, K, seed=70 + M)
+    run_w4a16(x, wref, K, nv.OUT_F32)
+    run_w4a16(x, wref, K, nv.OUT_BF16)
+    W = dev_weight(wref, K)
+    y = nv.nvfp4_linear(to_dev(x), W, nv.OUT_F32)
+    assert torch.equal(y, nv.nvfp4_gemm_w4a16(to_dev(x), W, nv.OUT_F32))
+    assert nv.nvfp4_get_device_status() == 0
