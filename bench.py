@@ -1,18 +1,19 @@
 """Benchmark of the NVFP4 linear-layer path on GB300.
 
-One step = one pass of the whole hot path over the decode-shaped workload
-(weight [4096, 4096] bf16, N(0, 0.02^2) with 0.5% outliers x8; activations
-[M, 4096] bf16 N(0, 1) for M in 1, 2, 4, 8, 16, 32, 48):
-  1. FourOverSix quantisation of the bf16 weight (tensor amax + per-block
-     M=4/M=6 selection, codes + MMA-tiled scales),
-  2. nvfp4_linear for every M, which dispatches on the measured crossover to
-     the W4A16 GEMM or to activation quantisation + the W4A4 tensor-core GEMM.
-value = algorithmic bytes of the step / step time (GB/s).  Every kernel reads
-cold data: weights rotate through buffers totalling several times the L2.
-The step is captured in a CUDA graph; kernels are timed with CUDA events on
-the launching stream.  The W4A4 throughput on the prefill workload
-(activations [M, 4096] 0.5*Student-t(4), weight [11008, 4096]) is reported
-alongside.
+One step = nvfp4_linear at every decode M (1, 2, 4, 8, 16, 32, 48) on the
+decode-shaped weight [4096, 4096] (bf16 N(0, 0.02^2) with 0.5% outliers x8,
+FourOverSix-quantised once beforehand; activations [M, 4096] bf16 N(0, 1)).
+At these M the dispatch takes the W4A16 GEMM, so value = the W4A16 GEMMs'
+algorithmic bytes / step time (GB/s).  Each call reads a weight no recent call
+touched: quantised copies rotate through buffers totalling several times the
+L2.  The step is captured in a CUDA graph; kernels are timed with CUDA events
+on the launching stream.
+
+Reported alongside: the whole path per step (FourOverSix quantisation of the
+bf16 weight followed by the same linears), the quantiser alone, the W4A4
+throughput on the prefill workload (activations [M, 4096] 0.5*Student-t(4),
+weight [11008, 4096]) against the FP4 MMA rate measured in the same run, the
+W4A16/W4A4 crossover sweep and the other library calls.
 
 --impl reference times the CPU oracle (test infrastructure) on a bounded
 sample of the same workload.
@@ -39,8 +40,8 @@ import synth  # noqa: E402
 N_DEC = K_DEC = 4096
 DECODE_M = synth.DECODE_M
 METRIC = "NVFP4 linear: W4A16 GB/s (M<=48), W4A4 TFLOPS (M>48), % of roofline"
-WORKLOAD = "decode-shaped NVFP4 linear: W[4096,4096] bf16 N(0,0.02^2) 0.5% outliers x8; " \
-           "FourOverSix quantise + linear at M in {1,2,4,8,16,32,48}"
+WORKLOAD = "decode-shaped NVFP4 linear: W[4096,4096] bf16 N(0,0.02^2) 0.5% outliers x8, " \
+           "FourOverSix-quantised once; linear (W4A16) at M in {1,2,4,8,16,32,48}"
 ROT_SLOTS = 64           # quantised-weight slots (9.4 MB each)
 ROT_W = 12               # bf16 weight copies (32 MB each)
 
@@ -212,16 +213,19 @@ def run_ours(args):
     Ys = {M: torch.empty((M, N), dtype=torch.bfloat16, device=dev) for M in DECODE_M}
     lws = {M: torch.empty(max(nv.nvfp4_workspace_bytes(nv.OP_LINEAR, M, N, K), 256), dtype=torch.uint8,
                           device=dev) for M in DECODE_M}
-    # weights are quantised once per slot and only read by the GEMMs of a
-    # step (the quantiser of a step writes a slot no GEMM of that step reads),
-    # so the GEMMs may start streaming them before the previous kernel ends
+    # weights are quantised once per slot and only read by the GEMMs (the
+    # quantiser of the whole-path step writes slots no GEMM of that step
+    # reads), so the GEMMs may start streaming them before the previous
+    # kernel ends
     nv.nvfp4_set_weight_prefetch(True)
     cross = nv.nvfp4_get_crossover(N, K)
     paths = {M: ("w4a16" if M <= cross else "w4a4") for M in DECODE_M}
-    launches_per_step = 2 + sum(1 if paths[M] == "w4a16" else 3 for M in DECODE_M)
+    launches_per_step = sum(1 if paths[M] == "w4a16" else 3 for M in DECODE_M)
 
     stream = torch.cuda.Stream(device=dev)
-    steps_per_cycle = ROT_SLOTS // (len(DECODE_M) + 1)  # 8: slot rotation period
+    nm = len(DECODE_M)
+    steps_per_cycle = ROT_SLOTS // nm            # 9: slot rotation period of the step
+    full_per_cycle = ROT_SLOTS // (nm + 1)       # 8: the same for the whole-path step
 
     def quant_into(slot, src):
         d = slot
@@ -234,7 +238,14 @@ def run_ours(args):
         nv.nvfp4_linear(Xs[M], slot, out=Ys[M], workspace=lws[M], stream=stream)
 
     def step_ops(s):
-        base = (s % steps_per_cycle) * (len(DECODE_M) + 1)
+        """The timed step: every decode M on its own cold quantised weight."""
+        base = (s % steps_per_cycle) * nm
+        for j, M in enumerate(DECODE_M):
+            linear(M, slots[base + j])
+
+    def full_step_ops(s):
+        """The whole path: quantise a bf16 weight, then the same linears."""
+        base = (s % full_per_cycle) * (nm + 1)
         quant_into(slots[base], Ws[s % ROT_W])
         for j, M in enumerate(DECODE_M):
             linear(M, slots[base + 1 + j])
@@ -248,11 +259,19 @@ def run_ours(args):
     W_steps = max(args.warmup, 3)
     K_steps = args.steps
     with torch.cuda.stream(stream):
-        for s in range(steps_per_cycle):  # eager warm-up (also sets kernel attributes)
+        for s in range(full_per_cycle):  # eager warm-up (also sets kernel attributes)
+            full_step_ops(s)
+        for s in range(steps_per_cycle):
             step_ops(s)
     stream.synchronize()
-    # one graph per position in the slot-rotation cycle
+    # one graph per position in the slot-rotation cycle, and one graph of a
+    # whole cycle (steps_per_cycle consecutive steps, every slot read once)
+    # starting at the position the timed region starts at: the timed steps
+    # replay whole cycles, then single steps for the remainder
     graphs = [capture(lambda s=s: step_ops(s)) for s in range(steps_per_cycle)]
+    p0 = W_steps % steps_per_cycle
+    cycle_graph = capture(lambda: [step_ops(p0 + j) for j in range(steps_per_cycle)])
+    full_graphs = [capture(lambda s=s: full_step_ops(s)) for s in range(full_per_cycle)]
     # per-kernel graphs (for per-kernel durations): 4 graphs of 16 calls over
     # disjoint slot sets, replayed in turn, so every call reads weights no
     # other call of the last ~600 MB touched (cold, larger than L2)
@@ -277,6 +296,7 @@ def run_ours(args):
         return e0.elapsed_time(e1) * 1e-3 / len(gs)
 
     with torch.cuda.stream(stream):
+        cycle_graph.replay()  # set-up: the first replay of a graph uploads it
         for s in range(W_steps):
             graphs[s % steps_per_cycle].replay()
     torch.cuda.synchronize()
@@ -290,12 +310,17 @@ def run_ours(args):
     t_end = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         t_start.record(stream)
-        for s in range(W_steps, W_steps + K_steps):
+        s = W_steps
+        while s + steps_per_cycle <= W_steps + K_steps:
+            cycle_graph.replay()
+            s += steps_per_cycle
+        for s in range(s, W_steps + K_steps):
             graphs[s % steps_per_cycle].replay()
         t_end.record(stream)
     t_end.synchronize()
-    # per-kernel durations, still inside the sampled window
+    # per-kernel durations and the whole-path step, still inside the sampled window
     q_avg = statistics.median(timed(g_quant) for _ in range(3)) / reps
+    full_s = statistics.median(timed(full_graphs) for _ in range(3))
     lin_avg = {M: statistics.median(timed(g_lin[M]) for _ in range(3)) / reps for M in DECODE_M}
     torch.cuda.synchronize()
     if world > 1:
@@ -303,44 +328,48 @@ def run_ours(args):
     clocks = sampler.stop()
     elapsed = max_over_ranks(t_start.elapsed_time(t_end) * 1e-3, dev)
 
-    step_bytes = q_bytes(N, K) + sum(
-        w4a16_bytes(M, N, K) if paths[M] == "w4a16" else actq_bytes(M, K) + w4a4_bytes(M, N, K)
-        for M in DECODE_M)
+    lin_bytes = {M: w4a16_bytes(M, N, K) if paths[M] == "w4a16" else actq_bytes(M, K) + w4a4_bytes(M, N, K)
+                 for M in DECODE_M}
+    step_bytes = sum(lin_bytes.values())
     ms_per_step = elapsed / K_steps * 1e3
     value = replica_value(step_bytes, K_steps, world, elapsed)
 
-    # dominant kernel family of the step
+    # dominant kernel family of the step: the W4A16 GEMM (every M of the step
+    # takes it while the crossover is above 48)
     w16_time = sum(lin_avg[M] for M in DECODE_M if paths[M] == "w4a16")
     w16_bytes = sum(w4a16_bytes(M, N, K) for M in DECODE_M if paths[M] == "w4a16")
-    if w16_time >= q_avg and w16_time > 0:
+    csrc = os.path.join(ROOT, "nvfp4_weight_quantized_gb300", "csrc")
+    if w16_time > 0:
         dom = "gemm_w4a16 (w4a16_sk_kernel for M <= 8, w4a16_rf_kernel above)"
         achieved = w16_bytes / w16_time / 1e9
-        csrc = os.path.join(ROOT, "nvfp4_weight_quantized_gb300", "csrc")
         # DRAM bytes per launch, averaged over the decode M sweep
         traffic = traffic_from_profiles("w4a16_decode", {"sk": os.path.join(csrc, "gemm_w4a16_sk.cu"),
-                                                         "rf": os.path.join(csrc, "gemm_w4a16_rf.cu")})
+                                                         "rf": os.path.join(csrc, "gemm_w4a16_rf.cu"),
+                                                         "frag": os.path.join(csrc, "w4a16_frag.cuh")})
         launches = sum(1 for M in DECODE_M if paths[M] == "w4a16")
     else:
-        dom = "quantize_fos"
-        achieved = q_bytes(N, K) / q_avg / 1e9
-        traffic = traffic_from_profiles("quantize_fos_decode", {"quant": os.path.join(
-            ROOT, "nvfp4_weight_quantized_gb300", "csrc", "quant.cu")})
-        launches = 2
+        dom = "gemm_w4a4 (activation quantisation + w4a4 kernels)"
+        achieved = step_bytes / sum(lin_avg.values()) / 1e9
+        traffic = None
+        launches = launches_per_step
 
+    full_bytes = q_bytes(N, K) + step_bytes
     detail = {
-        # the metric's W4A16 half on its own: the decode GEMMs' algorithmic bytes over their time
+        # the W4A16 calls on their own: algorithmic bytes over the summed per-call times
         "w4a16_gbs": round(w16_bytes / w16_time / 1e9, 1) if w16_time > 0 else None,
         "w4a16_frac_hbm": round(w16_bytes / w16_time / 1e9 / hbm_peak, 4) if w16_time > 0 else None,
+        # the whole path per step: FourOverSix quantisation of the bf16 weight + the same linears
+        "full_step": {"ms_per_step": round(full_s * 1e3, 5), "gbs": round(full_bytes / full_s / 1e9, 1),
+                      "bytes_per_step": full_bytes, "launches_per_step": launches_per_step + 2,
+                      "timing": f"{full_per_cycle} CUDA graphs (one per slot-rotation position), "
+                                "replayed once warm then timed, median of 3"},
         "quantize_fos_us": round(q_avg * 1e6, 2),
         "quantize_fos_gbs": round(q_bytes(N, K) / q_avg / 1e9, 1),
         "m4_block_fraction": round(m4_fraction, 4),
         "crossover_m": cross,
         "linear": {str(M): {"path": paths[M], "us": round(lin_avg[M] * 1e6, 2),
-                            "gbs": round((w4a16_bytes(M, N, K) if paths[M] == "w4a16" else
-                                          actq_bytes(M, K) + w4a4_bytes(M, N, K)) / lin_avg[M] / 1e9, 1),
-                            "frac_hbm": round((w4a16_bytes(M, N, K) if paths[M] == "w4a16" else
-                                               actq_bytes(M, K) + w4a4_bytes(M, N, K)) / lin_avg[M] / 1e9
-                                              / hbm_peak, 3)}
+                            "gbs": round(lin_bytes[M] / lin_avg[M] / 1e9, 1),
+                            "frac_hbm": round(lin_bytes[M] / lin_avg[M] / 1e9 / hbm_peak, 3)}
                    for M in DECODE_M},
     }
     if not args.no_prefill and rank == 0:
@@ -355,7 +384,7 @@ def run_ours(args):
                         ("qat_step", qat_bench), ("gptq_fos", gptq_bench), ("mlp_decode", mlp_decode_bench)):
             detail[key] = guarded(fn, nv, dev, stream)
 
-    e2e = measure_e2e(nv, dev, stream, w_bits, args, step_bytes, paths) if rank == 0 else None
+    e2e = measure_e2e(nv, dev, stream, q0, args, step_bytes) if rank == 0 else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -368,9 +397,11 @@ def run_ours(args):
         "data": "synthetic (seeded numpy PCG64), stands in for real model weights and prompts",
         "config": {"workload": WORKLOAD, "N": N, "K": K, "M": list(DECODE_M),
                    "parallelism": f"replicas x{world} (no collective)",
-                   "l2": f"inputs larger than L2: {ROT_W} bf16 weight copies and {ROT_SLOTS} quantised "
-                         f"weight slots rotate (about {(ROT_W * N * K * 2 + ROT_SLOTS * 9437184) / 1e9:.2f} GB)",
-                   "timing": "CUDA graph per step, CUDA events on the launching stream around the replays; "
+                   "l2": f"inputs larger than L2: {ROT_SLOTS} quantised weight slots rotate, "
+                         f"{nm * steps_per_cycle} of them in the step (about "
+                         f"{nm * steps_per_cycle * 9437184 / 1e9:.2f} GB)",
+                   "timing": f"CUDA graphs of {steps_per_cycle} steps (then of one step for the remainder), "
+                             "CUDA events on the launching stream around the replays; "
                   "per-kernel durations from 4 graphs x 16 calls over disjoint cold weight slots"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
@@ -819,46 +850,61 @@ def model_quantizer(nv, dev, stream, layers=32, distinct=2):
             "inputs": f"{distinct} distinct layers generated on the device (torch, seeded), reused in turn"}
 
 
-def measure_e2e(nv, dev, stream, w_bits, args, step_bytes, paths):
-    """Same step through the public API with host buffers: pinned host ->
-    device copies of the weight and activations, the calls, device -> host
-    copies of the quantised weight and every output, all inside the timed
-    region."""
+def measure_e2e(nv, dev, stream, q, args, step_bytes):
+    """The same step through the public API with host buffers: every step
+    copies each linear's quantised weight (codes, MMA-tiled scales, tensor
+    scale; one weight per M, as in the device-resident step) and its
+    activations from pinned host memory, runs nvfp4_linear, and copies every
+    output back, all inside the timed region.  The inputs of a step sit in one
+    pinned buffer (and one device buffer of the same layout), so a step is one
+    host-to-device copy, the calls, and one device-to-host copy."""
     import torch
     N, K = N_DEC, K_DEC
-    # this step quantises the weight and then runs the GEMMs on it: the GEMMs
-    # must not read it before the quantiser has finished
+    # the copy of a step writes the weights its GEMMs read: no GEMM may start
+    # streaming its weight before the kernel ahead of it has finished
     nv.nvfp4_set_weight_prefetch(False)
-    hW = torch.from_numpy(w_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hX = {M: torch.from_numpy(synth.decode_act(M).view(np.int16)).view(torch.bfloat16).pin_memory()
-          for M in DECODE_M}
-    dW = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
-    dX = {M: torch.empty((M, K), dtype=torch.bfloat16, device=dev) for M in DECODE_M}
-    q = nv.nvfp4_quantize_fos(dW.copy_(hW), logical_scales=False, choice=False)
-    hQc = torch.empty(q.codes.shape, dtype=torch.uint8).pin_memory()
-    hQs = torch.empty(q.scales_mma.shape, dtype=torch.uint8).pin_memory()
-    hY = {M: torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for M in DECODE_M}
-    Y = {M: torch.empty((M, N), dtype=torch.bfloat16, device=dev) for M in DECODE_M}
-    ws = torch.empty(nv.nvfp4_workspace_bytes(nv.OP_QUANTIZE_FOS, 0, N, K), dtype=torch.uint8, device=dev)
+    align = lambda n: (n + 1023) // 1024 * 1024  # noqa: E731
+    parts = [q.codes, q.scales_mma, q.tensor_scale]
+    seg_w = [align(t.numel() * t.element_size()) for t in parts]
+    offs, o = {}, 0
+    for M in DECODE_M:
+        offs[M] = o
+        o += sum(seg_w) + align(M * K * 2)
+    h_in = torch.empty(o, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(o, dtype=torch.uint8, device=dev)
+    y_off, yo = {}, 0
+    for M in DECODE_M:
+        y_off[M] = yo
+        yo += M * N * 2
+    h_out = torch.empty(yo, dtype=torch.uint8).pin_memory()
+    d_out = torch.empty(yo, dtype=torch.uint8, device=dev)
+
+    def view(buf, off, t):
+        n = t.numel() * t.element_size()
+        return buf[off:off + n].view(t.dtype).view(t.shape)
+
+    w, X, Y = {}, {}, {}
+    for M in DECODE_M:
+        o = offs[M]
+        views = []
+        for t, n in zip(parts, seg_w):
+            view(h_in, o, t).copy_(t.cpu())
+            views.append(view(d_in, o, t))
+            o += n
+        w[M] = nv.NVFP4Weight(views[0], views[1], views[2], N, K)
+        xh = torch.from_numpy(synth.decode_act(M).view(np.int16)).view(torch.bfloat16)
+        view(h_in, o, xh).copy_(xh)
+        X[M] = view(d_in, o, xh)
+        Y[M] = d_out[y_off[M]:y_off[M] + M * N * 2].view(torch.bfloat16).view(M, N)
     lws = {M: torch.empty(max(nv.nvfp4_workspace_bytes(nv.OP_LINEAR, M, N, K), 256), dtype=torch.uint8,
                           device=dev) for M in DECODE_M}
-    h2d = hW.numel() * 2 + sum(hX[M].numel() * 2 for M in DECODE_M)
-    d2h = hQc.numel() + hQs.numel() + sum(hY[M].numel() * 2 for M in DECODE_M)
+    h2d, d2h = h_in.numel(), h_out.numel()
 
     def step():
-        dW.copy_(hW, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
         for M in DECODE_M:
-            dX[M].copy_(hX[M], non_blocking=True)
-        st = nv.lib().nvfp4_quantize_fos(dW.data_ptr(), N, K, 0.0, q.codes.data_ptr(), None,
-                                         q.scales_mma.data_ptr(), q.tensor_scale.data_ptr(), None, None,
-                                         ws.data_ptr(), ws.numel(), stream.cuda_stream)
-        assert st == 0
-        for M in DECODE_M:
-            nv.nvfp4_linear(dX[M], q, out=Y[M], workspace=lws[M], stream=stream)
-        hQc.copy_(q.codes, non_blocking=True)
-        hQs.copy_(q.scales_mma, non_blocking=True)
-        for M in DECODE_M:
-            hY[M].copy_(Y[M], non_blocking=True)
+            nv.nvfp4_linear(X[M], w[M], out=Y[M], workspace=lws[M], stream=stream)
+        h_out.copy_(d_out, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 3)):
@@ -878,52 +924,58 @@ def measure_e2e(nv, dev, stream, w_bits, args, step_bytes, paths):
 
 # ------------------------------------------------------------ CPU oracle ---
 
-def cpu_sample(sample_rows: int, threads: int = 1):
-    """One bounded oracle pass over `sample_rows` weight rows of the decode
-    workload: quantise those rows (tensor scale from the whole tensor) and
-    compute those output columns of every linear, the rows split over
-    `threads` threads (independent oracle calls; each releases the GIL).
-    Returns (seconds, bytes)."""
-    import concurrent.futures as cf
+def cpu_prepare(sample_rows: int):
+    """The oracle's inputs for a sample of the decode workload: the first
+    `sample_rows` weight rows FourOverSix-quantised (tensor scale from the
+    whole tensor; done once, like the weight of the timed step) and the
+    activations of every M."""
     import oracle
     w = synth.decode_weight()
     ts = oracle.tensor_scale(w)
-    rows = w[:sample_rows]
-    xs = {M: synth.decode_act(M) for M in DECODE_M}
-    bounds = np.linspace(0, sample_rows, threads + 1).astype(int)
+    q = oracle.quantize_rows(w[:sample_rows], ts, True)
+    return {"rows": sample_rows, "ts": ts, "q": q, "xs": {M: synth.decode_act(M) for M in DECODE_M}}
 
-    def gemms(q, i):
+
+def cpu_step(prep: dict, threads: int = 1):
+    """One bounded oracle pass over a prepared sample: those output columns
+    of every linear (binary64 reference GEMM), the rows split over `threads`
+    threads (independent oracle calls; each releases the GIL).  Returns
+    (seconds, algorithmic bytes of the sampled share of the step)."""
+    import concurrent.futures as cf
+    import oracle
+    rows, q, xs, ts = prep["rows"], prep["q"], prep["xs"], prep["ts"]
+    bounds = np.linspace(0, rows, threads + 1).astype(int)
+
+    def gemms(i):
         a, b = int(bounds[i]), int(bounds[i + 1])
         for M in DECODE_M if a < b else ():
             oracle.gemm_w4a16(xs[M], q["codes"][a:b], q["scales"][a:b], ts)
 
     t0 = time.perf_counter()
-    q = oracle.quantize_rows(rows, ts, True, threads=threads)
     if threads == 1:
-        gemms(q, 0)
+        gemms(0)
     else:
         with cf.ThreadPoolExecutor(threads) as ex:
-            list(ex.map(lambda i: gemms(q, i), range(threads)))
+            list(ex.map(gemms, range(threads)))
     dt = time.perf_counter() - t0
-    frac = sample_rows / N_DEC
-    nbytes = q_bytes(N_DEC, K_DEC) * frac + sum(w4a16_bytes(M, N_DEC, K_DEC) * frac for M in DECODE_M)
-    return dt, nbytes
+    frac = rows / N_DEC
+    return dt, sum(w4a16_bytes(M, N_DEC, K_DEC) * frac for M in DECODE_M)
 
 
 def host_cores() -> int:
     return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
 
 
-def cpu_baseline(sample_rows: int = 512):
+def cpu_baseline(sample_rows: int = 1024):
     """The oracle on the host: single thread on a sample of the step (the
     reported figure), and, beside it, the whole step split over every core."""
-    dt, nbytes = cpu_sample(sample_rows)
+    dt, nbytes = cpu_step(cpu_prepare(sample_rows))
     out = {"value": round(nbytes / dt / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-           "sample": f"{sample_rows} of 4096 weight rows: quantise those rows and compute those output "
+           "sample": f"{sample_rows} of 4096 weight rows (quantised once beforehand): those output "
                      f"columns for every M (binary64 reference GEMM), single thread, {dt:.1f} s"}
     cores = host_cores()
     if cores > 1:
-        dt_all, nb_all = cpu_sample(N_DEC, threads=cores)
+        dt_all, nb_all = cpu_step(cpu_prepare(N_DEC), threads=cores)
         out["all_cores"] = {"value": round(nb_all / dt_all / 1e9, 6), "unit": "GB/s", "cores": cores,
                             "sample": f"the whole step (4096 weight rows) split by weight row over {cores} "
                                       f"threads, {dt_all:.1f} s"}
@@ -935,19 +987,21 @@ def run_reference(args):
     if rank != 0:
         return
     rows = args.cpu_rows_reference
+    prep = cpu_prepare(rows)
     for _ in range(args.warmup):
-        cpu_sample(rows)
+        cpu_step(prep)
     times, nbytes = [], 0
     for _ in range(args.steps):
-        dt, nbytes = cpu_sample(rows)
+        dt, nbytes = cpu_step(prep)
         times.append(dt)
     t = sum(times)
     value = nbytes * args.steps / t / 1e9
-    sample = f"{rows} of 4096 weight rows per step (quantise + every M of the binary64 GEMM), single thread"
+    sample = f"{rows} of 4096 weight rows per step (quantised once beforehand; every M of the binary64 GEMM), " \
+             "single thread"
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 quantiser, f64 GEMM",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": WORKLOAD, "N": N_DEC, "K": K_DEC, "M": list(DECODE_M)},
         "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
@@ -974,9 +1028,21 @@ def profile_case(which: str, m_decode: int):
         qp = nv.nvfp4_quantize_fos(bf(synth.prefill_weight()), logical_scales=False, choice=False)
         a = nv.nvfp4_quantize_act(bf(synth.prefill_act(2048)))
         nv.nvfp4_gemm_w4a4(a, qp)
-    if which == "gate_up":  # the gated MLP projection, fused form, on the config-3 gate/up weight
+    if which == "gate_up":  # the gated MLP projection, fused form, on the gate/up weight [2 x 11008, 4096]
         qg = nv.nvfp4_quantize_fos(bf(synth.mlp_weights()[0]), logical_scales=False, choice=False)
         nv.nvfp4_linear_silu_mul(bf(synth.prefill_act(2048)), qg)
+    if which == "qat":  # straight-through backward on the prefill weight [11008, 4096], M = 2048
+        qp = nv.nvfp4_quantize_fos(bf(synth.prefill_weight()), logical_scales=False, choice=False)
+        a = nv.nvfp4_quantize_act(bf(synth.prefill_act(2048)))
+        g = torch.Generator(device=dev).manual_seed(7)
+        dY = torch.randn((2048, 11008), device=dev, generator=g).bfloat16()
+        nv.nvfp4_qat_backward(dY, qp, a)
+    if which == "w4a16_any":  # a K that is a multiple of 16 but not of 64: [4096, 4080], M = m_decode
+        qa = nv.nvfp4_quantize_fos(bf(synth.decode_weight()[:, :4080].copy()), logical_scales=False,
+                                   choice=False)
+        nv.nvfp4_gemm_w4a16(bf(synth.decode_act(m_decode)[:, :4080].copy()), qa)
+    if which == "fp4_rate":  # the FP4 MMA rate kernel, 2000 x 4 MMAs per CTA pair
+        nv.nvfp4_measure_fp4_mma(2000)
     torch.cuda.synchronize()
     print("profile case", which, "status", nv.nvfp4_status_string(nv.nvfp4_get_device_status()))
 
@@ -991,7 +1057,8 @@ def main():
     ap.add_argument("--cpu-rows-reference", type=int, default=64)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["all", "quant", "w4a16", "w4a4", "gate_up"],
+    ap.add_argument("--profile-case", choices=["all", "quant", "w4a16", "w4a4", "gate_up", "qat", "w4a16_any",
+                                                "fp4_rate"],
                     help="launch each hot kernel once on a small case (for ncu) and exit")
     ap.add_argument("--profile-m", type=int, default=16, help="decode M of --profile-case")
     args = ap.parse_args()
