@@ -231,11 +231,21 @@ w4a4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
           const uint32_t sfb_t = sfa_t + C::kSfaCols + sfb_sub;
           const uint64_t adesc = smem_desc(smem_addr(sm.a[s]), 0, 1024, 2);
           const uint64_t bdesc = smem_desc(smem_addr(sm.b[s]), 0, 1024, 2);
-          for (int kk = 0; kk < kk_n; ++kk)
-            // advancing the start address by 32 bytes selects the next 64 FP4
-            // elements inside the 128-byte swizzle atom
-            mma_mxf4nvf4(tmem + C::kAccCol, adesc + 2ull * kk, bdesc + 2ull * kk, C::kIdesc, sfa_t + 4 * kk,
-                         sfb_t + 4 * C::kSfbTiles * kk, (ks | kk) != 0);
+          // advancing the start address by 32 bytes selects the next 64 FP4
+          // elements inside the 128-byte swizzle atom; a full stage is issued
+          // with constant offsets (see the pair kernel's issuer)
+          if (kk_n == 4) {
+            const uint32_t d = tmem + C::kAccCol, acc0 = ks != 0;
+            constexpr uint32_t sb = 4 * C::kSfbTiles;
+            mma_mxf4nvf4(d, adesc, bdesc, C::kIdesc, sfa_t, sfb_t, acc0);
+            mma_mxf4nvf4(d, adesc + 2ull, bdesc + 2ull, C::kIdesc, sfa_t + 4, sfb_t + sb, 1u);
+            mma_mxf4nvf4(d, adesc + 4ull, bdesc + 4ull, C::kIdesc, sfa_t + 8, sfb_t + 2 * sb, 1u);
+            mma_mxf4nvf4(d, adesc + 6ull, bdesc + 6ull, C::kIdesc, sfa_t + 12, sfb_t + 3 * sb, 1u);
+          } else {
+            for (int kk = 0; kk < kk_n; ++kk)
+              mma_mxf4nvf4(tmem + C::kAccCol, adesc + 2ull * kk, bdesc + 2ull * kk, C::kIdesc, sfa_t + 4 * kk,
+                           sfb_t + 4 * C::kSfbTiles * kk, (ks | kk) != 0);
+          }
           commit(&sm.empty[s]);
         }
         if (!failed) commit(&sm.acc_full);
@@ -563,34 +573,64 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
   } else if (warp == kMmaWarp) {
     if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer (even CTA of each pair) ----------------
-      int g = 0, t = 0;
+      // ring slot s and phase ph advance with the stage (no divisions); the
+      // descriptors and scale columns of slot s are the slot-0 ones plus s
+      // strides (a descriptor's start address is in 16-byte units)
+      int s = 0, t = 0;
+      uint32_t ph = 0;
+      const uint64_t adesc0 = smem_desc(smem_addr(sm.a[0]), 0, 1024, 2);
+      const uint64_t bdesc0 = smem_desc(smem_addr(sm.b[0]), 0, 1024, 2);
+      constexpr uint64_t kDescStride = (uint64_t)(kABytes >> 4);
+      static_assert(sizeof(sm.a[0]) == kABytes && sizeof(sm.b[0]) == kABytes, "stage stride");
       for (int64_t w = cl; w < n_work && !failed; w += ncl, ++t) {
         if (t > 0 && !mbar_wait(&sm.acc_free, (uint32_t)(t - 1) & 1u)) {
           failed = true;
           break;
         }
         fence_after_sync();
-        for (int ks = 0; ks < kt; ++ks, ++g) {
-          const int s = g % S;
-          if (!mbar_wait(&sm.sf_full[s], (uint32_t)(g / S) & 1u)) {
+        for (int ks = 0; ks < kt; ++ks) {
+          if (!mbar_wait(&sm.sf_full[s], ph)) {
             failed = true;
             break;
           }
           fence_after_sync();
           const int kk_n = min(4, kb64 - 4 * ks);
-          const uint32_t sfa_t = tmem + kPairSfCol + kPairSfStageCols * s;
+          const uint32_t sfa_t = tmem + kPairSfCol + kPairSfStageCols * (uint32_t)s;
           const uint32_t sfb_t = sfa_t + 16;
-          const uint64_t adesc = smem_desc(smem_addr(sm.a[s]), 0, 1024, 2);
-          const uint64_t bdesc = smem_desc(smem_addr(sm.b[s]), 0, 1024, 2);
+          const uint64_t adesc = adesc0 + kDescStride * (uint64_t)s;
+          const uint64_t bdesc = bdesc0 + kDescStride * (uint64_t)s;
+          // This thread is latency-bound: every tcgen05 instruction and barrier
+          // test takes ~90 cycles to issue, against 128 cycles of tensor work
+          // per pair MMA, so a full stage is issued as four MMAs with constant
+          // operand offsets and one accumulate flag (per-MMA address and
+          // predicate arithmetic in a rolled loop lengthened the stage period
+          // by ~17 %, measured).
+          const uint32_t acc0 = ks != 0;
           if (kBF16) {
-            for (int kk = 0; kk < kk_n; ++kk)
-              mma_f16_pair(tmem, adesc + 2ull * kk, bdesc + 2ull * kk, kPairIdescBf16, (ks | kk) != 0);
+            if (kk_n == 4) {
+              mma_f16_pair(tmem, adesc, bdesc, kPairIdescBf16, acc0);
+              mma_f16_pair(tmem, adesc + 2ull, bdesc + 2ull, kPairIdescBf16, 1u);
+              mma_f16_pair(tmem, adesc + 4ull, bdesc + 4ull, kPairIdescBf16, 1u);
+              mma_f16_pair(tmem, adesc + 6ull, bdesc + 6ull, kPairIdescBf16, 1u);
+            } else {
+              for (int kk = 0; kk < kk_n; ++kk)
+                mma_f16_pair(tmem, adesc + 2ull * kk, bdesc + 2ull * kk, kPairIdescBf16, (ks | kk) != 0);
+            }
+          } else if (kk_n == 4) {
+            mma_mxf4nvf4_pair(tmem, adesc, bdesc, kPairIdesc, sfa_t, sfb_t, acc0);
+            mma_mxf4nvf4_pair(tmem, adesc + 2ull, bdesc + 2ull, kPairIdesc, sfa_t + 4, sfb_t + 8, 1u);
+            mma_mxf4nvf4_pair(tmem, adesc + 4ull, bdesc + 4ull, kPairIdesc, sfa_t + 8, sfb_t + 16, 1u);
+            mma_mxf4nvf4_pair(tmem, adesc + 6ull, bdesc + 6ull, kPairIdesc, sfa_t + 12, sfb_t + 24, 1u);
           } else {
             for (int kk = 0; kk < kk_n; ++kk)
               mma_mxf4nvf4_pair(tmem, adesc + 2ull * kk, bdesc + 2ull * kk, kPairIdesc, sfa_t + 4 * kk,
                                 sfb_t + 8 * kk, (ks | kk) != 0);
           }
           commit_pair(&sm.empty[s], pair_mask);
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
         if (!failed) commit_pair(&sm.acc_full, pair_mask);
       }
