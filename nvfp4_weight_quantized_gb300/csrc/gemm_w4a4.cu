@@ -756,18 +756,21 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");  // staging buffer free
         uint32_t hi[8][8];
 #pragma unroll
-        for (int c2 = 0; c2 < 8; ++c2) {  // 32 columns per load: chunks 2 c2, 2 c2 + 1 of 16
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + 32 * c2, v);
+        for (int c4 = 0; c4 < 4; ++c4) {  // 64 columns per wait (two loads in flight): chunks 4 c4 .. 4 c4 + 3 of 16
+          uint32_t v0[32], v1[32];
+          tmem_ld_32x32b_x32(tmem + lane_base + 64 * c4, v0);
+          tmem_ld_32x32b_x32(tmem + lane_base + 64 * c4 + 32, v1);
           tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int c = 2 * c2 + h;
+          for (int h = 0; h < 4; ++h) {
+            const int c = 4 * c4 + h;
             uint32_t p[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              p[i] = bf16x2_rn(__uint_as_float(v[16 * h + 2 * i]) * alpha,
-                               __uint_as_float(v[16 * h + 2 * i + 1]) * alpha);
+            for (int i = 0; i < 8; ++i) {
+              const int j = 16 * (h & 1) + 2 * i;  // a constant once unrolled: both arrays stay in registers
+              const uint32_t lo = h < 2 ? v0[j] : v1[j], hi2 = h < 2 ? v0[j + 1] : v1[j + 1];
+              p[i] = bf16x2_rn(__uint_as_float(lo) * alpha, __uint_as_float(hi2) * alpha);
+            }
             if (c < 8) {
               uint8_t* box = sm.ystage + (c >> 2) * (BM * 128) + r * 128;
 #pragma unroll
@@ -816,11 +819,13 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + 32 * c, v);
+        for (int c = 0; c < 8; c += 2) {  // two loads in flight per wait
+          uint32_t v0[32], v1[32];
+          tmem_ld_32x32b_x32(tmem + lane_base + 32 * c, v0);
+          tmem_ld_32x32b_x32(tmem + lane_base + 32 * c + 32, v1);
           tmem_wait_ld();
-          if (row < M && n0 + 32 * c < N) store_row32<kF32>(y, row * N, n0 + 32 * c, N, v, alpha, vec_ok);
+          if (row < M && n0 + 32 * c < N) store_row32<kF32>(y, row * N, n0 + 32 * c, N, v0, alpha, vec_ok);
+          if (row < M && n0 + 32 * c + 32 < N) store_row32<kF32>(y, row * N, n0 + 32 * c + 32, N, v1, alpha, vec_ok);
         }
         fence_before_sync();
         __syncwarp();
