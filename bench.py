@@ -555,7 +555,7 @@ def act_fos_compare(nv, dev, stream, M=1024):
 
 
 def gate_up_bench(nv, dev, stream):
-    """Gated MLP projection silu(X W_gate^T) * (X W_up^T) on the config-3
+    """Gated MLP projection silu(X W_gate^T) * (X W_up^T) on the MLP
     gate/up weight [2 x 11008, 4096] (N(0, 0.02^2) x per-row lognormal(0, 0.5)):
     nvfp4_linear_silu_mul against nvfp4_linear on the same weight (Y [M, 2F]),
     at decode M (W4A16 + the separate silu kernel; 4 weight copies rotate so
