@@ -149,75 +149,84 @@ __device__ __forceinline__ uint32_t pack4(uint32_t b0, uint32_t b1, uint32_t b2,
   return __byte_perm(__byte_perm(b0, b1, 0x0040u), __byte_perm(b2, b3, 0x0040u), 0x5410u);
 }
 
-// E2M1 codes of two magnitudes from the IEEE binary32 quotients x / eff.
+// E2M1 codes of two values from the IEEE binary32 quotients x / eff.
 __device__ __forceinline__ uint32_t exact_pair(float x0, float x1, float eff) {
-  return cvt_e2m1x2(fminf(__fdiv_rn(x1, eff), 6.0f), fminf(__fdiv_rn(x0, eff), 6.0f));
+  return cvt_e2m1x2(fmaxf(fminf(__fdiv_rn(x1, eff), 6.0f), -6.0f), fmaxf(fminf(__fdiv_rn(x0, eff), 6.0f), -6.0f));
 }
 
-// One candidate scale for a block of 16 magnitudes (x2[j] = elements 2j,
-// 2j+1); eff = value(scale) * ts, bmax = max |x|.  Returns the block SSE and
-// the 16 magnitude codes packed 8 per word (element 0 in the lowest nibble);
-// the caller attaches the signs (the squared error of x equals that of |x|).
+// Non-negative E4M3 byte -> binary32 by the hardware E4M3 -> f16 conversion
+// (every E4M3 value is exact in f16, and f16 -> binary32 is exact).
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+  float f;
+  asm("{\n\t.reg .b16 e, lo, hi;\n\t.reg .b32 h;\n\tcvt.u16.u32 e, %1;\n\tcvt.rn.f16x2.e4m3x2 h, e;\n\t"
+      "mov.b32 {lo, hi}, h;\n\tcvt.f32.f16 %0, lo;\n\t}"
+      : "=f"(f) : "r"(b));
+  return f;
+}
+
+// One candidate scale for a block of 16 values, given negated (nx2[j] =
+// -elements 2j, 2j+1); eff = value(scale) * ts, bmax = max |x|.  Returns the
+// block SSE and the 16 signed codes packed 8 per word (element 0 in the lowest
+// nibble).  Signed values go through every step: round-to-nearest is
+// symmetric, so each code's magnitude and each squared error equal those of
+// |x|, and the conversion sets the code's sign bit from the quotient's sign.
+// The negated form keeps that sign right for x = -0, whose quotient must stay
+// -0: a sum of zeros of opposite signs rounds to +0, so the correction below
+// is arranged so that for a zero x every sum it forms has two zeros of x's
+// sign.
 //
-// Codes: with r ~ 1/eff (the hardware reciprocal approximation, relative
-// error below 2^-22), the products x * RN(r * (1 -/+ 2^-20)) bracket
-// RN(x / eff); when both ends convert to the same E2M1 code, that is the code
-// of RN(x / eff) (the conversion is monotone).  A pair whose ends differ (its
-// quotient lies within ~2^-20 of a rounding midpoint -- common, since x and
-// eff often share small factors) takes the IEEE division instead, as does a
-// whole block whose eff is outside the range where the bracket is safe.
-// Errors: d = RN(x - value * eff) (one fused step), then
+// Codes: RN(x / eff) for every element by Markstein's correction (P.
+// Markstein, "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Develop. 34(1), 1990): with y = RN(1 / eff) (the
+// IEEE reciprocal) and q = RN(x * y), the residual r = x - q * eff is exact in
+// one fused step and RN(q + r * y) is the correctly rounded quotient, as long
+// as nothing overflows or underflows.  Here q = RN((-x) * (-y)), the residual
+// is taken as RN(q * eff - x) and the quotient as RN(q - that * y).  That is three packed operations per
+// pair for every element and no data-dependent branch (quotients that land on
+// an E2M1 rounding midpoint are common, since x and eff often share small
+// factors, and a per-warp fallback for them cost more than the whole path).
+// A block whose eff is outside the guarded range takes IEEE divisions; a
+// quotient too small to be normal encodes as a zero code either way.
+// Errors: d = RN(value * eff - x) (one fused step; the negative of
+// RN(x - value * eff), so every square is the same), then
 // a_j = RN(d_j^2 + RN(d_j+8^2)), b_j = a_j + a_j+4, c_j = b_j + b_j+2,
 // SSE = c_0 + c_1.  A product only ever feeds the addend of an explicit fma,
 // so no compiler contraction can change the rounding.
-__device__ __forceinline__ float cand(const f2 (&x2)[8], float bmax, float eff, uint32_t (&codes)[2]) {
+__device__ __forceinline__ float cand(const f2 (&nx2)[8], float bmax, float eff, uint32_t (&codes)[2]) {
   uint32_t bl[8];
-  if (eff == 0.0f) {
+  const f2 eff2 = pk(eff, eff);
+  if (eff == 0.0f) {  // every code is a zero carrying the sign of its element
 #pragma unroll
-    for (int j = 0; j < 8; ++j) bl[j] = 0u;
+    for (int j = 0; j < 8; ++j) {
+      float n0, n1;
+      upk(nx2[j], n0, n1);
+      bl[j] = cvt_e2m1x2(__fmul_rn(n1, -0.0f), __fmul_rn(n0, -0.0f));
+    }
   } else {
-    float r;
-    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(eff));
-    if (eff >= 0x1p-100f && __fmul_rn(bmax, r) < 0x1p100f) {
-      const float rlo = __fmul_rn(r, 0.99999904632568359375f);  // 1 - 2^-20
-      const float rhi = __fmul_rn(r, 1.00000095367431640625f);  // 1 + 2^-20
-      const f2 rl2 = pk(rlo, rlo), rh2 = pk(rhi, rhi);
-      uint32_t differ = 0;  // OR of (low end code ^ high end code) over the pairs
+    const float y = __frcp_rn(eff);
+    if (eff >= 0x1p-100f && __fmul_rn(bmax, y) < 0x1p100f) {
+      const f2 ny2 = pk(-y, -y);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        float l0, l1, h0, h1;
-        upk(mul2(x2[j], rl2), l0, l1);
-        upk(mul2(x2[j], rh2), h0, h1);
-        bl[j] = cvt_e2m1x2(l1, l0);
-        differ |= bl[j] ^ cvt_e2m1x2(h1, h0);
-      }
-      if (__builtin_expect(differ != 0, 0)) {  // rare: redo the ambiguous pairs by division
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float l0, l1, h0, h1, x0, x1;
-          upk(mul2(x2[j], rl2), l0, l1);
-          upk(mul2(x2[j], rh2), h0, h1);
-          if (cvt_e2m1x2(l1, l0) != cvt_e2m1x2(h1, h0)) {
-            upk(x2[j], x0, x1);
-            bl[j] = exact_pair(x0, x1, eff);
-          }
-        }
+        const f2 q = mul2(nx2[j], ny2);                                   // RN(x * y)
+        float q0, q1;
+        upk(fma2(fma2(q, eff2, nx2[j]), ny2, q), q0, q1);  // RN(x / eff), satfinite to +-6 below
+        bl[j] = cvt_e2m1x2(q1, q0);
       }
     } else {
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        float x0, x1;
-        upk(x2[j], x0, x1);
-        bl[j] = exact_pair(x0, x1, eff);
+        float n0, n1;
+        upk(nx2[j], n0, n1);
+        bl[j] = exact_pair(-n0, -n1, eff);
       }
     }
   }
   codes[0] = pack4(bl[0], bl[1], bl[2], bl[3]);
   codes[1] = pack4(bl[4], bl[5], bl[6], bl[7]);
-  const f2 neff2 = pk(-eff, -eff);
   f2 d[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) d[j] = fma2(e2m1x2_to_f2(bl[j]), neff2, x2[j]);
+  for (int j = 0; j < 8; ++j) d[j] = fma2(e2m1x2_to_f2(bl[j]), eff2, nx2[j]);
   f2 a[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) a[j] = fma2(d[j], d[j], mul2(d[4 + j], d[4 + j]));  // (a_2j, a_2j+1)
@@ -236,7 +245,7 @@ __device__ __forceinline__ float cand(const f2 (&x2)[8], float bmax, float eff, 
 template <bool kFos>
 __device__ __forceinline__ void quantize_tile(const uint4 (&v)[2][2], const bool (&ok)[2], const int64_t (&rr)[2],
                                               int64_t t, int c, int ri, int ci, int kb, float ts, bool fast6,
-                                              float inv6ts, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                              float yts, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                                               uint8_t* __restrict__ scales_mma, uint8_t* __restrict__ choice,
                                               uint8_t* stage, uint32_t& n_m4) {
 #pragma unroll
@@ -245,43 +254,32 @@ __device__ __forceinline__ void quantize_tile(const uint4 (&v)[2][2], const bool
     if (ok[h]) {
       const uint32_t w[8] = {v[h][0].x, v[h][0].y, v[h][0].z, v[h][0].w,
                              v[h][1].x, v[h][1].y, v[h][1].z, v[h][1].w};
-      f2 x2[8];  // magnitudes, elements (2j, 2j+1)
-      uint32_t m2 = 0;
+      f2 nx2[8];  // negated values, elements (2j, 2j+1): adding 2^31 toggles the sign bit
+      uint32_t m2 = 0;  // largest magnitude bits, per half
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const uint32_t a = w[j] & 0x7FFF7FFFu;
-        x2[j] = pk(__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u));
-        m2 = __vmaxu2(m2, a);
-      }
-      // sign bits of the 16 codes: byte j of sgn[q] gets the signs of elements
-      // 8q+2j (bit 3) and 8q+2j+1 (bit 7), i.e. bit 15 and bit 31 of word 4q+j
-      uint32_t sgn[2];
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const uint32_t g1 = __byte_perm(__byte_perm(w[4 * q], w[4 * q + 1], 0x0051u),
-                                        __byte_perm(w[4 * q + 2], w[4 * q + 3], 0x0051u), 0x5410u);
-        const uint32_t g3 = __byte_perm(__byte_perm(w[4 * q], w[4 * q + 1], 0x0073u),
-                                        __byte_perm(w[4 * q + 2], w[4 * q + 3], 0x0073u), 0x5410u);
-        sgn[q] = ((g1 >> 4) & 0x08080808u) | (g3 & 0x80808080u);
+        nx2[j] = pk(__uint_as_float(w[j] * 65536u + 0x80000000u), __uint_as_float((w[j] & 0xFFFF0000u) ^ 0x80000000u));
+        m2 = __vmaxu2(m2, w[j] & 0x7FFF7FFFu);
       }
       const float bmax = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
-      // s6 = E4M3((amax_block / 6) / ts).  bmax * inv6ts is within 2^-21 of
-      // the twice-rounded quotient (relative; tiny quotients are far below
-      // the smallest E4M3 step either way), so the two ends of a 2^-20
-      // bracket convert to the same E4M3 code unless the quotient is within
-      // ~2^-20 of a rounding midpoint -- then it is formed as written.
+      // s6 = E4M3(RN(RN(amax_block / 6) / ts)): each division by Markstein's
+      // correction (RN(1/6) is a constant, yts = RN(1 / ts)); a block maximum
+      // too small for RN(bmax / 6) to be normal, or a tensor scale outside
+      // the normal range, takes the IEEE divisions.
       uint32_t s6;
-      {
-        const float q = __fmul_rn(bmax, inv6ts);
-        const uint32_t c2 =
-            cvt_e4m3x2(__fmul_rn(q, 1.00000095367431640625f), __fmul_rn(q, 0.99999904632568359375f));
-        s6 = c2 & 0xFFu;
-        if (__builtin_expect(!fast6 || s6 != (c2 >> 8), 0))
-          s6 = cvt_e4m3x2(0.0f, __fdiv_rn(__fdiv_rn(bmax, 6.0f), ts)) & 0xFFu;
+      if (__builtin_expect(fast6 && (bmax >= 0x1p-120f || bmax == 0.0f), 1)) {
+        constexpr float kInv6 = 1.0f / 6.0f;  // RN(1/6)
+        float q = __fmul_rn(bmax, kInv6);
+        q = __fmaf_rn(__fmaf_rn(q, -6.0f, bmax), kInv6, q);
+        float u = __fmul_rn(q, yts);
+        u = __fmaf_rn(__fmaf_rn(u, -ts, q), yts, u);
+        s6 = cvt_e4m3x2(0.0f, u) & 0xFFu;
+      } else {
+        s6 = cvt_e4m3x2(0.0f, __fdiv_rn(__fdiv_rn(bmax, 6.0f), ts)) & 0xFFu;
       }
-      const float s6v = e4m3_to_f32(s6);
+      const float s6v = e4m3_value(s6);
       uint32_t cw[2];
-      const float sse6 = cand(x2, bmax, __fmul_rn(s6v, ts), cw);
+      const float sse6 = cand(nx2, bmax, __fmul_rn(s6v, ts), cw);
       s = s6;
       const int64_t blk = rr[h] * kb + c;
       if (kFos) {
@@ -289,7 +287,7 @@ __device__ __forceinline__ void quantize_tile(const uint4 (&v)[2][2], const bool
         bool m4 = false;
         if (s4 != s6) {  // equal scales tie, and a tie keeps M=6
           uint32_t cw4[2];
-          const float sse4 = cand(x2, bmax, __fmul_rn(e4m3_to_f32(s4), ts), cw4);
+          const float sse4 = cand(nx2, bmax, __fmul_rn(e4m3_value(s4), ts), cw4);
           m4 = sse4 < sse6;
           if (m4) {
             cw[0] = cw4[0];
@@ -300,7 +298,7 @@ __device__ __forceinline__ void quantize_tile(const uint4 (&v)[2][2], const bool
         }
         if (choice != nullptr) choice[blk] = m4 ? 1 : 0;
       }
-      *reinterpret_cast<uint2*>(codes + 8 * blk) = make_uint2(cw[0] | sgn[0], cw[1] | sgn[1]);
+      *reinterpret_cast<uint2*>(codes + 8 * blk) = make_uint2(cw[0], cw[1]);
       if (scales != nullptr) scales[blk] = (uint8_t)s;
     }
     if (scales_mma != nullptr) {
@@ -334,9 +332,9 @@ quant_kernel(const uint4* __restrict__ x, int64_t rows, int64_t K, const uint32_
   const float amax = __uint_as_float(am << 16);
   const float ts = amax == 0.0f ? 1.0f : __fdiv_rn(amax, divisor);
   if (blockIdx.x == 0 && threadIdx.x == 0) *ts_out = ts;
-  // the bracketed s6 needs 6 * ts (and so its reciprocal) in the normal range
-  const bool fast6 = __fmul_rn(6.0f, ts) >= 0x1p-126f;
-  const float inv6ts = fast6 ? __frcp_rn(__fmul_rn(6.0f, ts)) : 0.0f;
+  // the corrected divisions of s6 need ts, and so RN(1 / ts), in the normal range
+  const bool fast6 = ts >= 0x1p-126f && ts <= 0x1p126f;
+  const float yts = fast6 ? __frcp_rn(ts) : 0.0f;
 
   // Work unit: one tile of the MMA scale layout, 128 rows x 4 blocks of 16
   // (64 K positions); thread i of the CTA takes blocks (i/4, i%4) and
@@ -369,7 +367,7 @@ quant_kernel(const uint4* __restrict__ x, int64_t rows, int64_t K, const uint32_
         v[h][1] = ld_u4_policy(p + 1, pol);
       }
     }
-quantize_tile<kFos>(v, ok, rr, t, c, ri, ci, kb, ts, fast6, inv6ts, codes, scales, scales_mma, choice, stage[buf],
+quantize_tile<kFos>(v, ok, rr, t, c, ri, ci, kb, ts, fast6, yts, codes, scales, scales_mma, choice, stage[buf],
                         n_m4);
   }
   griddep_launch_dependents();
@@ -451,8 +449,9 @@ quant_fused_kernel(const uint4* __restrict__ x, int64_t rows, int64_t K, uint32_
   const float amax = __uint_as_float(am << 16);
   const float ts = amax == 0.0f ? 1.0f : __fdiv_rn(amax, divisor);
   if (blockIdx.x == 0 && threadIdx.x == 0) *ts_out = ts;
-  const bool fast6 = __fmul_rn(6.0f, ts) >= 0x1p-126f;
-  const float inv6ts = fast6 ? __frcp_rn(__fmul_rn(6.0f, ts)) : 0.0f;
+  // the corrected divisions of s6 need ts, and so RN(1 / ts), in the normal range
+  const bool fast6 = ts >= 0x1p-126f && ts <= 0x1p126f;
+  const float yts = fast6 ? __frcp_rn(ts) : 0.0f;
   const uint64_t once = l2_policy_evict_first();
   uint32_t n_m4 = 0;
   int buf = 0;
@@ -474,7 +473,7 @@ quant_fused_kernel(const uint4* __restrict__ x, int64_t rows, int64_t K, uint32_
         v[h][1] = ld_u4_policy(p + 1, once);
       }
     }
-    quantize_tile<kFos>(v, ok, rr, t, c, ri, ci, kb, ts, fast6, inv6ts, codes, scales, scales_mma, choice, stage[buf],
+    quantize_tile<kFos>(v, ok, rr, t, c, ri, ci, kb, ts, fast6, yts, codes, scales, scales_mma, choice, stage[buf],
                         n_m4);
   }
   if (kFos && m4_count != nullptr) {
