@@ -855,9 +855,10 @@ def measure_e2e(nv, dev, stream, q, args, step_bytes):
     copies each linear's quantised weight (codes, MMA-tiled scales, tensor
     scale; one weight per M, as in the device-resident step) and its
     activations from pinned host memory, runs nvfp4_linear, and copies every
-    output back, all inside the timed region.  The inputs of a step sit in one
-    pinned buffer (and one device buffer of the same layout), so a step is one
-    host-to-device copy, the calls, and one device-to-host copy."""
+    output back, all inside the timed region.  A step's inputs sit in one
+    pinned buffer and go over in one host-to-device copy, on a copy stream,
+    into one of two device buffers in turn, so the next step's copy overlaps
+    this step's calls and its device-to-host read of the outputs."""
     import torch
     N, K = N_DEC, K_DEC
     # the copy of a step writes the weights its GEMMs read: no GEMM may start
@@ -871,55 +872,76 @@ def measure_e2e(nv, dev, stream, q, args, step_bytes):
         offs[M] = o
         o += sum(seg_w) + align(M * K * 2)
     h_in = torch.empty(o, dtype=torch.uint8).pin_memory()
-    d_in = torch.empty(o, dtype=torch.uint8, device=dev)
+    d_in = [torch.empty(o, dtype=torch.uint8, device=dev) for _ in range(2)]
     y_off, yo = {}, 0
     for M in DECODE_M:
         y_off[M] = yo
         yo += M * N * 2
-    h_out = torch.empty(yo, dtype=torch.uint8).pin_memory()
-    d_out = torch.empty(yo, dtype=torch.uint8, device=dev)
+    h_out = [torch.empty(yo, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    d_out = [torch.empty(yo, dtype=torch.uint8, device=dev) for _ in range(2)]
 
     def view(buf, off, t):
         n = t.numel() * t.element_size()
         return buf[off:off + n].view(t.dtype).view(t.shape)
 
-    w, X, Y = {}, {}, {}
+    w = [{}, {}]
+    X = [{}, {}]
+    Y = [{}, {}]
     for M in DECODE_M:
+        xh = torch.from_numpy(synth.decode_act(M).view(np.int16)).view(torch.bfloat16)
         o = offs[M]
-        views = []
         for t, n in zip(parts, seg_w):
             view(h_in, o, t).copy_(t.cpu())
-            views.append(view(d_in, o, t))
             o += n
-        w[M] = nv.NVFP4Weight(views[0], views[1], views[2], N, K)
-        xh = torch.from_numpy(synth.decode_act(M).view(np.int16)).view(torch.bfloat16)
         view(h_in, o, xh).copy_(xh)
-        X[M] = view(d_in, o, xh)
-        Y[M] = d_out[y_off[M]:y_off[M] + M * N * 2].view(torch.bfloat16).view(M, N)
+        for b in range(2):
+            o = offs[M]
+            views = []
+            for t, n in zip(parts, seg_w):
+                views.append(view(d_in[b], o, t))
+                o += n
+            w[b][M] = nv.NVFP4Weight(views[0], views[1], views[2], N, K)
+            X[b][M] = view(d_in[b], o, xh)
+            Y[b][M] = d_out[b][y_off[M]:y_off[M] + M * N * 2].view(torch.bfloat16).view(M, N)
     lws = {M: torch.empty(max(nv.nvfp4_workspace_bytes(nv.OP_LINEAR, M, N, K), 256), dtype=torch.uint8,
                           device=dev) for M in DECODE_M}
-    h2d, d2h = h_in.numel(), h_out.numel()
+    h2d, d2h = h_in.numel(), h_out[0].numel()
+    copy_stream = torch.cuda.Stream(device=dev)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    for b in range(2):
+        done[b].record(stream)
 
-    def step():
-        d_in.copy_(h_in, non_blocking=True)
-        for M in DECODE_M:
-            nv.nvfp4_linear(X[M], w[M], out=Y[M], workspace=lws[M], stream=stream)
-        h_out.copy_(d_out, non_blocking=True)
+    def step(i):
+        b = i % 2
+        copy_stream.wait_event(done[b])  # the buffer's previous step is over
+        with torch.cuda.stream(copy_stream):
+            d_in[b].copy_(h_in, non_blocking=True)
+            copied[b].record(copy_stream)
+        stream.wait_event(copied[b])
+        with torch.cuda.stream(stream):
+            for M in DECODE_M:
+                nv.nvfp4_linear(X[b][M], w[b][M], out=Y[b][M], workspace=lws[M], stream=stream)
+            h_out[b].copy_(d_out[b], non_blocking=True)
+            done[b].record(stream)
 
-    with torch.cuda.stream(stream):
-        for _ in range(max(args.warmup, 3)):
-            step()
-        stream.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for b in range(2):
+        done[b].record(stream)  # the timed copies start after e0
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)  # after the last step's outputs are back (its copy came before its calls)
     e1.synchronize()
     t = e0.elapsed_time(e1) * 1e-3 / args.steps
     return {"value": round(step_bytes / t / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(t * 1e3, 4)}
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(t * 1e3, 4),
+            "pipelining": "two device input buffers: a step's host-to-device copy overlaps the previous "
+                          "step's calls and output read-back"}
 
 
 # ------------------------------------------------------------ CPU oracle ---
