@@ -68,34 +68,6 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fmul_rn(__fdividef(g, __fadd_rn(1.0f, __expf(-g))), u);
 }
 
-// ------------------------------------------------------------ memory ops ---
-
-__device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ uint2 ld_stream_u2(const void* p) {
-  uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ uint32_t ld_stream_u8(const void* p) {
-  uint16_t v;
-  asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(v) : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ uint4 ld_cached_u4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
-
 // Programmatic dependent launch (kernels are launched with
 // cudaLaunchAttributeProgrammaticStreamSerialization): griddep_wait() blocks
 // until the previous grid in the stream has completed and its writes are

@@ -96,12 +96,6 @@ __device__ __forceinline__ void commit(uint64_t* bar) {
                : "memory");
 }
 
-// Copy a 32-row x 128-bit shared-memory tile into TMEM lanes 0-31 (4
-// columns), replicated into all four 32-lane sub-partitions.
-__device__ __forceinline__ void cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 // D[tmem] (+)= A[smem] * B[smem]^T with NVFP4 block scaling (E2M1 operands,
 // one UE4M3 scale per 16 elements, scales read from TMEM).  K = 64 per call.
 __device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
