@@ -423,9 +423,10 @@ w4a4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 //   scale loaders (warps 4-7, each CTA): full[s] -> TMEM -> arrive on the
 //     even CTA's sf_full[s] (8 arrivals: the stage is ready in both CTAs);
 //   MMA issuer (warp 9 of the even CTA): four pair MMAs per stage, then one
-//     commit that arrives on empty[s] of both CTAs; acc_full likewise;
+//     commit that arrives on empty[s] of both CTAs; acc_full[b] likewise;
 //   epilogue (warps 0-3, each CTA): drains its accumulator lanes, then
-//     arrives on the even CTA's acc_free (8 arrivals).
+//     arrives on the even CTA's acc_free[b] (8 arrivals).  b alternates
+//     between two accumulators in the bf16 mode and is 0 otherwise.
 // Every CTA loads its own operand tiles (no TMA multicast); rows both CTAs of
 // different pairs need are shared through L2.
 constexpr int kPairStages = 5;
@@ -445,8 +446,8 @@ struct __align__(1024) PairSmem {
   uint64_t full[kPairStages];     // this CTA's loads landed
   uint64_t sf_full[kPairStages];  // even CTA: scales in TMEM in both CTAs
   uint64_t empty[kPairStages];    // MMAs of the stage done (from the even CTA)
-  uint64_t acc_full;              // tile accumulated (from the even CTA)
-  uint64_t acc_free;              // even CTA: both accumulators drained
+  uint64_t acc_full[2];           // tile accumulated in accumulator b (from the even CTA)
+  uint64_t acc_free[2];           // even CTA: accumulator b drained in both CTAs
   uint32_t tmem_base;
 };
 
@@ -481,6 +482,13 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                  const float* __restrict__ b_ts, int64_t M, int64_t N, int64_t K, void* __restrict__ y,
                  unsigned int* __restrict__ status) {
   constexpr int S = kPairStages;
+  // The bf16 mode has no scale columns, so two 256-column accumulators fit
+  // in TMEM and alternate between tiles: the epilogue drains one while the
+  // MMAs fill the other.  The FP4 modes have one (columns 256-495 hold the
+  // stages' scale factors).
+  constexpr int kAccBufs = kBF16 ? 2 : 1;
+  constexpr uint32_t kAccStride = 256;
+  static_assert(kAccBufs * kAccStride <= kTmemCols && (kBF16 || kAccStride <= kPairSfCol), "TMEM budget");
   extern __shared__ uint8_t smem_raw[];
   PairSmem& sm = *reinterpret_cast<PairSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -502,8 +510,10 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
       mbar_init(&sm.sf_full[s], 2 * kSfWarps);
       mbar_init(&sm.empty[s], 1);
     }
-    mbar_init(&sm.acc_full, 1);
-    mbar_init(&sm.acc_free, 2 * kEpiWarps);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.acc_full[b], 1);
+      mbar_init(&sm.acc_free[b], 2 * kEpiWarps);
+    }
     fence_mbar_init();
     prefetch_tmap(&tmap_a);
     prefetch_tmap(&tmap_b);
@@ -583,7 +593,10 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
       constexpr uint64_t kDescStride = (uint64_t)(kABytes >> 4);
       static_assert(sizeof(sm.a[0]) == kABytes && sizeof(sm.b[0]) == kABytes, "stage stride");
       for (int64_t w = cl; w < n_work && !failed; w += ncl, ++t) {
-        if (t > 0 && !mbar_wait(&sm.acc_free, (uint32_t)(t - 1) & 1u)) {
+        // accumulator b of tile t, its use u (two alternate in the bf16 mode)
+        const int b = kAccBufs == 2 ? (t & 1) : 0, u = kAccBufs == 2 ? (t >> 1) : t;
+        const uint32_t acc = tmem + kAccStride * (uint32_t)b;
+        if (u > 0 && !mbar_wait(&sm.acc_free[b], (uint32_t)(u - 1) & 1u)) {
           failed = true;
           break;
         }
@@ -608,22 +621,22 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
           const uint32_t acc0 = ks != 0;
           if (kBF16) {
             if (kk_n == 4) {
-              mma_f16_pair(tmem, adesc, bdesc, kPairIdescBf16, acc0);
-              mma_f16_pair(tmem, adesc + 2ull, bdesc + 2ull, kPairIdescBf16, 1u);
-              mma_f16_pair(tmem, adesc + 4ull, bdesc + 4ull, kPairIdescBf16, 1u);
-              mma_f16_pair(tmem, adesc + 6ull, bdesc + 6ull, kPairIdescBf16, 1u);
+              mma_f16_pair(acc, adesc, bdesc, kPairIdescBf16, acc0);
+              mma_f16_pair(acc, adesc + 2ull, bdesc + 2ull, kPairIdescBf16, 1u);
+              mma_f16_pair(acc, adesc + 4ull, bdesc + 4ull, kPairIdescBf16, 1u);
+              mma_f16_pair(acc, adesc + 6ull, bdesc + 6ull, kPairIdescBf16, 1u);
             } else {
               for (int kk = 0; kk < kk_n; ++kk)
-                mma_f16_pair(tmem, adesc + 2ull * kk, bdesc + 2ull * kk, kPairIdescBf16, (ks | kk) != 0);
+                mma_f16_pair(acc, adesc + 2ull * kk, bdesc + 2ull * kk, kPairIdescBf16, (ks | kk) != 0);
             }
           } else if (kk_n == 4) {
-            mma_mxf4nvf4_pair(tmem, adesc, bdesc, kPairIdesc, sfa_t, sfb_t, acc0);
-            mma_mxf4nvf4_pair(tmem, adesc + 2ull, bdesc + 2ull, kPairIdesc, sfa_t + 4, sfb_t + 8, 1u);
-            mma_mxf4nvf4_pair(tmem, adesc + 4ull, bdesc + 4ull, kPairIdesc, sfa_t + 8, sfb_t + 16, 1u);
-            mma_mxf4nvf4_pair(tmem, adesc + 6ull, bdesc + 6ull, kPairIdesc, sfa_t + 12, sfb_t + 24, 1u);
+            mma_mxf4nvf4_pair(acc, adesc, bdesc, kPairIdesc, sfa_t, sfb_t, acc0);
+            mma_mxf4nvf4_pair(acc, adesc + 2ull, bdesc + 2ull, kPairIdesc, sfa_t + 4, sfb_t + 8, 1u);
+            mma_mxf4nvf4_pair(acc, adesc + 4ull, bdesc + 4ull, kPairIdesc, sfa_t + 8, sfb_t + 16, 1u);
+            mma_mxf4nvf4_pair(acc, adesc + 6ull, bdesc + 6ull, kPairIdesc, sfa_t + 12, sfb_t + 24, 1u);
           } else {
             for (int kk = 0; kk < kk_n; ++kk)
-              mma_mxf4nvf4_pair(tmem, adesc + 2ull * kk, bdesc + 2ull * kk, kPairIdesc, sfa_t + 4 * kk,
+              mma_mxf4nvf4_pair(acc, adesc + 2ull * kk, bdesc + 2ull * kk, kPairIdesc, sfa_t + 4 * kk,
                                 sfb_t + 8 * kk, (ks | kk) != 0);
           }
           commit_pair(&sm.empty[s], pair_mask);
@@ -632,7 +645,7 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             ph ^= 1u;
           }
         }
-        if (!failed) commit_pair(&sm.acc_full, pair_mask);
+        if (!failed) commit_pair(&sm.acc_full[b], pair_mask);
       }
       if (failed) atomicOr(status, kStatusTimeout);
     }
@@ -696,7 +709,9 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
       const int64_t m_tile = w / n_tiles, n_tile = w - m_tile * n_tiles;
       const int64_t m0 = m_tile * 256 + 128 * rank, n0 = n_tile * (kGateUp ? 128 : 256);
       const int64_t row = m0 + r;
-      const bool ok = __all_sync(0xffffffffu, !failed && mbar_wait(&sm.acc_full, (uint32_t)t & 1u));
+      const int b = kAccBufs == 2 ? (t & 1) : 0, u = kAccBufs == 2 ? (t >> 1) : t;
+      const uint32_t acc = tmem + kAccStride * (uint32_t)b + lane_base;  // this warp's lanes of accumulator b
+      const bool ok = __all_sync(0xffffffffu, !failed && mbar_wait(&sm.acc_full[b], (uint32_t)u & 1u));
       if (!ok) {
         failed = true;
         break;
@@ -711,8 +726,8 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
 #pragma unroll 1
         for (int c2 = 0; c2 < 4; ++c2) {  // 32 features per step: chunks 2 c2, 2 c2 + 1 of 16
           uint32_t vg[32], vu[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + 32 * c2, vg);
-          tmem_ld_32x32b_x32(tmem + lane_base + 128 + 32 * c2, vu);
+          tmem_ld_32x32b_x32(acc + 32 * c2, vg);
+          tmem_ld_32x32b_x32(acc + 128 + 32 * c2, vu);
           tmem_wait_ld();
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -735,7 +750,7 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         }
         fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(&sm.acc_free, lead);
+        if (lane == 0) mbar_arrive_cluster(&sm.acc_free[b], lead);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
         if (threadIdx.x == 0 && m0 < M) {
@@ -758,8 +773,8 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {  // 64 columns per wait (two loads in flight): chunks 4 c4 .. 4 c4 + 3 of 16
           uint32_t v0[32], v1[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + 64 * c4, v0);
-          tmem_ld_32x32b_x32(tmem + lane_base + 64 * c4 + 32, v1);
+          tmem_ld_32x32b_x32(acc + 64 * c4, v0);
+          tmem_ld_32x32b_x32(acc + 64 * c4 + 32, v1);
           tmem_wait_ld();
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
@@ -787,7 +802,7 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         }
         fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(&sm.acc_free, lead);
+        if (lane == 0) mbar_arrive_cluster(&sm.acc_free[b], lead);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           if (half == 1) {
@@ -821,15 +836,15 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
 #pragma unroll 1
         for (int c = 0; c < 8; c += 2) {  // two loads in flight per wait
           uint32_t v0[32], v1[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + 32 * c, v0);
-          tmem_ld_32x32b_x32(tmem + lane_base + 32 * c + 32, v1);
+          tmem_ld_32x32b_x32(acc + 32 * c, v0);
+          tmem_ld_32x32b_x32(acc + 32 * c + 32, v1);
           tmem_wait_ld();
           if (row < M && n0 + 32 * c < N) store_row32<kF32>(y, row * N, n0 + 32 * c, N, v0, alpha, vec_ok);
           if (row < M && n0 + 32 * c + 32 < N) store_row32<kF32>(y, row * N, n0 + 32 * c + 32, N, v1, alpha, vec_ok);
         }
         fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(&sm.acc_free, lead);
+        if (lane == 0) mbar_arrive_cluster(&sm.acc_free[b], lead);
       }
     }
     if (failed && lane == 0) atomicOr(status, kStatusTimeout);
