@@ -12,7 +12,7 @@
 //   dX [M, K] = dY [M, N] * (W_hat^T [K, N])^T   -- reduced over N;
 //   dW [N, K] = dY^T [N, M] * (X_hat^T [K, M])^T  -- reduced over M;
 // so the NVFP4 operands are dequantised straight into transposed bf16
-// buffers (dequant_bf16_t_kernel) and dY is transposed (transpose_bf16_kernel),
+// buffers (dequant_bf16_t_kernel) and dY is transposed (transpose_t_kernel),
 // rows padded with zeros to a multiple of 16 elements.
 #include <algorithm>
 
@@ -59,52 +59,130 @@ dequant_bf16_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict
   }
 }
 
+// The transposing kernels stage a tile in shared memory as bf16 pairs: word
+// (c, p) holds source rows 2p and 2p + 1 of tile column c (row 2p in the low
+// half), i.e. two adjacent elements of output row c.  A thread owns one row
+// pair, so every shared-memory write is a whole word, and word p of row c is
+// stored at p ^ swz(c) with swz(c) a multiple of 4: the 32 threads of a warp
+// that write one tile column hit 32 different banks, and four consecutive
+// words (one 16-byte piece of an output row) stay together.
+constexpr int kPairWords = kTile / 2;  // words per staged tile row (64 source rows)
+
+__device__ __forceinline__ uint32_t pair_lo(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x5410u); }
+__device__ __forceinline__ uint32_t pair_hi(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x7632u); }
+
+__device__ __forceinline__ uint32_t bf16_bits(float v) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  return (uint32_t)*reinterpret_cast<const uint16_t*>(&h);
+}
+
 // NVFP4 [R, K] -> bf16 out^T [K, Rp] (out[k * Rp + r]), columns R .. Rp - 1
-// zero; Rp % 8 == 0.  A CTA dequantises a 64 x 64 tile (one 16-element block
-// per thread), transposes it in shared memory and writes 64 rows of 128 bytes.
+// zero; Rp % 8 == 0.  A CTA covers 64 rows x 128 K positions: thread (p, b)
+// dequantises 16-element block b of rows 2p and 2p + 1, the tile is staged
+// transposed as described above, and the CTA writes 128 output rows of 128
+// bytes with 16-byte stores.
+constexpr int kDqK = 128;  // K positions per CTA
 __global__ void __launch_bounds__(kThreads)
 dequant_bf16_t_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ smma,
                       const float* __restrict__ ts_ptr, int64_t R, int64_t K, int64_t Rp,
                       __nv_bfloat16* __restrict__ out) {
-  __shared__ __align__(16) __nv_bfloat16 tile[kTile][kTilePitch];
+  __shared__ __align__(16) uint32_t tw[kDqK][kPairWords];
   griddep_wait();
   const float ts = *ts_ptr;
   const int64_t kb = K / 16, ct = (kb + 3) / 4;
-  const int64_t r0 = (int64_t)blockIdx.x * kTile, k0 = (int64_t)blockIdx.y * kTile;
+  const int64_t r0 = (int64_t)blockIdx.x * kTile, k0 = (int64_t)blockIdx.y * kDqK;
   {
-    const int rl = threadIdx.x & 63, cl = threadIdx.x >> 6;  // row, 16-block of the tile
-    const int64_t r = r0 + rl, c = k0 / 16 + cl;
-    __nv_bfloat16 v[16];
-    if (r < R && c < kb) {
-      const uint2 cw = *reinterpret_cast<const uint2*>(codes + r * (K / 2) + 8 * c);
-      const float s = e4m3_to_f32(smma[scale_mma_offset(r, c, ct)]);
+    const int p = threadIdx.x & 31, b = threadIdx.x >> 5;  // row pair, 16-block of the tile
+    const int64_t c = k0 / 16 + b;
+    uint32_t h[2][16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        v[j] = __float2bfloat16_rn(dequant_value(((j < 8 ? cw.x : cw.y) >> (4 * (j & 7))) & 15u, s, ts));
-    } else {
+    for (int e = 0; e < 2; ++e) {
+      const int64_t r = r0 + 2 * p + e;
+      if (r < R && c < kb) {
+        const uint2 cw = *reinterpret_cast<const uint2*>(codes + r * (K / 2) + 8 * c);
+        const float s = e4m3_to_f32(smma[scale_mma_offset(r, c, ct)]);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] = __float2bfloat16_rn(0.0f);
+        for (int j = 0; j < 16; ++j)
+          h[e][j] = bf16_bits(dequant_value(((j < 8 ? cw.x : cw.y) >> (4 * (j & 7))) & 15u, s, ts));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) h[e][j] = 0u;
+      }
     }
 #pragma unroll
-    for (int j = 0; j < 16; ++j) tile[16 * cl + j][rl] = v[j];
+    for (int j = 0; j < 16; ++j) {
+      const int cc = 16 * b + j;
+      tw[cc][p ^ (4 * (cc & 7))] = h[0][j] | (h[1][j] << 16);
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int pass = 0; pass < kDqK / 32; ++pass) {
+    const int cc = (threadIdx.x >> 3) + 32 * pass, u = threadIdx.x & 7;
+    const int64_t k = k0 + cc, r = r0 + 8 * u;
+    if (k < K && r < Rp)
+      *reinterpret_cast<uint4*>(out + k * Rp + r) = *reinterpret_cast<const uint4*>(&tw[cc][4 * (u ^ (cc & 7))]);
+  }
+}
+
+// bf16 [rows, cols] (row pitch `spitch`) -> dst^T [cols, rows_p]
+// (dst[c * rows_p + r]), rows rows .. rows_p - 1 zero; rows_p % 8 == 0.  A CTA
+// covers a 64 x 64 tile: thread (p, v) reads the 8 columns 8v .. 8v + 7 of
+// rows 2p and 2p + 1 (16-byte loads when the rows are 16-byte aligned and the
+// piece lies inside the source), the tile is staged transposed as described
+// above, and the CTA writes 64 output rows of 128 bytes with 16-byte stores.
+__global__ void __launch_bounds__(kThreads)
+transpose_t_kernel(const __nv_bfloat16* __restrict__ src, int64_t rows, int64_t cols, int64_t spitch,
+                   __nv_bfloat16* __restrict__ dst, int64_t rows_p) {
+  __shared__ __align__(16) uint32_t tw[kTile][kPairWords];
+  griddep_wait();
+  const int64_t r0 = (int64_t)blockIdx.x * kTile, c0 = (int64_t)blockIdx.y * kTile;
+  const bool vec = (spitch & 7) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+  {
+    const int p = threadIdx.x >> 3, v = threadIdx.x & 7;  // row pair, 8-column piece
+    const int64_t c = c0 + 8 * v;
+    uint4 x[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int64_t r = r0 + 2 * p + e;
+      x[e] = make_uint4(0u, 0u, 0u, 0u);
+      if (r < rows) {
+        const __nv_bfloat16* row = src + r * spitch;
+        if (vec && c + 8 <= cols) {
+          x[e] = *reinterpret_cast<const uint4*>(row + c);
+        } else {
+          uint16_t hv[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) hv[j] = c + j < cols ? reinterpret_cast<const uint16_t*>(row)[c + j] : 0;
+          x[e] = make_uint4(hv[0] | ((uint32_t)hv[1] << 16), hv[2] | ((uint32_t)hv[3] << 16),
+                            hv[4] | ((uint32_t)hv[5] << 16), hv[6] | ((uint32_t)hv[7] << 16));
+        }
+      }
+    }
+    const uint32_t a[4] = {x[0].x, x[0].y, x[0].z, x[0].w}, bb[4] = {x[1].x, x[1].y, x[1].z, x[1].w};
+    const int sw = p ^ (4 * v);  // tile columns 8v .. 8v + 7: swz = 4 * (column >> 3) = 4v
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      tw[8 * v + 2 * j][sw] = pair_lo(a[j], bb[j]);
+      tw[8 * v + 2 * j + 1][sw] = pair_hi(a[j], bb[j]);
+    }
   }
   __syncthreads();
 #pragma unroll
   for (int pass = 0; pass < 2; ++pass) {
-    const int kl = (threadIdx.x >> 3) + 32 * pass, v8 = threadIdx.x & 7;
-    const int64_t k = k0 + kl, r = r0 + 8 * v8;
-    if (k < K && r < Rp)
-      *reinterpret_cast<uint4*>(out + k * Rp + r) = *reinterpret_cast<const uint4*>(&tile[kl][8 * v8]);
+    const int cc = (threadIdx.x >> 3) + 32 * pass, u = threadIdx.x & 7;
+    const int64_t c = c0 + cc, r = r0 + 8 * u;
+    if (c < cols && r < rows_p)
+      *reinterpret_cast<uint4*>(dst + c * rows_p + r) = *reinterpret_cast<const uint4*>(&tw[cc][4 * (u ^ (cc >> 3))]);
   }
 }
 
-// bf16 [rows, cols] (row pitch `spitch`) -> dst, zero-padded: kTranspose:
-// dst^T [cols, rows_p] (dst[c * rows_p + r]); else a copy [rows, cols_p].
-// rows_p / cols_p % 8 == 0.  64 x 64 tiles through shared memory.
-template <bool kTranspose>
+// bf16 [rows, cols] (row pitch `spitch`) -> dst [rows, cols_p], columns
+// cols .. cols_p - 1 zero; cols_p % 8 == 0 (a copy of dY whose rows are not
+// 16-byte aligned).  64 x 64 tiles through shared memory.
 __global__ void __launch_bounds__(kThreads)
-transpose_bf16_kernel(const __nv_bfloat16* __restrict__ src, int64_t rows, int64_t cols, int64_t spitch,
-                      __nv_bfloat16* __restrict__ dst, int64_t dpad) {
+pad_copy_bf16_kernel(const __nv_bfloat16* __restrict__ src, int64_t rows, int64_t cols, int64_t spitch,
+                     __nv_bfloat16* __restrict__ dst, int64_t cols_p) {
   __shared__ __align__(16) __nv_bfloat16 tile[kTile][kTilePitch];
   griddep_wait();
   const int64_t r0 = (int64_t)blockIdx.x * kTile, c0 = (int64_t)blockIdx.y * kTile;
@@ -112,20 +190,15 @@ transpose_bf16_kernel(const __nv_bfloat16* __restrict__ src, int64_t rows, int64
   for (int i = threadIdx.x; i < kTile * kTile; i += kThreads) {  // coalesced along the source row
     const int rl = i >> 6, cl = i & 63;
     const int64_t r = r0 + rl, c = c0 + cl;
-    const __nv_bfloat16 v = (r < rows && c < cols) ? src[r * spitch + c] : zero;
-    if (kTranspose) tile[cl][rl] = v;
-    else tile[rl][cl] = v;
+    tile[rl][cl] = (r < rows && c < cols) ? src[r * spitch + c] : zero;
   }
   __syncthreads();
-  // 64 destination rows of 8 16-byte pieces
-  const int64_t d_rows = kTranspose ? cols : rows, d_cols = dpad;
-  const int64_t dr0 = kTranspose ? c0 : r0, dc0 = kTranspose ? r0 : c0;
 #pragma unroll
-  for (int pass = 0; pass < 2; ++pass) {
+  for (int pass = 0; pass < 2; ++pass) {  // 64 destination rows of 8 16-byte pieces
     const int rl = (threadIdx.x >> 3) + 32 * pass, v8 = threadIdx.x & 7;
-    const int64_t r = dr0 + rl, c = dc0 + 8 * v8;
-    if (r < d_rows && c < d_cols)
-      *reinterpret_cast<uint4*>(dst + r * d_cols + c) = *reinterpret_cast<const uint4*>(&tile[rl][8 * v8]);
+    const int64_t r = r0 + rl, c = c0 + 8 * v8;
+    if (r < rows && c < cols_p)
+      *reinterpret_cast<uint4*>(dst + r * cols_p + c) = *reinterpret_cast<const uint4*>(&tile[rl][8 * v8]);
   }
 }
 
@@ -181,7 +254,7 @@ cudaError_t qat_backward(const void* dy, int64_t M, const uint8_t* w_codes, cons
   cudaError_t err;
   if (dx != nullptr) {
     // dX [M, K] = dY [M, N] . W_hat^T [K, N]: reduced over N
-    cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)((N + kTile - 1) / kTile), (unsigned)((K + kTile - 1) / kTile)),
+    cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)((N + kTile - 1) / kTile), (unsigned)((K + kDqK - 1) / kDqK)),
                                         stream, attr);
     if ((err = cudaLaunchKernelEx(&cfg, dequant_bf16_t_kernel, w_codes, w_smma, w_ts, N, K, Np, wt)) != cudaSuccess)
       return err;
@@ -189,7 +262,7 @@ cudaError_t qat_backward(const void* dy, int64_t M, const uint8_t* w_codes, cons
     int64_t pitch = N;
     if (N % 8 != 0) {  // rows of dY are not 16-byte aligned: a zero-padded copy [M, Np]
       cfg = pdl_config(dim3((unsigned)((M + kTile - 1) / kTile), (unsigned)((N + kTile - 1) / kTile)), stream, attr);
-      if ((err = cudaLaunchKernelEx(&cfg, transpose_bf16_kernel<false>, dyb, M, N, N, dyp, Np)) != cudaSuccess)
+      if ((err = cudaLaunchKernelEx(&cfg, pad_copy_bf16_kernel, dyb, M, N, N, dyp, Np)) != cudaSuccess)
         return err;
       a = dyp;
       pitch = Np;
@@ -198,12 +271,12 @@ cudaError_t qat_backward(const void* dy, int64_t M, const uint8_t* w_codes, cons
   }
   if (dw != nullptr) {
     // dW [N, K] = dY^T [N, Mp] . X_hat^T [K, Mp]: reduced over M
-    cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)((M + kTile - 1) / kTile), (unsigned)((K + kTile - 1) / kTile)),
+    cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)((M + kTile - 1) / kTile), (unsigned)((K + kDqK - 1) / kDqK)),
                                         stream, attr);
     if ((err = cudaLaunchKernelEx(&cfg, dequant_bf16_t_kernel, a_codes, a_smma, a_ts, M, K, Mp, xt)) != cudaSuccess)
       return err;
     cfg = pdl_config(dim3((unsigned)((M + kTile - 1) / kTile), (unsigned)((N + kTile - 1) / kTile)), stream, attr);
-    if ((err = cudaLaunchKernelEx(&cfg, transpose_bf16_kernel<true>, dyb, M, N, N, dyt, Mp)) != cudaSuccess)
+    if ((err = cudaLaunchKernelEx(&cfg, transpose_t_kernel, dyb, M, N, N, dyt, Mp)) != cudaSuccess)
       return err;
     if ((err = launch_gemm_bf16_tn(dyt, Mp, xt, Mp, N, K, M, dw, true, status, stream)) != cudaSuccess) return err;
   }
