@@ -29,10 +29,15 @@ constexpr int kTilePitch = 72;   // bf16 per shared-memory tile row (16-byte ali
 
 // value(code) * value(scale) is exact in binary32 (at most 2 + 4 significant
 // bits); times the tensor scale rounded once; then rounded to bf16 (reading
-// R18 of the design notes).
+// R18 of the design notes).  No integer-to-float conversion: the code's
+// magnitude bits placed at binary32 bits 24:22 and its sign at bit 31 read as
+// value(code) * 2^-126 exactly (0.5 lands in the subnormal range, and a
+// negative zero code gives -0).  Its product with the E4M3 scale is exact too
+// (at most 6 significant bits, none below 2^-141), and the product times
+// 2^126 is exactly value(code) * value(scale).
 __device__ __forceinline__ float dequant_value(uint32_t code, float s, float ts) {
-  const float mag = e2m1_mag_to_f32(code & 7u);
-  return __fmul_rn(__fmul_rn(code & 8u ? -mag : mag, s), ts);
+  const float v = __uint_as_float(((code & 7u) << 22) | ((code & 8u) << 28));
+  return __fmul_rn(__fmul_rn(__fmul_rn(v, s), 0x1p126f), ts);
 }
 
 // One 16-element block per thread and step: 8 code bytes in, 32 bytes out.
@@ -77,11 +82,13 @@ __device__ __forceinline__ uint32_t bf16_bits(float v) {
 }
 
 // NVFP4 [R, K] -> bf16 out^T [K, Rp] (out[k * Rp + r]), columns R .. Rp - 1
-// zero; Rp % 8 == 0.  A CTA covers 64 rows x 128 K positions: thread (p, b)
-// dequantises 16-element block b of rows 2p and 2p + 1, the tile is staged
-// transposed as described above, and the CTA writes 128 output rows of 128
-// bytes with 16-byte stores.
-constexpr int kDqK = 128;  // K positions per CTA
+// zero; Rp % 8 == 0.  A CTA covers 64 rows x 256 K positions: thread (p, q)
+// dequantises 16-element blocks 2q and 2q + 1 of rows 2p and 2p + 1 (one
+// 16-byte code load per row; the 8 threads of a row pair read its 128 code
+// bytes contiguously), the tile is staged transposed as described above (here
+// swz(c) = 4 * ((c / 32) % 8), the block pair of tile column c), and the CTA
+// writes 256 output rows of 128 bytes with 16-byte stores.
+constexpr int kDqK = 256;  // K positions per CTA
 __global__ void __launch_bounds__(kThreads)
 dequant_bf16_t_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ smma,
                       const float* __restrict__ ts_ptr, int64_t R, int64_t K, int64_t Rp,
@@ -92,28 +99,44 @@ dequant_bf16_t_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restri
   const int64_t kb = K / 16, ct = (kb + 3) / 4;
   const int64_t r0 = (int64_t)blockIdx.x * kTile, k0 = (int64_t)blockIdx.y * kDqK;
   {
-    const int p = threadIdx.x & 31, b = threadIdx.x >> 5;  // row pair, 16-block of the tile
-    const int64_t c = k0 / 16 + b;
-    uint32_t h[2][16];
+    const int q = threadIdx.x & 7, p = threadIdx.x >> 3;  // block pair, row pair of the tile
+    const int64_t c = k0 / 16 + 2 * q;                     // first of the two blocks
+    uint32_t w[2][16];  // [block][element]: the bf16 pair of rows 2p, 2p + 1
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+      for (int j = 0; j < 16; ++j) w[blk][j] = 0u;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int64_t r = r0 + 2 * p + e;
       if (r < R && c < kb) {
-        const uint2 cw = *reinterpret_cast<const uint2*>(codes + r * (K / 2) + 8 * c);
-        const float s = e4m3_to_f32(smma[scale_mma_offset(r, c, ct)]);
+        const uint8_t* row = codes + r * (K / 2) + 8 * c;
+        uint2 cw[2];
+        if (c + 1 < kb && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+          const uint4 v = *reinterpret_cast<const uint4*>(row);
+          cw[0] = make_uint2(v.x, v.y);
+          cw[1] = make_uint2(v.z, v.w);
+        } else {
+          cw[0] = *reinterpret_cast<const uint2*>(row);
+          cw[1] = c + 1 < kb ? *reinterpret_cast<const uint2*>(row + 8) : make_uint2(0u, 0u);
+        }
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          h[e][j] = bf16_bits(dequant_value(((j < 8 ? cw.x : cw.y) >> (4 * (j & 7))) & 15u, s, ts));
-      } else {
+        for (int blk = 0; blk < 2; ++blk) {
+          if (c + blk < kb) {
+            const float s = e4m3_to_f32(smma[scale_mma_offset(r, c + blk, ct)]);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) h[e][j] = 0u;
+            for (int j = 0; j < 16; ++j)
+              w[blk][j] |= bf16_bits(dequant_value(((j < 8 ? cw[blk].x : cw[blk].y) >> (4 * (j & 7))) & 15u, s, ts))
+                           << (16 * e);
+          }
+        }
       }
     }
+    const int sw = p ^ (4 * q);  // tile columns 32q .. 32q + 31
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int cc = 16 * b + j;
-      tw[cc][p ^ (4 * (cc & 7))] = h[0][j] | (h[1][j] << 16);
-    }
+    for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+      for (int j = 0; j < 16; ++j) tw[32 * q + 16 * blk + j][sw] = w[blk][j];
   }
   __syncthreads();
 #pragma unroll
@@ -121,7 +144,8 @@ dequant_bf16_t_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restri
     const int cc = (threadIdx.x >> 3) + 32 * pass, u = threadIdx.x & 7;
     const int64_t k = k0 + cc, r = r0 + 8 * u;
     if (k < K && r < Rp)
-      *reinterpret_cast<uint4*>(out + k * Rp + r) = *reinterpret_cast<const uint4*>(&tw[cc][4 * (u ^ (cc & 7))]);
+      *reinterpret_cast<uint4*>(out + k * Rp + r) =
+          *reinterpret_cast<const uint4*>(&tw[cc][4 * (u ^ ((cc >> 5) & 7))]);
   }
 }
 
