@@ -832,6 +832,48 @@ w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
           }
         }
+      } else if (kF32 && tma_store) {
+        // fp32 rows leave through the staging buffer as well: four rounds of
+        // 64 columns, each two 128 x 32 fp32 boxes (128-byte rows, 128-byte
+        // swizzle) written by TMA stores that clip rows and columns outside
+        // Y; the accumulator goes back once the last round's columns are in
+        // registers.
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+          asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");  // staging buffer free
+          uint32_t v0[32], v1[32];
+          tmem_ld_32x32b_x32(acc + 64 * q, v0);
+          tmem_ld_32x32b_x32(acc + 64 * q + 32, v1);
+          tmem_wait_ld();
+          if (q == 3) {
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(&sm.acc_free[b], lead);
+          }
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint32_t* v = j == 0 ? v0 : v1;
+            uint8_t* box = sm.ystage + j * (BM * 128) + r * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              *reinterpret_cast<float4*>(box + ((u ^ (r & 7)) << 4)) =
+                  make_float4(__uint_as_float(v[4 * u]) * alpha, __uint_as_float(v[4 * u + 1]) * alpha,
+                              __uint_as_float(v[4 * u + 2]) * alpha, __uint_as_float(v[4 * u + 3]) * alpha);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+          if (threadIdx.x == 0 && m0 < M) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              if (n0 + 64 * q + 32 * j < N)
+                asm volatile(
+                    "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(&tmap_y),
+                    "r"((int)(n0 + 64 * q + 32 * j)), "r"((int)m0), "r"(smem_addr(sm.ystage + j * (BM * 128)))
+                    : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          }
+        }
       } else {
 #pragma unroll 1
         for (int c = 0; c < 8; c += 2) {  // two loads in flight per wait
@@ -910,14 +952,17 @@ bool make_map_pitch(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 
 // Y as bf16 [M, N] for TMA stores: boxes of 128 rows x 64 columns (128
 // bytes), 128-byte swizzle.
-bool make_y_map(CUtensorMap* map, void* y, uint64_t M, uint64_t N) {
+// The output map for TMA stores: boxes of 128 rows x 128 bytes (64 bf16 or
+// 32 fp32), 128-byte swizzle.  Rows of Y must be 16-byte aligned.
+bool make_y_map(CUtensorMap* map, void* y, uint64_t M, uint64_t N, bool f32 = false) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
   cuuint64_t dims[2] = {N, M};
-  cuuint64_t strides[1] = {N * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)BM};
+  cuuint64_t strides[1] = {N * (f32 ? 4 : 2)};
+  cuuint32_t box[2] = {f32 ? 32u : 64u, (cuuint32_t)BM};
   cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  return enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -969,9 +1014,11 @@ cudaError_t launch_pairs(const uint8_t* a_codes, const uint8_t* a_smma, const fl
       !make_map(&mb, w_codes, (uint64_t)N, (uint64_t)K / 2, 128))
     return cudaErrorInvalidValue;
   const int64_t n_out = kGateUp ? N / 2 : N;  // columns of Y
-  int tma_store = (!out_f32 && n_out % 8 == 0) ? 1 : 0;
+  // TMA stores of the output: rows of Y 16-byte aligned (fp32 as well, except
+  // for the gate/up epilogue, which writes bf16 only)
+  int tma_store = (out_f32 ? (!kGateUp && n_out % 4 == 0) : n_out % 8 == 0) ? 1 : 0;
   memset(&my, 0, sizeof my);
-  if (tma_store && !make_y_map(&my, y, (uint64_t)M, (uint64_t)n_out)) tma_store = 0;
+  if (tma_store && !make_y_map(&my, y, (uint64_t)M, (uint64_t)n_out, out_f32)) tma_store = 0;
   if (kGateUp && !tma_store) return cudaErrorNotSupported;
   const size_t smem = sizeof(PairSmem) + 1024;
   auto kern = out_f32 ? w4a4_pair_kernel<true> : w4a4_pair_kernel<false>;
@@ -1025,9 +1072,9 @@ cudaError_t launch_gemm_bf16_tn(const void* a, int64_t pitch_a, const void* b, i
   if (!make_map_pitch(&ma, a, (uint64_t)rows_a, (uint64_t)red * 2, (uint64_t)pitch_a * 2) ||
       !make_map_pitch(&mb, b, (uint64_t)rows_b, (uint64_t)red * 2, (uint64_t)pitch_b * 2))
     return cudaErrorInvalidValue;
-  int tma_store = (!out_f32 && rows_b % 8 == 0) ? 1 : 0;
+  int tma_store = (out_f32 ? rows_b % 4 == 0 : rows_b % 8 == 0) ? 1 : 0;
   memset(&my, 0, sizeof my);
-  if (tma_store && !make_y_map(&my, y, (uint64_t)rows_a, (uint64_t)rows_b)) tma_store = 0;
+  if (tma_store && !make_y_map(&my, y, (uint64_t)rows_a, (uint64_t)rows_b, out_f32)) tma_store = 0;
   const size_t smem = sizeof(PairSmem) + 1024;
   auto kern = out_f32 ? w4a4_pair_kernel<true, false, true> : w4a4_pair_kernel<false, false, true>;
   cudaLaunchAttribute attr[2];
