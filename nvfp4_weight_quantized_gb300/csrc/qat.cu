@@ -35,9 +35,30 @@ constexpr int kTilePitch = 72;   // bf16 per shared-memory tile row (16-byte ali
 // negative zero code gives -0).  Its product with the E4M3 scale is exact too
 // (at most 6 significant bits, none below 2^-141), and the product times
 // 2^126 is exactly value(code) * value(scale).
+__device__ __forceinline__ float code_bits(uint32_t code) {
+  return __uint_as_float(((code & 7u) << 22) | ((code & 8u) << 28));  // value(code) * 2^-126
+}
+
 __device__ __forceinline__ float dequant_value(uint32_t code, float s, float ts) {
-  const float v = __uint_as_float(((code & 7u) << 22) | ((code & 8u) << 28));
-  return __fmul_rn(__fmul_rn(__fmul_rn(v, s), 0x1p126f), ts);
+  return __fmul_rn(__fmul_rn(__fmul_rn(code_bits(code), s), 0x1p126f), ts);
+}
+
+// packed binary32 pairs (lo in the low word)
+__device__ __forceinline__ unsigned long long pack_f2(float lo, float hi) {
+  unsigned long long d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ unsigned long long mul_f2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// both halves rounded to bf16 (round to nearest even): lo -> bits 15:0
+__device__ __forceinline__ uint32_t bf16x2_of(unsigned long long v) {
+  uint32_t d;
+  asm("{\n\t.reg .f32 a, b;\n\tmov.b64 {a, b}, %1;\n\tcvt.rn.bf16x2.f32 %0, b, a;\n\t}" : "=r"(d) : "l"(v));
+  return d;
 }
 
 // One 16-element block per thread and step: 8 code bytes in, 32 bytes out.
@@ -76,11 +97,6 @@ constexpr int kPairWords = kTile / 2;  // words per staged tile row (64 source r
 __device__ __forceinline__ uint32_t pair_lo(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x5410u); }
 __device__ __forceinline__ uint32_t pair_hi(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x7632u); }
 
-__device__ __forceinline__ uint32_t bf16_bits(float v) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(v);
-  return (uint32_t)*reinterpret_cast<const uint16_t*>(&h);
-}
-
 // NVFP4 [R, K] -> bf16 out^T [K, Rp] (out[k * Rp + r]), columns R .. Rp - 1
 // zero; Rp % 8 == 0.  A CTA covers 64 rows x 256 K positions: thread (p, q)
 // dequantises 16-element blocks 2q and 2q + 1 of rows 2p and 2p + 1 (one
@@ -101,35 +117,47 @@ dequant_bf16_t_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restri
   {
     const int q = threadIdx.x & 7, p = threadIdx.x >> 3;  // block pair, row pair of the tile
     const int64_t c = k0 / 16 + 2 * q;                     // first of the two blocks
-    uint32_t w[2][16];  // [block][element]: the bf16 pair of rows 2p, 2p + 1
-#pragma unroll
-    for (int blk = 0; blk < 2; ++blk)
-#pragma unroll
-      for (int j = 0; j < 16; ++j) w[blk][j] = 0u;
+    // codes and scales of blocks c, c + 1 of rows 2p (e = 0) and 2p + 1;
+    // zero codes and scales outside the matrix give +0
+    uint2 cw[2][2];
+    float sc[2][2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int64_t r = r0 + 2 * p + e;
+#pragma unroll
+      for (int blk = 0; blk < 2; ++blk) {
+        cw[e][blk] = make_uint2(0u, 0u);
+        sc[e][blk] = 0.0f;
+      }
       if (r < R && c < kb) {
         const uint8_t* row = codes + r * (K / 2) + 8 * c;
-        uint2 cw[2];
         if (c + 1 < kb && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
           const uint4 v = *reinterpret_cast<const uint4*>(row);
-          cw[0] = make_uint2(v.x, v.y);
-          cw[1] = make_uint2(v.z, v.w);
+          cw[e][0] = make_uint2(v.x, v.y);
+          cw[e][1] = make_uint2(v.z, v.w);
         } else {
-          cw[0] = *reinterpret_cast<const uint2*>(row);
-          cw[1] = c + 1 < kb ? *reinterpret_cast<const uint2*>(row + 8) : make_uint2(0u, 0u);
+          cw[e][0] = *reinterpret_cast<const uint2*>(row);
+          if (c + 1 < kb) cw[e][1] = *reinterpret_cast<const uint2*>(row + 8);
         }
 #pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-          if (c + blk < kb) {
-            const float s = e4m3_to_f32(smma[scale_mma_offset(r, c + blk, ct)]);
+        for (int blk = 0; blk < 2; ++blk)
+          if (c + blk < kb) sc[e][blk] = e4m3_to_f32(smma[scale_mma_offset(r, c + blk, ct)]);
+      }
+    }
+    // word j of block blk: the bf16 pair (row 2p, row 2p + 1) of element j,
+    // both values formed as in dequant_value by packed binary32 multiplies
+    // (each lane rounded as the scalar multiply rounds it)
+    uint32_t w[2][16];
+    const unsigned long long two126 = pack_f2(0x1p126f, 0x1p126f), ts2 = pack_f2(ts, ts);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              w[blk][j] |= bf16_bits(dequant_value(((j < 8 ? cw[blk].x : cw[blk].y) >> (4 * (j & 7))) & 15u, s, ts))
-                           << (16 * e);
-          }
-        }
+    for (int blk = 0; blk < 2; ++blk) {
+      const unsigned long long s2 = pack_f2(sc[0][blk], sc[1][blk]);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t n0 = ((j < 8 ? cw[0][blk].x : cw[0][blk].y) >> (4 * (j & 7))) & 15u;
+        const uint32_t n1 = ((j < 8 ? cw[1][blk].x : cw[1][blk].y) >> (4 * (j & 7))) & 15u;
+        const unsigned long long v2 = pack_f2(code_bits(n0), code_bits(n1));
+        w[blk][j] = bf16x2_of(mul_f2(mul_f2(mul_f2(v2, s2), two126), ts2));
       }
     }
     const int sw = p ^ (4 * q);  // tile columns 32q .. 32q + 31
