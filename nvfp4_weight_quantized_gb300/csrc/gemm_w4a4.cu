@@ -1138,9 +1138,18 @@ cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma
                              cudaStream_t stream) {
   if (M <= 0) return cudaSuccess;
   if (K < BK || K % 64 != 0 || M > INT32_MAX || N > INT32_MAX) return cudaErrorNotSupported;
-  if (M <= BM)
-    return launch_bn<64>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, out_f32, status,
-                         num_sms, stream);
+  if (M <= BM) {
+    // one CTA per weight tile, the narrowest tile (64, 128 or 256 rows) whose
+    // tiles fit one wave: each CTA streams one tile's rows
+    if ((N + 63) / 64 <= num_sms)
+      return launch_bn<64>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, out_f32, status,
+                           num_sms, stream);
+    if ((N + 127) / 128 <= num_sms)
+      return launch_bn<128>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, out_f32, status,
+                            num_sms, stream);
+    return launch_bn<256>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, out_f32, status,
+                          num_sms, stream);
+  }
   const int ctas = w4a4_get_cluster_ctas();
   cudaError_t err = cudaErrorNotSupported;
   if (ctas == 2)
