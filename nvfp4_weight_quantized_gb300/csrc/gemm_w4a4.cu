@@ -18,8 +18,10 @@
 //                        else (an MMA stream is bound by its issuer's latency);
 //   warps 0-3         -- epilogue: tcgen05.ld of the accumulator, scale by
 //                        ts_a * ts_w, convert, store, release the accumulator.
-// BN = 256 for large M; BN = 64 when M fits one tile so that a skinny GEMM
-// still spreads over every SM.  Every mbarrier wait is bounded; a wait that
+// BN = 256 for large M.  When M fits one tile, the narrowest weight tile
+// (64, 128 or 256 rows) whose tiles fit one wave of CTAs: a skinny GEMM
+// spreads over the SMs, and no SM streams a second tile after the others have
+// finished (64-row tiles on W[11008, 4096] took two waves and 1.4x as long).  Every mbarrier wait is bounded; a wait that
 // runs out sets the library's status word (NVFP4_ERR_TIMEOUT) and the CTA
 // winds down.
 #include <cuda.h>
