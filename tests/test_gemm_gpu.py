@@ -233,6 +233,21 @@ def test_w4a4_small(shape, M):
     run_w4a4(x, wref, K, nv.OUT_BF16)
 
 
+@pytest.mark.parametrize("N", [9768, 19528])
+@pytest.mark.parametrize("M", [1, 37, 128])
+def test_w4a4_narrow_tiles_ragged(N, M):
+    """M <= 128 runs one CTA per weight tile with the narrowest tile (64, 128
+    or 256 rows) whose tiles fit one wave; on a 152-SM GB300 these N take 128-
+    and 256-row tiles, each with a partial last tile (40 and 72 rows; the
+    256-row one has no rows in its second 128-row scale tile)."""
+    K = 256
+    wref = oracle_weight(synth.weight_normal(N, K, seed=N + 7, outlier_frac=0.01))
+    x = synth.act_student_t(M, K, seed=M + 3000)
+    run_w4a4(x, wref, K, nv.OUT_F32)
+    run_w4a4(x, wref, K, nv.OUT_BF16)
+    assert nv.nvfp4_get_device_status() == 0
+
+
 def each_w4a4_kernel(fn):
     """Runs fn() with each W4A4 kernel for M > 128 forced in turn: CTA pairs,
     single CTAs (M <= 128 has one kernel)."""
