@@ -406,10 +406,11 @@ nvfp4_status nvfp4_linear_silu_mul(const void* X, int64_t M, const nvfp4_weight*
   st = quantize_common(X, M, K, NVFP4_DEFAULT_DIVISOR, g_act_fos.load(std::memory_order_relaxed), a_codes, nullptr,
                        a_smma, a_ts, nullptr, nullptr, ws + l.quant_off, l.total - l.quant_off, stream);
   if (st != NVFP4_OK) return st;
-  if (!f32 && M > 128 && nvfp4::w4a4_get_cluster_ctas() >= 2) {
-    // silu(G) * U in the epilogue of the CTA-pair kernel
+  if (!f32) {
+    // silu(G) * U in the epilogue of the W4A4 kernel (CTA pairs above 128
+    // tokens, single CTAs otherwise)
     err = nvfp4::launch_gemm_w4a4_gate_up(a_codes, a_smma, a_ts, M, W->codes, W->scales_mma, W->tensor_scale, N, K,
-                                          Y, d->status, stream);
+                                          Y, d->status, d->num_sms, stream);
     if (err == cudaSuccess) return NVFP4_OK;
     if (err != cudaErrorNotSupported) return fail_cuda(err, "gemm_w4a4 gate/up launch");
   }

@@ -140,7 +140,12 @@ __device__ __forceinline__ void store_row32(void* y, int64_t row_off, int64_t n,
   }
 }
 
-template <int BN, bool kF32>
+// kGateUp (BN = 256, bf16 output): W is a gated-MLP input projection [2F, K]
+// (rows [0, F) gate, [F, 2F) up, F % 128 == 0); a tile covers 128 features,
+// its B stage holding their gate rows (first 128 rows) and up rows (last 128),
+// so accumulator column j < 128 of a row holds G[m, f0 + j] and column 128 + j
+// holds U[m, f0 + j], and the epilogue writes silu(G) * U for F features.
+template <int BN, bool kF32, bool kGateUp = false>
 __global__ void __launch_bounds__(kThreads, 1)
 w4a4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
             const __grid_constant__ CUtensorMap tmap_y, int tma_store, const uint8_t* __restrict__ a_smma, const uint8_t* __restrict__ b_smma,
@@ -154,7 +159,9 @@ w4a4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   const int kb64 = (int)(K / 64);                 // 64-wide K blocks = scale column tiles per row tile
   const int kt = (kb64 + 3) / 4;                  // K stages per tile
   const int64_t b_row_tiles = (N + 127) / 128;    // row tiles present in the weight scale tiling
-  const int64_t m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN - 1) / BN;
+  static_assert(!kGateUp || (BN == 256 && !kF32), "gate/up epilogue: 256-row tiles, bf16 output");
+  const int64_t F = N / 2;                        // features of a gate/up weight
+  const int64_t m_tiles = (M + BM - 1) / BM, n_tiles = kGateUp ? F / 128 : (N + BN - 1) / BN;
   const int64_t n_work = m_tiles * n_tiles;
 
   if (warp == kProducerWarp && lane == 0) {
@@ -183,9 +190,9 @@ w4a4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       int g = 0;       // stage counter across this CTA's tiles
       for (int64_t w = blockIdx.x; w < n_work && !failed; w += gridDim.x) {
         const int64_t m_tile = w / n_tiles, n_tile = w - m_tile * n_tiles;
-        const int64_t n0 = n_tile * BN;
+        const int64_t n0 = n_tile * (kGateUp ? 128 : BN);
         const int64_t sfb_left = b_row_tiles - n0 / 128;
-        const int nsfb = sfb_left < C::kSfbTiles ? (int)sfb_left : C::kSfbTiles;
+        const int nsfb = kGateUp ? 2 : sfb_left < C::kSfbTiles ? (int)sfb_left : C::kSfbTiles;
         for (int ks = 0; ks < kt; ++ks, ++g) {
           const int s = g % kStages;
           if (g >= kStages && !mbar_wait(&sm.empty[s], (uint32_t)(g / kStages - 1) & 1u)) {
@@ -197,10 +204,16 @@ w4a4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
           mbar_arrive_expect_tx(&sm.full[s], kABytes + C::kBBytes + sf_bytes * (1 + nsfb));
           tma_load_2d(sm.a[s], &tmap_a, ks * (BK / 2), (int)(m_tile * BM), &sm.full[s]);
           tma_load_2d(sm.b[s], &tmap_b, ks * (BK / 2), (int)n0, &sm.full[s]);
+          if (kGateUp)  // the up rows of the same features (the B map's box is 128 rows here)
+            tma_load_2d(sm.b[s] + C::kBBytes / 2, &tmap_b, ks * (BK / 2), (int)(F + n0), &sm.full[s]);
           bulk_load(sm.sfa[s], a_smma + (m_tile * kb64 + 4 * ks) * kScaleTileBytes, sf_bytes, &sm.full[s]);
-          for (int rt = 0; rt < nsfb; ++rt)
-            bulk_load(sm.sfb[s] + rt * (BK / 64) * kScaleTileBytes,
-                      b_smma + ((n0 / 128 + rt) * kb64 + 4 * ks) * kScaleTileBytes, sf_bytes, &sm.full[s]);
+          for (int rt = 0; rt < nsfb; ++rt) {
+            // scale tile of B rows 128 rt ..: the next weight row tile, or for
+            // gate/up the up rows' tile F / 128 further on
+            const int64_t bt = kGateUp ? (n0 + F * rt) / 128 : n0 / 128 + rt;
+            bulk_load(sm.sfb[s] + rt * (BK / 64) * kScaleTileBytes, b_smma + (bt * kb64 + 4 * ks) * kScaleTileBytes,
+                      sf_bytes, &sm.full[s]);
+          }
         }
       }
       // let every load this thread issued land before the CTA can exit
@@ -324,7 +337,56 @@ w4a4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         break;
       }
       fence_after_sync();
-      if (BN <= 64) {
+      if (kGateUp) {
+        // silu(G) * U for features f0 .. f0 + 127 straight into the staging
+        // buffer (two 128 x 64 bf16 boxes, 128-byte swizzle), then the
+        // accumulator goes back and two TMA stores (clipping rows past M)
+        // write the tile -- the arithmetic of the pair kernel's gate/up
+        // epilogue
+        const int r = warp * 32 + lane;  // tile row = TMEM lane
+        const uint32_t acc = tmem + lane_base + C::kAccCol;
+        if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");  // staging buffer free
+#pragma unroll 1
+        for (int c2 = 0; c2 < 4; ++c2) {  // 32 features per step: chunks 2 c2, 2 c2 + 1 of 16
+          uint32_t vg[32], vu[32];
+          tmem_ld_32x32b_x32(acc + 32 * c2, vg);
+          tmem_ld_32x32b_x32(acc + 128 + 32 * c2, vu);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int c = 2 * c2 + h;
+            uint32_t p[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int j = 16 * h + 2 * i;
+              p[i] = bf16x2_rn(silu_mul(__uint_as_float(vg[j]) * alpha, __uint_as_float(vu[j]) * alpha),
+                               silu_mul(__uint_as_float(vg[j + 1]) * alpha, __uint_as_float(vu[j + 1]) * alpha));
+            }
+            uint8_t* box = sm.ystage + (c >> 2) * (BM * 128) + r * 128;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int unit = ((c & 3) * 2 + u) ^ (r & 7);
+              *reinterpret_cast<uint4*>(box + unit * 16) =
+                  make_uint4(p[4 * u], p[4 * u + 1], p[4 * u + 2], p[4 * u + 3]);
+            }
+          }
+        }
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.acc_free);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+        if (threadIdx.x == 0) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            asm volatile(
+                "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(&tmap_y),
+                "r"((int)(n_tile * 128 + 64 * j)), "r"((int)(m_tile * BM)), "r"(smem_addr(sm.ystage + j * (BM * 128)))
+                : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+      } else if (BN <= 64) {
         // small tile: drain it all, hand the accumulator back, then store
         uint32_t v[BN / 32][32];
 #pragma unroll
@@ -1120,11 +1182,36 @@ cudaError_t launch_gemm_bf16_tn(const void* a, int64_t pitch_a, const void* b, i
 cudaError_t launch_gemm_w4a4_gate_up(const uint8_t* a_codes, const uint8_t* a_scales_mma, const float* a_ts,
                                      int64_t M, const uint8_t* w_codes, const uint8_t* w_scales_mma,
                                      const float* w_ts, int64_t N, int64_t K, void* y, unsigned int* status,
-                                     cudaStream_t stream) {
+                                     int num_sms, cudaStream_t stream) {
   if (M <= 0) return cudaSuccess;
   if (N % 256 != 0 || K < BK || K % 64 != 0 || M > INT32_MAX || N > INT32_MAX) return cudaErrorNotSupported;
-  return launch_pairs<true>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, false, status,
-                               stream);
+  if (M > BM && w4a4_get_cluster_ctas() >= 2)
+    return launch_pairs<true>(a_codes, a_scales_mma, a_ts, M, w_codes, w_scales_mma, w_ts, N, K, y, false, status,
+                              stream);
+  // single CTAs, one per 128-feature tile (256 weight rows: gate, then up)
+  const int64_t F = N / 2;
+  CUtensorMap ma, mb, my;
+  if (!make_map(&ma, a_codes, (uint64_t)M, (uint64_t)K / 2, BM) ||
+      !make_map(&mb, w_codes, (uint64_t)N, (uint64_t)K / 2, 128))
+    return cudaErrorInvalidValue;
+  memset(&my, 0, sizeof my);
+  if (!make_y_map(&my, y, (uint64_t)M, (uint64_t)F)) return cudaErrorNotSupported;
+  const size_t smem = std::max<size_t>(sizeof(Smem<256>) + 1024, 120u * 1024u);  // one CTA per SM (see launch_bn)
+  auto kern = w4a4_kernel<256, false, true>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  const int64_t work = ((M + BM - 1) / BM) * (F / 128);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::min<int64_t>(work, num_sms));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, ma, mb, my, 1, a_scales_mma, w_scales_mma, a_ts, w_ts, M, N, K, y, status);
 }
 
 bool w4a4_set_cluster_ctas(int ctas) {

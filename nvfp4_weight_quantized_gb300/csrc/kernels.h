@@ -72,13 +72,14 @@ cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales_mma
                              int64_t M, const uint8_t* w_codes, const uint8_t* w_scales_mma,
                              const float* w_ts, int64_t N, int64_t K, void* y, bool out_f32,
                              unsigned int* status, int num_sms, cudaStream_t stream);
-// W4A4 on a gate/up weight [2F, K] with silu(G) * U applied in the epilogue
-// of the CTA-pair kernel: Y bf16 [M, F].  cudaErrorNotSupported unless
-// F % 128 == 0 and a pair of CTAs can be resident.
+// W4A4 on a gate/up weight [2F, K] with silu(G) * U applied in the GEMM's
+// epilogue: Y bf16 [M, F].  CTA pairs above 128 tokens (when pairs are
+// enabled), single CTAs otherwise.  cudaErrorNotSupported unless
+// F % 128 == 0 and the kernel can be resident.
 cudaError_t launch_gemm_w4a4_gate_up(const uint8_t* a_codes, const uint8_t* a_scales_mma, const float* a_ts,
                                      int64_t M, const uint8_t* w_codes, const uint8_t* w_scales_mma,
                                      const float* w_ts, int64_t N, int64_t K, void* y, unsigned int* status,
-                                     cudaStream_t stream);
+                                     int num_sms, cudaStream_t stream);
 // Y [rows_a, rows_b] (bf16, or fp32 when out_f32) = A B^T for bf16 A
 // [rows_a, red] and B [rows_b, red] whose rows are pitch_a / pitch_b elements
 // apart (multiples of 8), on the CTA-pair tensor-core kernel (tcgen05

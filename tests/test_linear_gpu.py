@@ -117,9 +117,10 @@ def _gate_up_refs(x, wref, path_w4a4, m_rows=None):
 @pytest.mark.parametrize("F", [256, 384, 200])
 def test_linear_silu_mul(F):
     """Gated MLP projection against the oracle on both paths: W4A16 (M <= 40)
-    with the separate silu kernel, W4A4 with silu(G) * U fused into the
-    CTA-pair kernel's epilogue (bf16, M > 128, F % 128 == 0) or separate
-    (fp32 output, M <= 128, F = 200, single-CTA kernels)."""
+    with the separate silu kernel; W4A4 with silu(G) * U fused into the GEMM's
+    epilogue for bf16 output and F % 128 == 0 (CTA pairs above 128 tokens,
+    single CTAs up to 128 or when pairs are off), separate otherwise (fp32
+    output, F = 200)."""
     K = 1024
     N = 2 * F
     w = synth.weight_normal(N, K, seed=F + 17, outlier_frac=0.01)
@@ -129,7 +130,7 @@ def test_linear_silu_mul(F):
     saved_cl = nv.nvfp4_get_w4a4_cluster()
     nv.nvfp4_set_crossover(N, K, 40)
     try:
-        for M in (1, 40, 41, 130, 300):
+        for M in (1, 40, 41, 128, 130, 300):
             x = synth.act_student_t(M, K, seed=900 + M)
             X = to_dev(x)
             g, u = _gate_up_refs(x, wref, M > 40)
