@@ -266,12 +266,13 @@ nvfp4_status nvfp4_linear(const void* X, int64_t M, const nvfp4_weight* W, void*
  *   W          in:  quantised [2F, K] weight (N = 2F even)
  *   Y          out: device [M, F] of out_dtype
  *   workspace  nvfp4_workspace_bytes(NVFP4_OP_LINEAR_SILU_MUL, M, 2F, K) bytes
- * Above 128 tokens with bf16 output and F % 128 == 0 the CTA-pair W4A4
- * kernel applies silu(G) * U in its epilogue (CTA 0 of a pair holds 128 gate
- * rows, CTA 1 the matching up rows), so G and U never reach memory.
- * Otherwise the GEMM writes fp32 [rows, 2F] into the workspace, 1024 rows at
- * a time, and a separate kernel applies it; the fused and separate forms
- * evaluate the same binary32 expression.
+ * On the W4A4 branch with bf16 output and F % 128 == 0 the W4A4 kernel
+ * applies silu(G) * U in its epilogue: a tile covers 128 features, its 256
+ * weight rows the 128 gate rows and the matching up rows (split over the two
+ * CTAs of a pair above 128 tokens, in one CTA otherwise), so G and U never
+ * reach memory.  Otherwise the GEMM writes fp32 [rows, 2F] into the
+ * workspace, 1024 rows at a time, and a separate kernel applies it; the fused
+ * and separate forms evaluate the same binary32 expression.
  */
 nvfp4_status nvfp4_linear_silu_mul(const void* X, int64_t M, const nvfp4_weight* W, void* Y,
                                    int out_dtype, void* workspace, size_t workspace_bytes,

@@ -2,9 +2,10 @@
 //
 // For the MLP input projection the quantised weight is [2F, K] (gate rows
 // [0, F), up rows [F, 2F)); nvfp4_linear_silu_mul computes G and U with the
-// linear-layer path and applies silu(g) * u = g / (1 + e^-g) * u.  Above 128
-// tokens the CTA-pair W4A4 kernel applies it in its epilogue; otherwise the
-// GEMM writes fp32 [M, 2F] into the workspace and this kernel applies it.
+// linear-layer path and applies silu(g) * u = g / (1 + e^-g) * u.  On the
+// W4A4 branch (bf16 output, F % 128 == 0) the W4A4 kernel applies it in its
+// epilogue; otherwise the GEMM writes fp32 [M, 2F] into the workspace and
+// this kernel applies it.
 #include "common.cuh"
 #include "kernels.h"
 
