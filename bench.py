@@ -558,9 +558,11 @@ def gate_up_bench(nv, dev, stream):
     """Gated MLP projection silu(X W_gate^T) * (X W_up^T) on the MLP
     gate/up weight [2 x 11008, 4096] (N(0, 0.02^2) x per-row lognormal(0, 0.5)):
     nvfp4_linear_silu_mul against nvfp4_linear on the same weight (Y [M, 2F]),
-    at decode M (W4A16 + the separate silu kernel; 4 weight copies rotate so
-    reads are cold) and prefill M (W4A4 with silu(G) * U fused into the
-    CTA-pair kernel's epilogue)."""
+    4 weight copies rotating so that reads are cold: M <= 8 takes W4A16 and
+    the separate silu kernel, M = 32 / 48 single-CTA W4A4 with silu(G) * U in
+    its epilogue, prefill M the CTA-pair kernel with it in its epilogue.  At
+    prefill M also the separate form (fp32 output: GEMM to fp32 in 1024-row
+    chunks, then the silu kernel) and the fused form on single CTAs."""
     import torch
     bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
     gate_up, _ = synth.mlp_weights()
@@ -599,17 +601,22 @@ def gate_up_bench(nv, dev, stream):
         t2 = timed(lambda i: nv.nvfp4_linear(X, copies[i % 4], out=Y2, workspace=ws2, stream=stream), reps)
         res[str(M)] = {"silu_mul_us": round(t1 * 1e6, 2), "linear_us": round(t2 * 1e6, 2)}
         if M > 64:
-            # the separate form (GEMM to fp32 in 1024-row chunks, then the silu
-            # kernel), which single-CTA W4A4 tiles force
+            # the separate form, which an fp32 output takes
+            Y1f = torch.empty((M, N // 2), dtype=torch.float32, device=dev)
+            t3 = timed(lambda i: nv.nvfp4_linear_silu_mul(X, copies[i % 4], nv.OUT_F32, out=Y1f, workspace=ws1,
+                                                          stream=stream), reps)
+            # the fused form on single CTAs (CTA pairs off)
             saved = nv.nvfp4_get_w4a4_cluster()
             nv.nvfp4_set_w4a4_cluster(1)
             try:
-                t3 = timed(lambda i: nv.nvfp4_linear_silu_mul(X, copies[i % 4], out=Y1, workspace=ws1,
+                t4 = timed(lambda i: nv.nvfp4_linear_silu_mul(X, copies[i % 4], out=Y1, workspace=ws1,
                                                               stream=stream), reps)
             finally:
                 nv.nvfp4_set_w4a4_cluster(saved)
-            res[str(M)]["silu_mul_separate_us"] = round(t3 * 1e6, 2)
+            res[str(M)]["silu_mul_separate_fp32_us"] = round(t3 * 1e6, 2)
+            res[str(M)]["silu_mul_single_cta_us"] = round(t4 * 1e6, 2)
             res[str(M)]["silu_mul_tflops"] = round(2 * M * N * K / t1 / 1e12, 1)
+            del Y1f
         del ws1, ws2, Y1, Y2, X
     return res
 
