@@ -1057,6 +1057,10 @@ def profile_case(which: str, m_decode: int):
         qp = nv.nvfp4_quantize_fos(bf(synth.prefill_weight()), logical_scales=False, choice=False)
         a = nv.nvfp4_quantize_act(bf(synth.prefill_act(2048)))
         nv.nvfp4_gemm_w4a4(a, qp)
+    if which == "w4a4_small":  # single-CTA W4A4 (M <= 128) on the prefill weight
+        qp = nv.nvfp4_quantize_fos(bf(synth.prefill_weight()), logical_scales=False, choice=False)
+        a = nv.nvfp4_quantize_act(bf(synth.prefill_act(m_decode)))
+        nv.nvfp4_gemm_w4a4(a, qp)
     if which == "gate_up":  # the gated MLP projection, fused form, on the gate/up weight [2 x 11008, 4096]
         qg = nv.nvfp4_quantize_fos(bf(synth.mlp_weights()[0]), logical_scales=False, choice=False)
         nv.nvfp4_linear_silu_mul(bf(synth.prefill_act(2048)), qg)
@@ -1086,10 +1090,10 @@ def main():
     ap.add_argument("--cpu-rows-reference", type=int, default=64)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["all", "quant", "w4a16", "w4a4", "gate_up", "qat", "w4a16_any",
-                                                "fp4_rate"],
+    ap.add_argument("--profile-case", choices=["all", "quant", "w4a16", "w4a4", "w4a4_small", "gate_up", "qat",
+                                                "w4a16_any", "fp4_rate"],
                     help="launch each hot kernel once on a small case (for ncu) and exit")
-    ap.add_argument("--profile-m", type=int, default=16, help="decode M of --profile-case")
+    ap.add_argument("--profile-m", type=int, default=16, help="decode M of --profile-case (and M of w4a4_small)")
     args = ap.parse_args()
     if args.profile_case:
         profile_case(args.profile_case, args.profile_m)
