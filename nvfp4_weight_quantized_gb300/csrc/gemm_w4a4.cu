@@ -53,8 +53,10 @@ constexpr int kSfaBytes = (BK / 64) * kScaleTileBytes;    // 2 KB: 4 atoms (one 
 template <int BN>
 struct Cfg {
   // operand stages: 3 for the wide tile, whose epilogue also stages half an
-  // output tile (32 KB) in shared memory for TMA stores; 4 for the narrow one
-  static constexpr int kStages = BN == 256 ? 3 : 4;
+  // output tile (32 KB) in shared memory for TMA stores; 6 for the 128-row
+  // tile (a one-wave weight stream at M <= 128, bound by the copies each CTA
+  // has in flight); 4 for the 64-row one
+  static constexpr int kStages = BN == 256 ? 3 : BN == 128 ? 6 : 4;
   static constexpr int kYStageBytes = BN == 256 ? 2 * BM * 128 : 1024;  // two 128 x 64 bf16 boxes (unused at BN = 64)
   static constexpr int kBBytes = BN * BK / 2;
   static constexpr int kSfbTiles = (BN + 127) / 128;                        // 128-row scale tiles
