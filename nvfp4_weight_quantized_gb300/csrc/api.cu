@@ -29,7 +29,7 @@ std::mutex g_mu;
 // nvfp4_weight_quantized_gb300.tune (sweep M = 1..256, cold weights, weight
 // prefetch on); re-run it to retune.
 std::map<std::pair<int64_t, int64_t>, int64_t> g_crossover = {
-    {{4096, 4096}, 64}, {{11008, 4096}, 24}, {{22016, 4096}, 8}, {{4096, 11008}, 64}};
+    {{4096, 4096}, 64}, {{11008, 4096}, 16}, {{22016, 4096}, 8}, {{4096, 11008}, 64}};
 int64_t g_default_crossover = 48;
 // Largest M that nvfp4_gemm_w4a16 sends to the register-file kernel.
 std::atomic<int64_t> g_w4a16_rf_max_m{64};
